@@ -1,0 +1,253 @@
+/*
+ * rbkv.h - C ABI of librbkv: the data-parallel hot path of a Dynamic SplitFuse
+ * serving pass on one GB300 (sm_103a).
+ *
+ * A pass is composed on the host to a fixed token budget, its new K/V rows are
+ * appended into a blocked (paged) cache, and ragged causal attention is run
+ * for every token of the pass against its sequence's cached keys.
+ *
+ *   DeepSpeed-FastGen paper summary page, "Summary" and idea I3: every forward
+ *     pass holds a fixed token budget; long prompts are cut into chunks over
+ *     several passes, short prompts and generation tokens fill it up.
+ *   FastGen guide, "Paged KV Memory Management": the cache is non-contiguous
+ *     fixed-size blocks reached through block tables, read directly by the
+ *     attention kernels.
+ *   FastGen guide, "Dynamic SplitKV Attention": a decode token's keys are split
+ *     across SMs by sequence length; each split yields a partial output and a
+ *     log-sum-exp, and a small reduction kernel combines them.
+ *   FastGen guide, "The Continuous Batching Dilemma": prompt work is a dense
+ *     contraction for the tensor cores, decode work is bound by HBM.
+ *
+ * Conventions for every call:
+ *  - Nothing is thrown across this ABI.  Every call returns an rbkv_status;
+ *    on error it changes no state and launches nothing, and rbkv_last_error()
+ *    returns a message for the calling thread.
+ *  - Device pointers are plain CUDA device addresses on the current device,
+ *    owned by the caller, contiguous, 16-byte aligned.  Host pointers are
+ *    ordinary process memory.  Streams are CUDA stream handles
+ *    (cudaStream_t); NULL is the legacy default stream.
+ *  - Launches are asynchronous on the given stream.
+ *  - A composer and the passes it made are not thread-safe; use one thread per
+ *    composer at a time.
+ *  - Shapes and element types come from the composer's rbkv_config.  Supported:
+ *    RBKV_BF16 or RBKV_F32 elements, head_dim a multiple of 32 up to 256,
+ *    num_heads_q a multiple of num_heads_kv (at most 64 query heads per KV
+ *    head).
+ *
+ * Layouts (row-major, innermost last):
+ *    Q, O          [T][H_q][D]     element type of the config
+ *    K_new, V_new  [T][H_kv][D]
+ *    K/V cache     [num_blocks][H_kv][B][D]   (separate K and V arrays)
+ *  Token position p of a sequence lives in block table[p / B], slot p % B.
+ *  Query head h reads KV head h / (H_q / H_kv).
+ */
+#ifndef RBKV_H
+#define RBKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RBKV_ABI_VERSION 1
+
+typedef enum {
+  RBKV_OK = 0,
+  RBKV_ERR_INVALID = -1,       /* bad argument, state or sequence id */
+  RBKV_ERR_NO_BLOCKS = -2,     /* block pool too small for the pass; nothing changed */
+  RBKV_ERR_CUDA = -3,          /* a CUDA runtime/driver call failed (message has it) */
+  RBKV_ERR_DEVICE_BOUNDS = -4, /* a kernel met an out-of-range index and skipped it */
+  RBKV_ERR_UNSUPPORTED = -5,   /* shape or type outside what the kernels handle */
+  RBKV_ERR_WORKSPACE = -6,     /* workspace missing or smaller than required */
+  RBKV_ERR_TIMEOUT = -7        /* a bounded device-side wait gave up */
+} rbkv_status;
+
+typedef enum { RBKV_BF16 = 0, RBKV_F32 = 1 } rbkv_dtype;
+
+/* Shape of one attention layer and the size of the block pool. */
+typedef struct {
+  int32_t num_heads_q;
+  int32_t num_heads_kv;
+  int32_t head_dim;
+  int32_t block_size;   /* B, tokens per cache block */
+  int32_t dtype;        /* rbkv_dtype of Q, K, V, O and the caches */
+  int32_t num_blocks;   /* blocks in the pool (ids 0 .. num_blocks-1) */
+} rbkv_config;
+
+/* One request as the caller lists it for a pass.
+ * seen < prompt_len : prefilling; the pass may take a chunk of its prompt.
+ * seen >= prompt_len: decoding; the pass may take its one generation token.
+ * seen must equal the number of tokens the composer has recorded for the id
+ * (0 for an id it has not seen). */
+typedef struct {
+  int64_t seq_id;
+  int32_t prompt_len;
+  int32_t seen;
+} rbkv_seq_state;
+
+typedef struct rbkv_composer rbkv_composer;
+typedef struct rbkv_pass rbkv_pass;
+typedef struct CUstream_st* rbkv_stream;   /* same type as cudaStream_t */
+
+/* Read-only host view of a pass's ragged-batch metadata.  S = num_seqs
+ * scheduled sequences in the caller's list order, T = num_tokens.
+ * Valid until rbkv_pass_destroy. */
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_tokens;
+  int32_t num_block_ids;
+  int32_t block_size;
+  const int64_t* seq_ids;     /* [S] */
+  const int32_t* q_start;     /* [S+1] first pass row of each sequence; q_start[S] = T */
+  const int32_t* n_new;       /* [S] tokens of the sequence in this pass (>= 1) */
+  const int32_t* seen;        /* [S] tokens cached before the pass */
+  const int32_t* ctx;         /* [S] seen + n_new */
+  const int32_t* block_start; /* [S+1] offsets into block_ids */
+  const int32_t* block_ids;   /* block table of sequence s: block_ids[block_start[s] ..] */
+  const int32_t* slot;        /* [T] block_id * B + offset of each pass row's K/V */
+} rbkv_pass_meta;
+
+/* How the attention work of a pass was split (for tests and reports). */
+typedef struct {
+  int32_t num_sms;            /* SMs of the device the plan was made for */
+  int32_t decode_rows;        /* pass rows with one new token (decode path) */
+  int32_t decode_items;       /* (row, kv head, key split) work units */
+  int32_t max_splits;         /* largest number of splits of one (row, kv head) */
+  int32_t split_keys;         /* keys per split used by the plan */
+  int32_t partials;           /* partial outputs written to the workspace */
+  int32_t chunk_rows;         /* pass rows of multi-token prompt chunks */
+  int32_t chunk_tiles;        /* tensor-core tiles (128 query rows, one head) */
+  int32_t generic_items;      /* work units on the CUDA-core path */
+  int32_t fast_decode;        /* 1 if the TMA/tensor-core decode kernel is used */
+  int32_t fast_chunk;         /* 1 if the tcgen05 chunk kernel is used */
+} rbkv_plan_info;
+
+/* Library ABI version (RBKV_ABI_VERSION). */
+int32_t rbkv_abi_version(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* rbkv_last_error(void);
+
+/* ---- composition (host only; FastGen paper summary page, Summary) -------- */
+
+/* Create a composer with an empty pool of cfg->num_blocks blocks.
+ * Errors: RBKV_ERR_INVALID for a bad config, RBKV_ERR_UNSUPPORTED for shapes
+ * the kernels cannot run. */
+rbkv_status rbkv_composer_create(const rbkv_config* cfg, rbkv_composer** out);
+
+/* Free a composer.  Passes it made stay valid and must still be destroyed. */
+void rbkv_composer_destroy(rbkv_composer* c);
+
+/* Compose one pass from n_states requests in list order.
+ * token_budget >= 0: the pass holds min(budget, demand) tokens, demand being
+ *   one token per decoding request plus each prefilling request's remaining
+ *   prompt (capped at max_chunk when max_chunk > 0).
+ * Generation tokens are admitted first, in list order; then each prefilling
+ * request takes min(remaining prompt, max_chunk, remaining budget) in list
+ * order.  Scheduled sequences are laid out in list order.  Each receives the
+ * blocks its new context needs, lowest free block id first.
+ * Errors: RBKV_ERR_INVALID (negative budget, duplicate id, prompt_len < 1,
+ * seen not matching the recorded context), RBKV_ERR_NO_BLOCKS (pool short; no
+ * state changed).  *out receives a new pass (owned by the caller; destroy it
+ * with rbkv_pass_destroy), also for an empty pass. */
+rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t max_chunk,
+                              const rbkv_seq_state* states, int32_t n_states,
+                              rbkv_pass** out);
+
+/* Return every block of seq_id to the pool and forget the sequence.
+ * Errors: RBKV_ERR_INVALID for an unknown id. */
+rbkv_status rbkv_release_seq(rbkv_composer* c, int64_t seq_id);
+
+/* Free blocks in the pool. */
+int32_t rbkv_composer_free_blocks(const rbkv_composer* c);
+
+/* Host view of a pass's metadata (pointers owned by the pass). */
+rbkv_status rbkv_pass_get_meta(const rbkv_pass* p, rbkv_pass_meta* view);
+
+/* Override the key-split length of the decode plan: keys per split, a positive
+ * multiple of 16 (0 = automatic from context lengths and the SM count).  Must
+ * be called before the pass's first device call.  Results do not depend on it
+ * beyond floating-point rounding. */
+rbkv_status rbkv_pass_set_split_keys(rbkv_pass* p, int32_t keys_per_split);
+
+/* Plan summary; makes the plan for the current device if not made yet. */
+rbkv_status rbkv_pass_get_plan(rbkv_pass* p, rbkv_plan_info* info);
+
+/* Plan summary for a hypothetical device with num_sms SMs (host only; the
+ * pass's own plan is not changed).  For inspecting the split planner. */
+rbkv_status rbkv_pass_plan_for_sms(const rbkv_pass* p, int32_t num_sms, rbkv_plan_info* info);
+
+/* Free a pass.  Its device metadata is released in stream order after the last
+ * work launched with it, so the last stream it was used on must still exist. */
+void rbkv_pass_destroy(rbkv_pass* p);
+
+/* ---- device steps ---------------------------------------------------------- */
+
+/* Append the pass's new K and V rows into the caches (FastGen guide, "Paged KV
+ * Memory Management"): for pass row t of sequence s at position p,
+ * k_cache[table_s[p/B]][h][p%B][:] = k_new[t][h][:] (same for V), all h.
+ * k_new, v_new: [T][H_kv][D]; k_cache, v_cache: [num_blocks][H_kv][B][D].
+ * The first device call of a pass uploads its metadata (one host-to-device
+ * copy on `stream`).  A pass is bound to the device current at that call.
+ * Errors: RBKV_ERR_INVALID (null pointer with T > 0, other device),
+ * RBKV_ERR_CUDA. */
+rbkv_status rbkv_kv_append(rbkv_pass* p, const void* k_new, const void* v_new,
+                           void* k_cache, void* v_cache, rbkv_stream stream);
+
+/* Bytes of device workspace rbkv_ragged_attention needs for this pass (fp32
+ * partial outputs and log-sum-exps of split decode rows); 0 when nothing is
+ * split.  Makes the plan for the current device if not made yet. */
+size_t rbkv_attention_workspace_bytes(rbkv_pass* p);
+
+/* Ragged causal attention of every pass row (FastGen guide, "Dynamic SplitKV
+ * Attention" and Step 3's reference operator; exact softmax attention):
+ *   O[t][h][:] = sum_{i<=p} softmax_i(Q[t][h] . K_s[i] / sqrt(D)) V_s[i]
+ * for row t of sequence s at position p, keys read through s's block table
+ * after this pass's append (call rbkv_kv_append first, same stream).
+ * q: [T][H_q][D]; o: [T][H_q][D] (written); caches as above.
+ * workspace: device memory of at least rbkv_attention_workspace_bytes(p)
+ * bytes (may be NULL when that is 0), 256-byte aligned, owned by the caller;
+ * it must not be used by other work until this call's kernels complete.
+ * Errors: RBKV_ERR_INVALID, RBKV_ERR_WORKSPACE, RBKV_ERR_CUDA. */
+rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cache,
+                                  const void* v_cache, void* o, void* workspace,
+                                  size_t workspace_bytes, rbkv_stream stream);
+
+/* Wait for `stream`, then read and clear the pass's device status word:
+ * RBKV_OK, RBKV_ERR_DEVICE_BOUNDS (a kernel met a block id outside the pool and
+ * skipped that access) or RBKV_ERR_TIMEOUT (a bounded wait gave up). */
+rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream);
+
+/* ---- measurement ----------------------------------------------------------- */
+
+/* Kernel kinds for rbkv_profile_read. */
+typedef enum {
+  RBKV_KERNEL_KV_APPEND = 0,
+  RBKV_KERNEL_CHUNK = 1,      /* tcgen05 prompt-chunk attention */
+  RBKV_KERNEL_DECODE = 2,     /* split-KV decode attention (TMA + tensor cores) */
+  RBKV_KERNEL_GENERIC = 3,    /* CUDA-core attention */
+  RBKV_KERNEL_COMBINE = 4,    /* log-sum-exp combine */
+  RBKV_KERNEL_KINDS = 5
+} rbkv_kernel_kind;
+
+/* Kernels this process has launched through the library so far. */
+int64_t rbkv_kernel_launches(void);
+
+/* Turn per-launch CUDA-event timing on (1) or off (0).  While on, every kernel
+ * launch is bracketed by two events recorded on its own stream. */
+void rbkv_profile_enable(int32_t on);
+
+/* Wait for the recorded events and return the summed device time (ms) and the
+ * number of timed launches of one kernel kind since the last reset. */
+rbkv_status rbkv_profile_read(int32_t kind, double* total_ms, int64_t* launches);
+
+/* Forget all recorded launches. */
+void rbkv_profile_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RBKV_H */

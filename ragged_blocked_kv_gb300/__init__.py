@@ -1,0 +1,342 @@
+"""Python binding of librbkv (ctypes; argument marshalling only).
+
+Every step of the pass runs in the library: composition, block allocation and
+split planning in its host C++ code, appending and attention in its sm_103a
+kernels.  This module turns torch tensors into device pointers and streams into
+handles, and raises on a non-OK status.  There is no fallback: if the library
+is missing, importing the names below raises.
+
+    cfg = Config(num_heads_q=32, num_heads_kv=8, head_dim=128, block_size=64,
+                 dtype="bf16", num_blocks=4096)
+    comp = Composer(cfg)
+    p = comp.compose(budget=2048, max_chunk=768, states=[(seq_id, prompt_len, seen), ...])
+    kv_append(p, k_new, v_new, k_cache, v_cache)
+    o = ragged_attention(p, q, k_cache, v_cache)
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from pathlib import Path
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_LIB_PATH = Path(__file__).resolve().parent / "_lib" / "librbkv.so"
+
+OK, ERR_INVALID, ERR_NO_BLOCKS, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_UNSUPPORTED, ERR_WORKSPACE, \
+    ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
+BF16, F32 = 0, 1
+
+
+class RbkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"rbkv status {status}: {message}")
+        self.status = status
+
+
+class NoBlocksError(RbkvError):
+    pass
+
+
+class _Config(C.Structure):
+    _fields_ = [("num_heads_q", C.c_int32), ("num_heads_kv", C.c_int32), ("head_dim", C.c_int32),
+                ("block_size", C.c_int32), ("dtype", C.c_int32), ("num_blocks", C.c_int32)]
+
+
+class _SeqState(C.Structure):
+    _fields_ = [("seq_id", C.c_int64), ("prompt_len", C.c_int32), ("seen", C.c_int32)]
+
+
+class _PassMeta(C.Structure):
+    _fields_ = [("num_seqs", C.c_int32), ("num_tokens", C.c_int32), ("num_block_ids", C.c_int32),
+                ("block_size", C.c_int32),
+                ("seq_ids", C.POINTER(C.c_int64)), ("q_start", C.POINTER(C.c_int32)),
+                ("n_new", C.POINTER(C.c_int32)), ("seen", C.POINTER(C.c_int32)),
+                ("ctx", C.POINTER(C.c_int32)), ("block_start", C.POINTER(C.c_int32)),
+                ("block_ids", C.POINTER(C.c_int32)), ("slot", C.POINTER(C.c_int32))]
+
+
+class _PlanInfo(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "num_sms", "decode_rows", "decode_items", "max_splits", "split_keys", "partials",
+        "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk")]
+
+
+# Every symbol include/rbkv.h declares, with (restype, argtypes).
+_P = C.c_void_p
+SIGNATURES = {
+    "rbkv_abi_version": (C.c_int32, []),
+    "rbkv_last_error": (C.c_char_p, []),
+    "rbkv_composer_create": (C.c_int, [C.POINTER(_Config), C.POINTER(_P)]),
+    "rbkv_composer_destroy": (None, [_P]),
+    "rbkv_compose_pass": (C.c_int, [_P, C.c_int32, C.c_int32, C.POINTER(_SeqState), C.c_int32,
+                                    C.POINTER(_P)]),
+    "rbkv_release_seq": (C.c_int, [_P, C.c_int64]),
+    "rbkv_composer_free_blocks": (C.c_int32, [_P]),
+    "rbkv_pass_get_meta": (C.c_int, [_P, C.POINTER(_PassMeta)]),
+    "rbkv_pass_set_split_keys": (C.c_int, [_P, C.c_int32]),
+    "rbkv_pass_get_plan": (C.c_int, [_P, C.POINTER(_PlanInfo)]),
+    "rbkv_pass_plan_for_sms": (C.c_int, [_P, C.c_int32, C.POINTER(_PlanInfo)]),
+    "rbkv_pass_destroy": (None, [_P]),
+    "rbkv_kv_append": (C.c_int, [_P, _P, _P, _P, _P, _P]),
+    "rbkv_attention_workspace_bytes": (C.c_size_t, [_P]),
+    "rbkv_ragged_attention": (C.c_int, [_P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "rbkv_pass_device_status": (C.c_int, [_P, _P]),
+    "rbkv_kernel_launches": (C.c_int64, []),
+    "rbkv_profile_enable": (None, [C.c_int32]),
+    "rbkv_profile_read": (C.c_int, [C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
+    "rbkv_profile_reset": (None, []),
+}
+
+KERNEL_KINDS = {"kv_append": 0, "chunk": 1, "decode": 2, "generic": 3, "combine": 4}
+
+_lib = None
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded librbkv (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not _LIB_PATH.exists():
+            raise ImportError(
+                f"{_LIB_PATH} is missing; build it with `python -m ragged_blocked_kv_gb300.build` "
+                "(there is no fallback implementation)")
+        L = C.CDLL(str(_LIB_PATH))
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != OK:
+        msg = lib().rbkv_last_error().decode(errors="replace")
+        if status == ERR_NO_BLOCKS:
+            raise NoBlocksError(status, msg)
+        raise RbkvError(status, msg)
+
+
+@dataclass(frozen=True)
+class Config:
+    num_heads_q: int
+    num_heads_kv: int
+    head_dim: int
+    block_size: int
+    dtype: str          # "bf16" or "f32"
+    num_blocks: int
+
+    def _c(self) -> _Config:
+        return _Config(self.num_heads_q, self.num_heads_kv, self.head_dim, self.block_size,
+                       BF16 if self.dtype == "bf16" else F32, self.num_blocks)
+
+    @property
+    def torch_dtype(self):
+        import torch
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def cache_shape(self) -> Tuple[int, int, int, int]:
+        return (self.num_blocks, self.num_heads_kv, self.block_size, self.head_dim)
+
+
+@dataclass
+class PassMeta:
+    seq_ids: np.ndarray
+    q_start: np.ndarray
+    n_new: np.ndarray
+    seen: np.ndarray
+    ctx: np.ndarray
+    block_start: np.ndarray
+    block_ids: np.ndarray
+    slot: np.ndarray
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q_start[-1])
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seq_ids)
+
+
+def _arr(ptr, n, dtype):
+    if n == 0:
+        return np.zeros(0, dtype)
+    return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dtype, copy=True)
+
+
+class Pass:
+    """One composed pass (owns its library handle)."""
+
+    def __init__(self, handle: int, config: Config):
+        self._h = _P(handle)
+        self.config = config
+        m = _PassMeta()
+        _check(lib().rbkv_pass_get_meta(self._h, C.byref(m)))
+        S, T = m.num_seqs, m.num_tokens
+        self.meta = PassMeta(_arr(m.seq_ids, S, np.int64), _arr(m.q_start, S + 1, np.int32),
+                             _arr(m.n_new, S, np.int32), _arr(m.seen, S, np.int32),
+                             _arr(m.ctx, S, np.int32), _arr(m.block_start, S + 1, np.int32),
+                             _arr(m.block_ids, m.num_block_ids, np.int32),
+                             _arr(m.slot, T, np.int32))
+
+    @property
+    def num_tokens(self) -> int:
+        return self.meta.num_tokens
+
+    def set_split_keys(self, keys: int) -> None:
+        _check(lib().rbkv_pass_set_split_keys(self._h, int(keys)))
+
+    def plan(self) -> dict:
+        info = _PlanInfo()
+        _check(lib().rbkv_pass_get_plan(self._h, C.byref(info)))
+        return {n: getattr(info, n) for n, _ in _PlanInfo._fields_}
+
+    def plan_for_sms(self, num_sms: int) -> dict:
+        info = _PlanInfo()
+        _check(lib().rbkv_pass_plan_for_sms(self._h, int(num_sms), C.byref(info)))
+        return {n: getattr(info, n) for n, _ in _PlanInfo._fields_}
+
+    def workspace_bytes(self) -> int:
+        return int(lib().rbkv_attention_workspace_bytes(self._h))
+
+    def device_status(self, stream=None) -> None:
+        _check(lib().rbkv_pass_device_status(self._h, _stream(stream)))
+
+    def destroy(self) -> None:
+        if self._h:
+            lib().rbkv_pass_destroy(self._h)
+            self._h = _P(None)
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class Composer:
+    """Dynamic SplitFuse composer and block pool of one cache layout."""
+
+    def __init__(self, config: Config):
+        self.config = config
+        h = _P()
+        cfg = config._c()
+        _check(lib().rbkv_composer_create(C.byref(cfg), C.byref(h)))
+        self._h = h
+
+    def compose(self, budget: int, max_chunk: int,
+                states: Sequence[Tuple[int, int, int]]) -> Pass:
+        arr = (_SeqState * max(1, len(states)))()
+        for i, (sid, plen, seen) in enumerate(states):
+            arr[i] = _SeqState(int(sid), int(plen), int(seen))
+        out = _P()
+        _check(lib().rbkv_compose_pass(self._h, int(budget), int(max_chunk), arr, len(states),
+                                       C.byref(out)))
+        return Pass(out.value, self.config)
+
+    def release(self, seq_id: int) -> None:
+        _check(lib().rbkv_release_seq(self._h, int(seq_id)))
+
+    def free_blocks(self) -> int:
+        return int(lib().rbkv_composer_free_blocks(self._h))
+
+    def close(self) -> None:
+        if self._h:
+            lib().rbkv_composer_destroy(self._h)
+            self._h = _P(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return _P(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return _P(stream)
+    return _P(stream.cuda_stream)
+
+
+def _dev_ptr(t, name, dtype, shape):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return _P(t.data_ptr())
+
+
+def kv_append(p: Pass, k_new, v_new, k_cache, v_cache, stream=None) -> None:
+    """Scatter the pass's new K/V rows into the blocked caches (in place)."""
+    c = p.config
+    T = p.num_tokens
+    dt = c.torch_dtype
+    row = (T, c.num_heads_kv, c.head_dim)
+    _check(lib().rbkv_kv_append(p._h, _dev_ptr(k_new, "k_new", dt, row),
+                                _dev_ptr(v_new, "v_new", dt, row),
+                                _dev_ptr(k_cache, "k_cache", dt, c.cache_shape()),
+                                _dev_ptr(v_cache, "v_cache", dt, c.cache_shape()),
+                                _stream(stream)))
+
+
+def ragged_attention(p: Pass, q, k_cache, v_cache, o=None, workspace=None, stream=None):
+    """Ragged causal attention of every pass row; returns O ``[T][H_q][D]``."""
+    import torch
+    c = p.config
+    T = p.num_tokens
+    dt = c.torch_dtype
+    qshape = (T, c.num_heads_q, c.head_dim)
+    if o is None:
+        o = torch.empty(qshape, dtype=dt, device=q.device)
+    need = p.workspace_bytes()
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _P(workspace.data_ptr()) if workspace is not None else _P(None)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().rbkv_ragged_attention(p._h, _dev_ptr(q, "q", dt, qshape),
+                                       _dev_ptr(k_cache, "k_cache", dt, c.cache_shape()),
+                                       _dev_ptr(v_cache, "v_cache", dt, c.cache_shape()),
+                                       _dev_ptr(o, "o", dt, qshape), ws_ptr, ws_bytes,
+                                       _stream(stream)))
+    return o
+
+
+def kernel_launches() -> int:
+    """Kernels launched through the library by this process so far."""
+    return int(lib().rbkv_kernel_launches())
+
+
+def profile_enable(on: bool = True) -> None:
+    lib().rbkv_profile_enable(1 if on else 0)
+
+
+def profile_reset() -> None:
+    lib().rbkv_profile_reset()
+
+
+def profile_read() -> dict:
+    """{kernel: (total_ms, launches)} of the launches timed since the last reset."""
+    out = {}
+    for name, k in KERNEL_KINDS.items():
+        ms, n = C.c_double(), C.c_int64()
+        _check(lib().rbkv_profile_read(k, C.byref(ms), C.byref(n)))
+        out[name] = (ms.value, n.value)
+    return out
+
+
+__all__ = ["kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+           "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

@@ -1,0 +1,702 @@
+// Host side of librbkv: the Dynamic SplitFuse composer, the block pool, the
+// split-KV planner, the metadata packer and the C ABI entry points.
+//
+// Composition follows the DeepSpeed-FastGen paper summary page ("Summary",
+// idea I3): a pass holds a fixed token budget; long prompts are chunked over
+// passes; generation tokens and short prompts top the pass up.  Split planning
+// follows the FastGen guide ("Dynamic SplitKV Attention"): the number of key
+// splits of a decode row grows with its context so that every SM has work.
+#include "rbkv.h"
+#include "rbkv_internal.h"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+using namespace rbkv;
+
+namespace {
+
+thread_local std::string g_err;
+
+rbkv_status fail(rbkv_status st, const std::string& msg) {
+  g_err = msg;
+  return st;
+}
+
+rbkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RBKV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+constexpr int32_t kMaxTokens = 1 << 30;
+
+// ---- block pool: one bit per block, set = free; lowest free id first --------
+class BlockPool {
+ public:
+  explicit BlockPool(int32_t n) : n_(n), nfree_(n), hint_(0) {
+    words_.assign((size_t)(n + 63) / 64, ~0ull);
+    if (n % 64) words_.back() = (1ull << (n % 64)) - 1;
+    if (n == 0) words_.clear();
+  }
+  int32_t free_count() const { return nfree_; }
+  int32_t take_lowest() {
+    for (size_t w = hint_; w < words_.size(); ++w) {
+      if (words_[w]) {
+        int bit = __builtin_ctzll(words_[w]);
+        words_[w] &= ~(1ull << bit);
+        hint_ = w;
+        --nfree_;
+        return (int32_t)(w * 64 + bit);
+      }
+    }
+    return -1;
+  }
+  void give_back(int32_t b) {
+    words_[(size_t)b / 64] |= 1ull << (b % 64);
+    hint_ = std::min(hint_, (size_t)b / 64);
+    ++nfree_;
+  }
+
+ private:
+  std::vector<uint64_t> words_;
+  int32_t n_, nfree_;
+  size_t hint_;
+};
+
+// ---- pinned staging buffers for the per-pass metadata upload ---------------
+// A buffer goes back to the pool as soon as its copy is enqueued; it is reused
+// only once the event recorded after that copy has completed, so no call ever
+// blocks on it.
+struct PinnedBuf {
+  void* ptr = nullptr;
+  size_t cap = 0;
+  cudaEvent_t ev = nullptr;
+};
+
+class PinnedPool {
+ public:
+  ~PinnedPool() {
+    for (auto& b : free_) {
+      if (b.ev) { cudaEventSynchronize(b.ev); cudaEventDestroy(b.ev); }
+      if (b.ptr) cudaFreeHost(b.ptr);
+    }
+  }
+  cudaError_t acquire(size_t bytes, PinnedBuf& out) {
+    for (size_t i = 0; i < free_.size(); ++i) {
+      if (free_[i].cap >= bytes && cudaEventQuery(free_[i].ev) == cudaSuccess) {
+        out = free_[i];
+        free_.erase(free_.begin() + i);
+        return cudaSuccess;
+      }
+    }
+    (void)cudaGetLastError();  // cudaEventQuery may have left cudaErrorNotReady
+    size_t cap = 4096;
+    while (cap < bytes) cap *= 2;
+    PinnedBuf b;
+    cudaError_t e = cudaHostAlloc(&b.ptr, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return e;
+    e = cudaEventCreateWithFlags(&b.ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) { cudaFreeHost(b.ptr); return e; }
+    b.cap = cap;
+    out = b;
+    return cudaSuccess;
+  }
+  void release(const PinnedBuf& b) {
+    free_.push_back(b);
+    if (free_.size() > 64) {  // keep the pool small: drop the oldest idle buffer
+      PinnedBuf old = free_.front();
+      cudaEventSynchronize(old.ev);
+      cudaEventDestroy(old.ev);
+      cudaFreeHost(old.ptr);
+      free_.erase(free_.begin());
+    }
+  }
+
+ private:
+  std::vector<PinnedBuf> free_;
+};
+
+// ---- launch counting and optional per-launch event timing -------------------
+std::atomic<int64_t> g_launches{0};
+
+struct Profiler {
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> rec[RBKV_KERNEL_KINDS];
+  std::vector<cudaEvent_t> spare;
+  cudaEvent_t get() {
+    cudaEvent_t e = nullptr;
+    if (!spare.empty()) { e = spare.back(); spare.pop_back(); return e; }
+    cudaEventCreate(&e);
+    return e;
+  }
+  void reset() {
+    for (auto& r : rec) {
+      for (auto& pr : r) { spare.push_back(pr.first); spare.push_back(pr.second); }
+      r.clear();
+    }
+  }
+};
+Profiler g_prof;
+
+template <class F>
+cudaError_t launch_counted(int kind, cudaStream_t st, F&& f) {
+  cudaEvent_t a = nullptr;
+  if (g_prof.on) { a = g_prof.get(); cudaEventRecord(a, st); }
+  cudaError_t e = f();
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_prof.on) {
+    cudaEvent_t b = g_prof.get();
+    cudaEventRecord(b, st);
+    g_prof.rec[kind].push_back({a, b});
+  }
+  return e;
+}
+
+int32_t ceil_div(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
+int32_t round_up(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b * b); }
+
+// ---- the attention plan of one pass -----------------------------------------
+struct Plan {
+  rbkv_plan_info info{};
+  std::vector<WorkItem> decode, generic;
+  std::vector<ChunkTile> chunk;
+  std::vector<CombineRow> combine;
+  int32_t n_parts = 0;
+  int32_t decode_grid = 0;
+};
+
+}  // namespace
+
+struct rbkv_composer {
+  rbkv_config cfg;
+  BlockPool pool;
+  std::unordered_map<int64_t, std::vector<int32_t>> held;
+  std::unordered_map<int64_t, int32_t> tokens;
+  std::shared_ptr<PinnedPool> pinned;
+  explicit rbkv_composer(const rbkv_config& c)
+      : cfg(c), pool(c.num_blocks), pinned(std::make_shared<PinnedPool>()) {}
+};
+
+struct rbkv_pass {
+  rbkv_config cfg;
+  std::shared_ptr<PinnedPool> pinned;
+  std::vector<int64_t> seq_ids;
+  std::vector<int32_t> q_start{0}, n_new, seen, ctx, block_start{0}, block_ids, slot;
+  int32_t split_keys = 0;
+  // plan, made once for the device of the first device call
+  bool planned = false;
+  int device = -1;
+  Plan plan;
+  // device copy of the metadata
+  void* dev = nullptr;
+  size_t dev_bytes = 0;
+  cudaStream_t upload_stream = nullptr;
+  cudaStream_t last_stream = nullptr;
+  cudaEvent_t upload_ev = nullptr;
+  DevPass dp{};
+};
+
+namespace {
+
+ShapeInfo shape_of(const rbkv_config& c) {
+  ShapeInfo s;
+  s.H_q = c.num_heads_q;
+  s.H_kv = c.num_heads_kv;
+  s.D = c.head_dim;
+  s.B = c.block_size;
+  s.g = c.num_heads_q / c.num_heads_kv;
+  s.dtype = c.dtype;
+  s.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+  return s;
+}
+
+// Split the keys [0, n_keys) of one (row, kv head) into near-equal pieces of
+// at most `split` keys, each a multiple of `gran` except the last.
+void split_keys(int32_t n_keys, int32_t split, int32_t gran, std::vector<int32_t>& bounds) {
+  bounds.clear();
+  int32_t nsplit = std::max(1, ceil_div(n_keys, split));
+  int32_t piece = round_up(ceil_div(n_keys, nsplit), gran);
+  for (int32_t k = 0; k < n_keys; k += piece) bounds.push_back(k);
+  bounds.push_back(n_keys);
+}
+
+// Reorder `items` (sorted longest first) so that a persistent grid of G CTAs,
+// CTA c taking items c, c+G, c+2G, ..., receives them in snake order: round r
+// hands sorted items r*G .. r*G+G-1 to CTAs 0..G-1 on even rounds and to
+// G-1..0 on odd rounds.  Long and short units even out across CTAs.
+void snake_order(std::vector<WorkItem>& items, int32_t G) {
+  std::vector<WorkItem> out(items.size());
+  for (size_t i = 0; i < items.size(); ++i) {
+    size_t r = i / G, c = i % G;
+    size_t base = r * G;
+    size_t width = std::min((size_t)G, items.size() - base);
+    size_t src = (r % 2 == 0) ? base + c : base + (width - 1 - c);
+    out[i] = items[src];
+  }
+  items.swap(out);
+}
+
+Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
+  Plan pl;
+  ShapeInfo s = shape_of(p.cfg);
+  const bool fast_decode = decode_fast_supported(s);
+  const bool fast_chunk = chunk_fast_supported(s);
+  const int32_t gran = fast_decode ? kDecodeTileKeys : 16;
+  const int32_t S = (int32_t)p.seq_ids.size();
+
+  int64_t decode_work = 0;
+  int32_t decode_rows = 0, chunk_rows = 0;
+  for (int32_t i = 0; i < S; ++i) {
+    if (p.n_new[i] == 1) { decode_work += (int64_t)p.ctx[i] * s.H_kv; ++decode_rows; }
+    else chunk_rows += p.n_new[i];
+  }
+  int32_t split;
+  if (p.split_keys > 0) {
+    split = round_up(p.split_keys, gran);
+  } else {
+    // about four waves of equal-size units over every CTA slot of the GPU,
+    // never shorter than 512 keys (shorter units cost more in partial-output
+    // traffic than they gain in balance)
+    int64_t slots = (int64_t)std::max(1, num_sms) * kDecodeCtasPerSm;
+    int64_t target = (decode_work + slots * 4 - 1) / (slots * 4);
+    split = std::max<int32_t>(512, round_up(std::max<int64_t>(target, 1), gran));
+  }
+
+  std::vector<int32_t> bounds;
+  std::vector<WorkItem> decode, generic;
+  int32_t max_splits = 0;
+  auto add_row = [&](int32_t row, int32_t n_keys, int32_t table_off, std::vector<WorkItem>& dst) {
+    for (int32_t h = 0; h < s.H_kv; ++h) {
+      split_keys(n_keys, split, gran, bounds);
+      int32_t ns = (int32_t)bounds.size() - 1;
+      max_splits = std::max(max_splits, ns);
+      int32_t part0 = -1;
+      if (ns > 1) {
+        part0 = pl.n_parts;
+        pl.n_parts += ns;
+        pl.combine.push_back(CombineRow{row, h, part0, ns});
+      }
+      for (int32_t k = 0; k < ns; ++k)
+        dst.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1, table_off});
+    }
+  };
+  for (int32_t i = 0; i < S; ++i) {
+    if (p.n_new[i] == 1) {
+      add_row(p.q_start[i], p.ctx[i], p.block_start[i], fast_decode ? decode : generic);
+    } else if (fast_chunk) {
+      for (int32_t r = 0; r < p.n_new[i]; r += kChunkTileRows) {
+        int32_t n = std::min(kChunkTileRows, p.n_new[i] - r);
+        pl.chunk.push_back(ChunkTile{p.block_start[i], p.q_start[i] + r, n, p.seen[i] + r});
+      }
+    } else {
+      for (int32_t j = 0; j < p.n_new[i]; ++j)
+        add_row(p.q_start[i] + j, p.seen[i] + j + 1, p.block_start[i], generic);
+    }
+  }
+  auto longer = [](const WorkItem& a, const WorkItem& b) {
+    return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+  };
+  std::stable_sort(decode.begin(), decode.end(), longer);
+  std::stable_sort(generic.begin(), generic.end(), longer);
+  int32_t grid = (int32_t)std::min<int64_t>((int64_t)decode.size(),
+                                            (int64_t)std::max(1, num_sms) * kDecodeCtasPerSm);
+  if (grid > 0) snake_order(decode, grid);
+  pl.decode_grid = grid;
+  pl.decode.swap(decode);
+  pl.generic.swap(generic);
+
+  rbkv_plan_info& in = pl.info;
+  in.num_sms = num_sms;
+  in.decode_rows = decode_rows;
+  in.decode_items = fast_decode ? (int32_t)pl.decode.size() : 0;
+  in.max_splits = max_splits;
+  in.split_keys = split;
+  in.partials = pl.n_parts;
+  in.chunk_rows = chunk_rows;
+  in.chunk_tiles = (int32_t)pl.chunk.size();
+  in.generic_items = (int32_t)pl.generic.size();
+  in.fast_decode = fast_decode ? 1 : 0;
+  in.fast_chunk = fast_chunk ? 1 : 0;
+  return pl;
+}
+
+size_t workspace_bytes_of(const rbkv_pass& p) {
+  if (p.plan.n_parts == 0) return 0;
+  ShapeInfo s = shape_of(p.cfg);
+  return partial_o_bytes(p.plan.n_parts, s) + partial_lse_bytes(p.plan.n_parts, s);
+}
+
+rbkv_status ensure_plan(rbkv_pass* p) {
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->planned) {
+    if (dev != p->device)
+      return fail(RBKV_ERR_INVALID, "pass was bound to another device by its first device call");
+    return RBKV_OK;
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  p->plan = make_plan(*p, sms);
+  p->device = dev;
+  p->planned = true;
+  return RBKV_OK;
+}
+
+template <class T>
+void put(std::vector<int32_t>& w, size_t& off, const std::vector<T>& v) {
+  static_assert(sizeof(T) % 4 == 0, "int32 packing");
+  size_t words = v.size() * sizeof(T) / 4;
+  off = w.size();
+  w.resize(off + words);
+  if (words) std::memcpy(w.data() + off, v.data(), words * 4);
+  while (w.size() % 4) w.push_back(0);  // 16-byte aligned sections
+}
+
+// Plan (if needed), pack and upload the metadata on `st`; order `st` after
+// the upload when it is another stream.
+rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
+  rbkv_status rs = ensure_plan(p);
+  if (rs != RBKV_OK) return rs;
+  if (!p->dev) {
+    const Plan& pl = p->plan;
+    std::vector<int32_t> w(4, 0);  // status word + padding
+    size_t o_slot, o_blocks, o_dec, o_gen, o_chunk, o_comb;
+    put(w, o_slot, p->slot);
+    put(w, o_blocks, p->block_ids);
+    put(w, o_dec, pl.decode);
+    put(w, o_gen, pl.generic);
+    put(w, o_chunk, pl.chunk);
+    put(w, o_comb, pl.combine);
+    size_t bytes = w.size() * 4;
+    PinnedBuf pin;
+    cudaError_t e = p->pinned->acquire(bytes, pin);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+    std::memcpy(pin.ptr, w.data(), bytes);
+    void* dev = nullptr;
+    e = cudaMallocAsync(&dev, bytes, st);
+    if (e != cudaSuccess) { p->pinned->release(pin); return cuda_fail(e, "cudaMallocAsync"); }
+    e = cudaMemcpyAsync(dev, pin.ptr, bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(pin.ev, st);
+    p->pinned->release(pin);
+    if (e != cudaSuccess) { cudaFreeAsync(dev, st); return cuda_fail(e, "metadata upload"); }
+    e = cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(p->upload_ev, st);
+    if (e != cudaSuccess) { cudaFreeAsync(dev, st); return cuda_fail(e, "upload event"); }
+    p->dev = dev;
+    p->dev_bytes = bytes;
+    p->upload_stream = st;
+    int32_t* base = (int32_t*)dev;
+    DevPass& dp = p->dp;
+    dp.status = base;
+    dp.slot = base + o_slot;
+    dp.block_ids = base + o_blocks;
+    dp.decode_items = (const WorkItem*)(base + o_dec);
+    dp.generic_items = (const WorkItem*)(base + o_gen);
+    dp.chunk_tiles = (const ChunkTile*)(base + o_chunk);
+    dp.combine_rows = (const CombineRow*)(base + o_comb);
+    dp.num_tokens = (int32_t)p->slot.size();
+    dp.n_decode = (int32_t)pl.decode.size();
+    dp.n_generic = (int32_t)pl.generic.size();
+    dp.n_chunk = (int32_t)pl.chunk.size();
+    dp.n_combine = (int32_t)pl.combine.size();
+    dp.n_parts = pl.n_parts;
+    dp.num_blocks = p->cfg.num_blocks;
+    dp.decode_grid = pl.decode_grid;
+  } else if (st != p->upload_stream) {
+    cudaError_t e = cudaStreamWaitEvent(st, p->upload_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  p->last_stream = st;
+  return RBKV_OK;
+}
+
+rbkv_status check_config(const rbkv_config* c) {
+  if (!c) return fail(RBKV_ERR_INVALID, "config is NULL");
+  if (c->num_heads_q < 1 || c->num_heads_kv < 1 || c->num_heads_q % c->num_heads_kv)
+    return fail(RBKV_ERR_INVALID, "num_heads_q must be a positive multiple of num_heads_kv");
+  if (c->block_size < 1 || c->num_blocks < 0)
+    return fail(RBKV_ERR_INVALID, "block_size must be >= 1 and num_blocks >= 0");
+  if ((int64_t)c->num_blocks * c->block_size >= (int64_t)1 << 31)
+    return fail(RBKV_ERR_INVALID, "num_blocks * block_size must fit in int32");
+  if (c->dtype != RBKV_BF16 && c->dtype != RBKV_F32)
+    return fail(RBKV_ERR_INVALID, "dtype must be RBKV_BF16 or RBKV_F32");
+  if (c->head_dim < 32 || c->head_dim > 256 || c->head_dim % 32)
+    return fail(RBKV_ERR_UNSUPPORTED, "head_dim must be a multiple of 32 in [32, 256]");
+  if (c->num_heads_q / c->num_heads_kv > 64)
+    return fail(RBKV_ERR_UNSUPPORTED, "at most 64 query heads per KV head");
+  return RBKV_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+int32_t rbkv_abi_version(void) { return RBKV_ABI_VERSION; }
+
+const char* rbkv_last_error(void) { return g_err.c_str(); }
+
+rbkv_status rbkv_composer_create(const rbkv_config* cfg, rbkv_composer** out) {
+  if (!out) return fail(RBKV_ERR_INVALID, "out is NULL");
+  rbkv_status st = check_config(cfg);
+  if (st != RBKV_OK) return st;
+  try {
+    *out = new rbkv_composer(*cfg);
+  } catch (...) {
+    return fail(RBKV_ERR_INVALID, "out of host memory");
+  }
+  return RBKV_OK;
+}
+
+void rbkv_composer_destroy(rbkv_composer* c) { delete c; }
+
+int32_t rbkv_composer_free_blocks(const rbkv_composer* c) { return c ? c->pool.free_count() : 0; }
+
+rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t max_chunk,
+                              const rbkv_seq_state* states, int32_t n_states, rbkv_pass** out) {
+  if (!c || !out) return fail(RBKV_ERR_INVALID, "composer or out is NULL");
+  if (token_budget < 0) return fail(RBKV_ERR_INVALID, "token budget must be >= 0");
+  if (n_states < 0 || (n_states > 0 && !states))
+    return fail(RBKV_ERR_INVALID, "states must hold n_states entries");
+  try {
+    std::unordered_set<int64_t> ids;
+    ids.reserve((size_t)n_states * 2);
+    for (int32_t i = 0; i < n_states; ++i) {
+      const rbkv_seq_state& q = states[i];
+      if (!ids.insert(q.seq_id).second)
+        return fail(RBKV_ERR_INVALID, "sequence " + std::to_string(q.seq_id) + " listed twice");
+      if (q.prompt_len < 1 || q.prompt_len > kMaxTokens || q.seen < 0 || q.seen > kMaxTokens)
+        return fail(RBKV_ERR_INVALID, "sequence " + std::to_string(q.seq_id) +
+                                          ": prompt_len must be in [1, 2^30] and seen in [0, 2^30]");
+      auto it = c->tokens.find(q.seq_id);
+      int32_t have = it == c->tokens.end() ? 0 : it->second;
+      if (q.seen != have)
+        return fail(RBKV_ERR_INVALID, "sequence " + std::to_string(q.seq_id) + ": seen=" +
+                                          std::to_string(q.seen) + " but the cache holds " +
+                                          std::to_string(have) + " tokens");
+    }
+    // generation tokens first, then prompt chunks; both in list order
+    std::vector<int32_t> take((size_t)n_states, 0);
+    int32_t left = token_budget;
+    for (int32_t i = 0; i < n_states && left > 0; ++i)
+      if (states[i].seen >= states[i].prompt_len) { take[i] = 1; --left; }
+    for (int32_t i = 0; i < n_states; ++i) {
+      const rbkv_seq_state& q = states[i];
+      if (q.seen >= q.prompt_len) continue;
+      int32_t n = q.prompt_len - q.seen;
+      if (max_chunk > 0 && n > max_chunk) n = max_chunk;
+      if (n > left) n = left;
+      take[i] = n;
+      left -= n;
+    }
+    // blocks: all or nothing
+    const int32_t B = c->cfg.block_size;
+    int64_t need_total = 0;
+    std::vector<int32_t> need((size_t)n_states, 0);
+    for (int32_t i = 0; i < n_states; ++i) {
+      if (!take[i]) continue;
+      auto it = c->held.find(states[i].seq_id);
+      int32_t have = it == c->held.end() ? 0 : (int32_t)it->second.size();
+      need[i] = std::max(0, ceil_div((int64_t)states[i].seen + take[i], B) - have);
+      need_total += need[i];
+    }
+    if (need_total > c->pool.free_count())
+      return fail(RBKV_ERR_NO_BLOCKS, "pass needs " + std::to_string(need_total) +
+                                          " new blocks, " + std::to_string(c->pool.free_count()) +
+                                          " free");
+    std::unique_ptr<rbkv_pass> p(new rbkv_pass());
+    p->cfg = c->cfg;
+    p->pinned = c->pinned;
+    for (int32_t i = 0; i < n_states; ++i) {
+      if (!take[i]) continue;
+      const rbkv_seq_state& q = states[i];
+      std::vector<int32_t>& blocks = c->held[q.seq_id];
+      for (int32_t k = 0; k < need[i]; ++k) blocks.push_back(c->pool.take_lowest());
+      const int32_t n = take[i], seen = q.seen, ctx = seen + n;
+      c->tokens[q.seq_id] = ctx;
+      p->seq_ids.push_back(q.seq_id);
+      p->n_new.push_back(n);
+      p->seen.push_back(seen);
+      p->ctx.push_back(ctx);
+      p->q_start.push_back(p->q_start.back() + n);
+      const int32_t nb = ceil_div(ctx, B);
+      p->block_ids.insert(p->block_ids.end(), blocks.begin(), blocks.begin() + nb);
+      p->block_start.push_back(p->block_start.back() + nb);
+      for (int32_t pos = seen; pos < ctx; ++pos)
+        p->slot.push_back(blocks[pos / B] * B + pos % B);
+    }
+    *out = p.release();
+  } catch (...) {
+    return fail(RBKV_ERR_INVALID, "out of host memory");
+  }
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_release_seq(rbkv_composer* c, int64_t seq_id) {
+  if (!c) return fail(RBKV_ERR_INVALID, "composer is NULL");
+  auto th = c->tokens.find(seq_id);
+  auto hb = c->held.find(seq_id);
+  if (th == c->tokens.end() && hb == c->held.end())
+    return fail(RBKV_ERR_INVALID, "unknown sequence " + std::to_string(seq_id));
+  if (hb != c->held.end()) {
+    for (int32_t b : hb->second) c->pool.give_back(b);
+    c->held.erase(hb);
+  }
+  if (th != c->tokens.end()) c->tokens.erase(th);
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_pass_get_meta(const rbkv_pass* p, rbkv_pass_meta* v) {
+  if (!p || !v) return fail(RBKV_ERR_INVALID, "pass or view is NULL");
+  v->num_seqs = (int32_t)p->seq_ids.size();
+  v->num_tokens = (int32_t)p->slot.size();
+  v->num_block_ids = (int32_t)p->block_ids.size();
+  v->block_size = p->cfg.block_size;
+  v->seq_ids = p->seq_ids.data();
+  v->q_start = p->q_start.data();
+  v->n_new = p->n_new.data();
+  v->seen = p->seen.data();
+  v->ctx = p->ctx.data();
+  v->block_start = p->block_start.data();
+  v->block_ids = p->block_ids.data();
+  v->slot = p->slot.data();
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_pass_set_split_keys(rbkv_pass* p, int32_t keys) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (keys < 0 || keys % 16) return fail(RBKV_ERR_INVALID, "keys per split must be a multiple of 16");
+  if (p->planned) return fail(RBKV_ERR_INVALID, "the pass was already planned by a device call");
+  p->split_keys = keys;
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_pass_get_plan(rbkv_pass* p, rbkv_plan_info* info) {
+  if (!p || !info) return fail(RBKV_ERR_INVALID, "pass or info is NULL");
+  rbkv_status st = ensure_plan(p);
+  if (st != RBKV_OK) return st;
+  *info = p->plan.info;
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_pass_plan_for_sms(const rbkv_pass* p, int32_t num_sms, rbkv_plan_info* info) {
+  if (!p || !info || num_sms < 1) return fail(RBKV_ERR_INVALID, "bad arguments");
+  *info = make_plan(*p, num_sms).info;
+  return RBKV_OK;
+}
+
+void rbkv_pass_destroy(rbkv_pass* p) {
+  if (!p) return;
+  if (p->dev) cudaFreeAsync(p->dev, p->last_stream);
+  if (p->upload_ev) cudaEventDestroy(p->upload_ev);
+  delete p;
+}
+
+rbkv_status rbkv_kv_append(rbkv_pass* p, const void* k_new, const void* v_new, void* k_cache,
+                           void* v_cache, rbkv_stream stream) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (p->slot.empty()) return RBKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache) return fail(RBKV_ERR_INVALID, "NULL tensor");
+  cudaStream_t st = (cudaStream_t)stream;
+  rbkv_status rs = ensure_device(p, st);
+  if (rs != RBKV_OK) return rs;
+  const ShapeInfo s = shape_of(p->cfg);
+  cudaError_t e = launch_counted(RBKV_KERNEL_KV_APPEND, st, [&] {
+    return launch_kv_append(p->dp, s, k_new, v_new, k_cache, v_cache, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return RBKV_OK;
+}
+
+size_t rbkv_attention_workspace_bytes(rbkv_pass* p) {
+  if (!p || ensure_plan(p) != RBKV_OK) return 0;
+  return workspace_bytes_of(*p);
+}
+
+rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cache,
+                                  const void* v_cache, void* o, void* workspace,
+                                  size_t workspace_bytes, rbkv_stream stream) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (p->slot.empty()) return RBKV_OK;
+  if (!q || !k_cache || !v_cache || !o) return fail(RBKV_ERR_INVALID, "NULL tensor");
+  rbkv_status rs = ensure_plan(p);
+  if (rs != RBKV_OK) return rs;
+  const size_t need = workspace_bytes_of(*p);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(RBKV_ERR_WORKSPACE, "workspace needs " + std::to_string(need) + " bytes");
+  if (need > 0 && ((uintptr_t)workspace % 256))
+    return fail(RBKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  rs = ensure_device(p, st);
+  if (rs != RBKV_OK) return rs;
+  const ShapeInfo s = shape_of(p->cfg);
+  float* part_o = (float*)workspace;
+  float* part_lse = need ? (float*)((char*)workspace + partial_o_bytes(p->plan.n_parts, s)) : nullptr;
+  const DevPass& dp = p->dp;
+  cudaError_t e = cudaSuccess;
+  if (dp.n_chunk)
+    e = launch_counted(RBKV_KERNEL_CHUNK, st,
+                       [&] { return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, st); });
+  if (e == cudaSuccess && dp.n_decode)
+    e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
+      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    });
+  if (e == cudaSuccess && dp.n_generic)
+    e = launch_counted(RBKV_KERNEL_GENERIC, st, [&] {
+      return launch_generic_attention(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    });
+  if (e == cudaSuccess && dp.n_combine)
+    e = launch_counted(RBKV_KERNEL_COMBINE, st,
+                       [&] { return launch_combine(dp, s, part_o, part_lse, o, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (!p->dev) return RBKV_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t word = 0;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, p->dev, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(p->dev, 0, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  if (word == kDevBounds) return fail(RBKV_ERR_DEVICE_BOUNDS, "a kernel met an out-of-range block id");
+  if (word == kDevTimeout) return fail(RBKV_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (word != 0) return fail(RBKV_ERR_CUDA, "unknown device status " + std::to_string(word));
+  return RBKV_OK;
+}
+
+int64_t rbkv_kernel_launches(void) { return g_launches.load(); }
+
+void rbkv_profile_enable(int32_t on) { g_prof.on = on != 0; }
+
+rbkv_status rbkv_profile_read(int32_t kind, double* total_ms, int64_t* launches) {
+  if (kind < 0 || kind >= RBKV_KERNEL_KINDS || !total_ms || !launches)
+    return fail(RBKV_ERR_INVALID, "bad arguments");
+  double t = 0.0;
+  for (auto& pr : g_prof.rec[kind]) {
+    cudaError_t e = cudaEventSynchronize(pr.second);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, pr.first, pr.second);
+    if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    t += ms;
+  }
+  *total_ms = t;
+  *launches = (int64_t)g_prof.rec[kind].size();
+  return RBKV_OK;
+}
+
+void rbkv_profile_reset(void) { g_prof.reset(); }
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// Internal structures shared by the host side (rbkv_host.cpp) and the kernels.
+// Nothing here is part of the public ABI (include/rbkv.h).
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+namespace rbkv {
+
+// One unit of split attention work: the keys [key_begin, key_end) of one
+// sequence's KV head, for one pass row (all query heads of the group).
+// part < 0: the unit covers all keys of the row; write O directly.
+// part >= 0: write the normalised partial output and its log-sum-exp to
+// partial slot `part` of the workspace.
+struct WorkItem {
+  int32_t row;        // pass row (index into Q / O)
+  int32_t kv_head;
+  int32_t key_begin;
+  int32_t key_end;
+  int32_t part;
+  int32_t table_off;  // offset of the sequence's block table in block_ids
+};
+static_assert(sizeof(WorkItem) == 24, "WorkItem is 6 int32");
+
+// (row, kv head) whose keys were split: partial slots [part_begin, part_begin+nsplit).
+struct CombineRow {
+  int32_t row;
+  int32_t kv_head;
+  int32_t part_begin;
+  int32_t nsplit;
+};
+
+// Up to 128 consecutive rows of one prompt chunk (one sequence).  Row r of the
+// tile is pass row row_begin + r at position pos_begin + r; it sees keys
+// 0 .. pos_begin + r.
+struct ChunkTile {
+  int32_t table_off;
+  int32_t row_begin;
+  int32_t n_rows;
+  int32_t pos_begin;
+};
+
+// Device view of a pass (pointers into its uploaded metadata buffer).
+struct DevPass {
+  int32_t* status;                 // device status word (rbkv_status codes)
+  const int32_t* slot;             // [T]
+  const int32_t* block_ids;        // all block tables
+  const WorkItem* decode_items;    // fast decode path
+  const WorkItem* generic_items;   // CUDA-core path
+  const ChunkTile* chunk_tiles;    // tensor-core prompt path
+  const CombineRow* combine_rows;
+  int32_t num_tokens;
+  int32_t n_decode;
+  int32_t n_generic;
+  int32_t n_chunk;
+  int32_t n_combine;
+  int32_t n_parts;
+  int32_t num_blocks;
+  int32_t decode_grid;             // CTAs of the persistent decode launch
+};
+
+struct ShapeInfo {
+  int32_t H_q, H_kv, D, B, g;
+  int32_t dtype;       // rbkv_dtype
+  float scale;         // 1/sqrt(D)
+};
+
+// Workspace carve-up: partial outputs [n_parts][g][D] fp32, then LSE [n_parts][g].
+inline size_t partial_o_bytes(int32_t n_parts, const ShapeInfo& s) {
+  size_t b = (size_t)n_parts * s.g * s.D * sizeof(float);
+  return (b + 255) / 256 * 256;
+}
+inline size_t partial_lse_bytes(int32_t n_parts, const ShapeInfo& s) {
+  size_t b = (size_t)n_parts * s.g * sizeof(float);
+  return (b + 255) / 256 * 256;
+}
+
+// Status codes written by kernels (same values as rbkv_status).
+constexpr int32_t kDevBounds = -4;
+constexpr int32_t kDevTimeout = -7;
+
+// Fast-path envelopes.
+constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decode kernel
+constexpr int kDecodeCtasPerSm = 2;
+constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
+constexpr int kChunkTileKeys = 64;       // keys per tensor-core KV tile
+
+bool decode_fast_supported(const ShapeInfo& s);
+bool chunk_fast_supported(const ShapeInfo& s);
+
+// Kernel launchers (return the launch's cudaError_t).
+cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* k_new,
+                             const void* v_new, void* k_cache, void* v_cache, cudaStream_t st);
+cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
+                                     const void* k_cache, const void* v_cache, void* o,
+                                     float* part_o, float* part_lse, cudaStream_t st);
+cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
+                               const void* k_cache, const void* v_cache, void* o,
+                               float* part_o, float* part_lse, cudaStream_t st);
+cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
+                              const void* k_cache, const void* v_cache, void* o,
+                              cudaStream_t st);
+cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
+                           const float* part_lse, void* o, cudaStream_t st);
+
+}  // namespace rbkv

@@ -1,0 +1,247 @@
+// kv_append, the CUDA-core attention path and the log-sum-exp combine.
+//
+// kv_append: FastGen guide, "Paged KV Memory Management" - new K/V rows go to
+//   fixed-size blocks reached through the block table.  One thread moves 16
+//   bytes of K and 16 bytes of V; consecutive threads cover consecutive bytes
+//   of a row, so loads and stores are fully coalesced 16-byte accesses.
+// generic attention: exact softmax attention of one (row, KV head, key split)
+//   work unit per CTA, online softmax over 32-key chunks (one key per lane),
+//   fp32 arithmetic.  Used for fp32 layers and for shapes outside the
+//   tensor-core kernels' envelope.
+// combine: FastGen guide, "Two-Phase Softmax Reduction" and Step 3's split
+//   path - partial outputs O_i with log-sum-exps L_i merge as
+//   O = sum_i 2^(L_i - M) O_i / sum_i 2^(L_i - M), M = max_i L_i
+//   (log-sum-exps are kept in base 2 inside the library).
+#include "rbkv_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace rbkv {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+  atomicCAS(status, 0, code);
+}
+
+template <class T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <class T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ---------------------------------------------------------------------------
+// kv_append
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) kv_append_kernel(DevPass dp, int32_t H_kv, int32_t B,
+                                                        int32_t vec_per_row,
+                                                        const uint4* __restrict__ k_new,
+                                                        const uint4* __restrict__ v_new,
+                                                        uint4* __restrict__ k_cache,
+                                                        uint4* __restrict__ v_cache) {
+  const int64_t total = (int64_t)dp.num_tokens * H_kv * vec_per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t v = (int32_t)(i % vec_per_row);
+    const int64_t th = i / vec_per_row;         // t * H_kv + h
+    const int32_t h = (int32_t)(th % H_kv);
+    const int32_t t = (int32_t)(th / H_kv);
+    const int32_t slot = dp.slot[t];
+    const int32_t blk = slot / B, off = slot - (slot / B) * B;
+    if (slot < 0 || blk >= dp.num_blocks) {
+      report(dp.status, kDevBounds);
+      continue;
+    }
+    const int64_t dst = (((int64_t)blk * H_kv + h) * B + off) * vec_per_row + v;
+    k_cache[dst] = k_new[i];
+    v_cache[dst] = v_new[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core attention over one work unit per CTA
+// ---------------------------------------------------------------------------
+constexpr int kGenWarps = 4;
+constexpr int kMaxDPerLane = 8;  // head_dim <= 256
+
+template <class T>
+__global__ void __launch_bounds__(kGenWarps * 32)
+    generic_attention_kernel(DevPass dp, ShapeInfo s, const T* __restrict__ q,
+                             const T* __restrict__ k_cache, const T* __restrict__ v_cache,
+                             T* __restrict__ o, float* __restrict__ part_o,
+                             float* __restrict__ part_lse) {
+  __shared__ float q_s[kGenWarps][256];
+  const WorkItem it = dp.generic_items[blockIdx.x];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int D = s.D, B = s.B, H_kv = s.H_kv;
+  const int dpl = D / 32;  // elements of the output row per lane (D % 32 == 0 here)
+  const float qscale = s.scale * kLog2e;
+  const int32_t* table = dp.block_ids + it.table_off;
+
+  for (int gi = warp; gi < s.g; gi += kGenWarps) {
+    const int h = it.kv_head * s.g + gi;
+    const T* qrow = q + ((int64_t)it.row * s.H_q + h) * D;
+    for (int d = lane; d < D; d += 32) q_s[warp][d] = to_f(qrow[d]) * qscale;
+    __syncwarp();
+
+    float m = -INFINITY, l = 0.f;
+    float acc[kMaxDPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxDPerLane; ++i) acc[i] = 0.f;
+
+    for (int k0 = it.key_begin; k0 < it.key_end; k0 += 32) {
+      const int key = k0 + lane;
+      float sc = -INFINITY;
+      int64_t row_off = -1;
+      if (key < it.key_end) {
+        const int32_t blk = table[key / B];
+        if (blk >= 0 && blk < dp.num_blocks) {
+          row_off = (((int64_t)blk * H_kv + it.kv_head) * B + key % B) * D;
+          const T* krow = k_cache + row_off;
+          float dot = 0.f;
+          for (int d = 0; d < D; ++d) dot = fmaf(q_s[warp][d], to_f(krow[d]), dot);
+          sc = dot;
+        } else {
+          report(dp.status, kDevBounds);
+        }
+      }
+      float cmax = sc;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, off));
+      const float m_new = fmaxf(m, cmax);
+      if (m_new == -INFINITY) continue;  // every key of this chunk skipped
+      const float corr = exp2f(m - m_new);
+      const float p = exp2f(sc - m_new);
+      float psum = p;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+      l = l * corr + psum;
+#pragma unroll
+      for (int i = 0; i < kMaxDPerLane; ++i) acc[i] *= corr;
+      for (int j = 0; j < 32; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+        const int64_t roff = __shfl_sync(0xffffffffu, row_off, j);
+        if (roff < 0) continue;
+        const T* vrow = v_cache + roff;
+#pragma unroll
+        for (int i = 0; i < kMaxDPerLane; ++i)
+          if (i < dpl) acc[i] = fmaf(pj, to_f(vrow[lane + 32 * i]), acc[i]);
+      }
+      m = m_new;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (it.part < 0) {
+      T* orow = o + ((int64_t)it.row * s.H_q + h) * D;
+#pragma unroll
+      for (int i = 0; i < kMaxDPerLane; ++i)
+        if (i < dpl) orow[lane + 32 * i] = from_f<T>(acc[i] * inv);
+    } else {
+      float* prow = part_o + ((int64_t)it.part * s.g + gi) * D;
+#pragma unroll
+      for (int i = 0; i < kMaxDPerLane; ++i)
+        if (i < dpl) prow[lane + 32 * i] = acc[i] * inv;
+      if (lane == 0) part_lse[(int64_t)it.part * s.g + gi] = l > 0.f ? m + log2f(l) : -INFINITY;
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// log-sum-exp combine: one warp per (split row, query head of the group)
+// ---------------------------------------------------------------------------
+template <class T>
+__global__ void __launch_bounds__(128)
+    combine_kernel(DevPass dp, ShapeInfo s, const float* __restrict__ part_o,
+                   const float* __restrict__ part_lse, T* __restrict__ o) {
+  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (w >= (int64_t)dp.n_combine * s.g) return;
+  const CombineRow cr = dp.combine_rows[w / s.g];
+  const int gi = (int)(w % s.g);
+  const int D = s.D, dpl = D / 32;
+  float M = -INFINITY;
+  for (int i = 0; i < cr.nsplit; ++i) M = fmaxf(M, part_lse[(int64_t)(cr.part_begin + i) * s.g + gi]);
+  float acc[kMaxDPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxDPerLane; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  for (int i = 0; i < cr.nsplit; ++i) {
+    const int64_t part = cr.part_begin + i;
+    const float lse = part_lse[part * s.g + gi];
+    const float wi = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
+    wsum += wi;
+    const float* prow = part_o + (part * s.g + gi) * D;
+#pragma unroll
+    for (int k = 0; k < kMaxDPerLane; ++k)
+      if (k < dpl) acc[k] = fmaf(wi, prow[lane + 32 * k], acc[k]);
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  T* orow = o + ((int64_t)cr.row * s.H_q + cr.kv_head * s.g + gi) * D;
+#pragma unroll
+  for (int k = 0; k < kMaxDPerLane; ++k)
+    if (k < dpl) orow[lane + 32 * k] = from_f<T>(acc[k] * inv);
+}
+
+int num_sms_current() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* k_new,
+                             const void* v_new, void* k_cache, void* v_cache, cudaStream_t st) {
+  const int esz = s.dtype == 0 ? 2 : 4;
+  const int vec = s.D * esz / 16;
+  const int64_t total = (int64_t)dp.num_tokens * s.H_kv * vec;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms_current() * 16;
+  if (blocks > cap) blocks = cap;
+  kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(dp, s.H_kv, s.B, vec, (const uint4*)k_new,
+                                                     (const uint4*)v_new, (uint4*)k_cache,
+                                                     (uint4*)v_cache);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
+                                     const void* k_cache, const void* v_cache, void* o,
+                                     float* part_o, float* part_lse, cudaStream_t st) {
+  if (s.D % 32) return cudaErrorNotSupported;
+  if (dp.n_generic == 0) return cudaSuccess;
+  if (s.dtype == 0)
+    generic_attention_kernel<__nv_bfloat16><<<dp.n_generic, kGenWarps * 32, 0, st>>>(
+        dp, s, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k_cache,
+        (const __nv_bfloat16*)v_cache, (__nv_bfloat16*)o, part_o, part_lse);
+  else
+    generic_attention_kernel<float><<<dp.n_generic, kGenWarps * 32, 0, st>>>(
+        dp, s, (const float*)q, (const float*)k_cache, (const float*)v_cache, (float*)o, part_o,
+        part_lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
+                           const float* part_lse, void* o, cudaStream_t st) {
+  if (s.D % 32) return cudaErrorNotSupported;
+  const int64_t warps = (int64_t)dp.n_combine * s.g;
+  if (warps == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((warps * 32 + 127) / 128);
+  if (s.dtype == 0)
+    combine_kernel<__nv_bfloat16><<<blocks, 128, 0, st>>>(dp, s, part_o, part_lse,
+                                                          (__nv_bfloat16*)o);
+  else
+    combine_kernel<float><<<blocks, 128, 0, st>>>(dp, s, part_o, part_lse, (float*)o);
+  return cudaGetLastError();
+}
+
+}  // namespace rbkv

@@ -1,0 +1,215 @@
+"""The library's C++ composer matches the oracle's bit for bit (CPU only).
+
+Both sides compose the same call sequences independently; every metadata array
+(sequence ids, row offsets, token counts, contexts, block tables, slots) must be
+identical, errors must fall in the same class, and the pool must agree.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tiny_pass.json")
+FIELDS = ("seq_ids", "q_start", "n_new", "seen", "ctx", "block_start", "block_ids", "slot")
+
+
+def _same(lib_pass, ometa):
+    m = lib_pass.meta
+    for f in FIELDS:
+        a = np.asarray(getattr(m, f), dtype=np.int64)
+        b = np.asarray(getattr(ometa, f), dtype=np.int64)
+        assert a.shape == b.shape and np.array_equal(a, b), f
+    return True
+
+
+class Both:
+    """Drive the library composer and the oracle composer in lockstep."""
+
+    def __init__(self, rbkv, B, num_blocks, shape=(8, 2, 64, "f32")):
+        hq, hkv, d, dt = shape
+        self.lib = rbkv.Composer(rbkv.Config(hq, hkv, d, B, dt, num_blocks))
+        self.orc = oracle.Composer(B, num_blocks)
+        self.rbkv = rbkv
+
+    def compose(self, budget, max_chunk, states):
+        err_l = err_o = None
+        p = m = None
+        try:
+            p = self.lib.compose(budget, max_chunk, states)
+        except self.rbkv.NoBlocksError:
+            err_l = "noblocks"
+        except self.rbkv.RbkvError:
+            err_l = "invalid"
+        try:
+            m = self.orc.compose(budget, max_chunk, states)
+        except oracle.NoBlocks:
+            err_o = "noblocks"
+        except oracle.InvalidRequest:
+            err_o = "invalid"
+        assert err_l == err_o
+        if p is not None:
+            _same(p, m)
+        assert self.lib.free_blocks() == self.orc.free_blocks()
+        return m
+
+    def release(self, sid):
+        err_l = err_o = None
+        try:
+            self.lib.release(sid)
+        except self.rbkv.RbkvError:
+            err_l = "invalid"
+        try:
+            self.orc.release(sid)
+        except oracle.InvalidRequest:
+            err_o = "invalid"
+        assert err_l == err_o
+        assert self.lib.free_blocks() == self.orc.free_blocks()
+
+
+def test_tiny_worked_pass_bit_exact(rbkv):
+    g = json.load(open(GOLDEN))
+    both = Both(rbkv, 16, 64)
+    r = g["registration"]
+    both.compose(r["budget"], r["max_chunk"], [tuple(s) for s in r["states"]])
+    p = g["pass"]
+    m = both.compose(p["budget"], p["max_chunk"], [tuple(s) for s in p["states"]])
+    assert list(m.block_ids) == g["expected"]["block_ids"]
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_random_call_sequences(rbkv, seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.choice([1, 4, 16, 64]))
+    both = Both(rbkv, B, int(rng.integers(0, 300)))
+    known = {}      # seq_id -> (prompt_len, seen)
+    next_id = 1
+    for _ in range(60):
+        r = rng.random()
+        if r < 0.1 and known:
+            sid = int(rng.choice(list(known)))
+            both.release(sid)
+            known.pop(sid)
+            continue
+        if r < 0.13:
+            both.release(10_000 + next_id)       # unknown id: both reject
+            continue
+        states = []
+        for sid, (pl, seen) in known.items():
+            if rng.random() < 0.8:
+                states.append((sid, pl, seen))
+        for _ in range(int(rng.integers(0, 3))):
+            states.append((next_id, int(rng.integers(1, 200)), 0))
+            next_id += 1
+        if rng.random() < 0.05 and states:
+            states.append(states[0])                 # duplicate: both reject
+        if rng.random() < 0.05 and states:
+            sid, pl, seen = states[-1]
+            states[-1] = (sid, pl, seen + 1)         # wrong seen: both reject
+        order = rng.permutation(len(states))
+        states = [states[i] for i in order]
+        budget = int(rng.integers(-1, 300))
+        M = int(rng.choice([-5, 0, 1, 16, 100]))
+        m = both.compose(budget, M, states)
+        if m is not None:
+            for s in range(m.num_seqs):
+                sid = m.seq_ids[s]
+                pl = dict((x[0], x[1]) for x in states)[sid]
+                known[sid] = (pl, m.ctx[s])
+            for sid, pl, seen in states:
+                if sid not in known and seen == 0:
+                    pass
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama2_7b", "decode_stress", "mistral_7b"])
+def test_scenarios_bit_exact(rbkv, name):
+    scn = workloads.SCENARIOS[name](0)
+    sh = scn.shape
+    both = Both(rbkv, sh.block_size, scn.num_blocks,
+                (sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.dtype))
+    b, st = scn.registration()
+    both.compose(b, 0, st)
+    states = list(scn.requests)
+    for _ in range(12):
+        m = both.compose(scn.budget, scn.max_chunk, states)
+        n = dict(zip(m.seq_ids, m.n_new))
+        states = [(sid, pl, seen + n.get(sid, 0)) for sid, pl, seen in states]
+        if m.num_tokens == 0:
+            break
+
+
+def test_llama2_7b_chunks_are_497(rbkv):
+    scn = workloads.llama2_7b(0)
+    sh = scn.shape
+    both = Both(rbkv, sh.block_size, scn.num_blocks,
+                (sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.dtype))
+    b, st = scn.registration()
+    both.compose(b, 0, st)
+    states = list(scn.requests)
+    chunks = []
+    while True:
+        m = both.compose(scn.budget, scn.max_chunk, states)
+        n = dict(zip(m.seq_ids, m.n_new))
+        if states[0][2] >= states[0][1]:
+            break
+        chunks.append(n[1])
+        states = [(sid, pl, seen + n.get(sid, 0)) for sid, pl, seen in states]
+    assert chunks == [497] * 8 + [120]
+
+
+def test_full_trace_bit_exact(rbkv):
+    """512 requests, 32 closed-loop clients, budget 512: every pass identical."""
+    reqs_l = workloads.trace_requests(seed=0)
+    reqs_o = workloads.trace_requests(seed=0)
+    nb = workloads.trace_block_pool(reqs_l, 32, 64)
+    lib_c = rbkv.Composer(rbkv.Config(32, 32, 128, 64, "bf16", nb))
+    orc_c = oracle.Composer(64, nb)
+    lib_metas = []
+
+    def lib_compose(b, M, st):
+        p = lib_c.compose(b, M, st)
+        lib_metas.append(p.meta)
+        return p.meta
+
+    n_l = workloads.run_trace(reqs_l, 32, 512, 512, lib_compose, lib_c.release)
+    i = [0]
+
+    def orc_compose(b, M, st):
+        m = orc_c.compose(b, M, st)
+        lm = lib_metas[i[0]]
+        for f in FIELDS:
+            assert np.array_equal(np.asarray(getattr(lm, f), np.int64),
+                                  np.asarray(getattr(m, f), np.int64)), (i[0], f)
+        i[0] += 1
+        return m
+
+    n_o = workloads.run_trace(reqs_o, 32, 512, 512, orc_compose, orc_c.release)
+    assert n_l == n_o == len(lib_metas)
+    assert 2000 < n_l < 3500
+    assert lib_c.free_blocks() == orc_c.free_blocks() == nb
+
+
+def test_plan_covers_every_row_and_head(rbkv):
+    scn = workloads.decode_stress(0)
+    sh = scn.shape
+    comp = rbkv.Composer(rbkv.Config(sh.num_heads_q, sh.num_heads_kv, sh.head_dim,
+                                     sh.block_size, sh.dtype, scn.num_blocks))
+    b, st = scn.registration()
+    comp.compose(b, 0, st)
+    p = comp.compose(scn.budget, scn.max_chunk, scn.requests)
+    info = p.plan_for_sms(152)
+    assert info["decode_rows"] == 64
+    items = info["decode_items"] + info["generic_items"]
+    assert items >= 64 * sh.num_heads_kv
+    # splits exist for the long contexts and partials match the split rows
+    assert info["max_splits"] > 1 and info["partials"] > 0
+    keys = info["split_keys"]
+    ctx = p.meta.ctx
+    expect_max = max(-(-int(c) // keys) for c in ctx)
+    assert info["max_splits"] == expect_max
+    # forcing the split length changes only the plan
+    p2 = comp.compose(0, 0, [])
+    assert p2.plan_for_sms(152)["decode_items"] + p2.plan_for_sms(152)["generic_items"] == 0

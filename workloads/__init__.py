@@ -172,18 +172,20 @@ def _stream_seed(seed: int, pass_index: int, tag: str) -> int:
 
 
 def make_qkv(shape: Shape, num_tokens: int, seed: int, pass_index: int,
-             device: str = "cpu"):
+             device: str = "cpu", which: str = "qkv"):
     """Q ``[T][H_q][D]`` and new K, V ``[T][H_kv][D]`` for one pass.
 
     Values are i.i.d. N(0,1) drawn in fp32 from a seeded torch generator on
     ``device``, multiplied by ``shape.input_scale`` and rounded to the storage
     type (round-to-nearest-even for bf16).  The same (seed, pass, device) gives
-    the same values.
+    the same values.  ``which`` selects the tensors returned (e.g. "kv").
     """
     import torch
     dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
     out = []
     for tag, heads in (("q", shape.num_heads_q), ("k", shape.num_heads_kv), ("v", shape.num_heads_kv)):
+        if tag not in which:
+            continue
         g = torch.Generator(device=device)
         g.manual_seed(_stream_seed(seed, pass_index, tag))
         x = torch.randn((num_tokens, heads, shape.head_dim), generator=g,
