@@ -81,11 +81,15 @@ constexpr int32_t kDevTimeout = -7;
 
 // Fast-path envelopes.
 constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decode kernel
-constexpr int kDecodeCtasPerSm = 2;
+constexpr int kDecodeCtasPerSm = 1;
 constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
 constexpr int kChunkTileKeys = 64;       // keys per tensor-core KV tile
 
 bool decode_fast_supported(const ShapeInfo& s);
+// 2-D view of a bf16 [num_blocks][H_kv][B][head_dim] cache for TMA: `rows`
+// rows of head_dim elements, boxes of 64 columns x box_rows rows, 128 B swizzle.
+cudaError_t make_cache_tmap(struct CUtensorMap_st* m, const void* cache, int64_t rows,
+                            int head_dim, int box_rows);
 bool chunk_fast_supported(const ShapeInfo& s);
 
 // Kernel launchers (return the launch's cudaError_t).
