@@ -1,13 +1,471 @@
-// Prompt-chunk attention on tcgen05 tensor cores (filled in below).
+// Prompt-chunk attention on the fifth-generation tensor cores (tcgen05).
+//
+// FastGen guide, "The Continuous Batching Dilemma": prompt processing is a
+// dense contraction that belongs on the tensor cores.  A chunk row at position
+// p attends keys 0..p of its sequence: the cached prefix read through the
+// block table plus the chunk's own earlier rows (causal within the chunk).
+//
+// One CTA owns 128 consecutive rows of one chunk for one query head:
+//  - warp 4 (TMA): loads the 128x128 Q tile once and streams 64-key K and V
+//    tiles of the paged cache into a 2-stage ring (128-byte swizzle);
+//  - warp 5 (MMA): allocates 256 TMEM columns; one thread issues
+//    S = Q K^T (M=128, N=64, K=128) into one of two TMEM S buffers and
+//    O += P V (M=128, N=128, K=64) into the TMEM O accumulator, and signals
+//    completion with tcgen05.commit;
+//  - warps 0-3 (softmax): thread i owns query row i = TMEM lane i; it reads its
+//    64 scores with tcgen05.ld, masks causally, keeps a running max that is
+//    raised only when a row's max grows by more than 2^8 (the accumulator in
+//    TMEM is then rescaled in place), writes P as bf16 into shared memory in
+//    the MMA operand layout, and finally normalises O and stores it.
+// Two CTAs fit on an SM (112 KB shared memory, 256 TMEM columns each).
+// Every wait is bounded; on timeout the kernel records RBKV_ERR_TIMEOUT, lets
+// its copies and MMAs drain (bounded), frees its TMEM and returns.
 #include "rbkv_internal.h"
+#include "rbkv_ptx.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
 namespace rbkv {
 
-bool chunk_fast_supported(const ShapeInfo&) { return false; }
+namespace {
 
-cudaError_t launch_chunk_fast(const DevPass&, const ShapeInfo&, const void*, const void*,
-                              const void*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kRows = kChunkTileRows;       // 128 query rows (MMA M)
+constexpr int kKeys = kChunkTileKeys;       // 64 keys per KV tile
+constexpr int kStages = 2;
+constexpr int kThreads = 6 * 32;
+constexpr int kQHalf = kRows * 128;         // 16 KB: 128 rows x 64 bf16
+constexpr int kQBytes = 2 * kQHalf;
+constexpr int kKVHalf = kKeys * 128;        // 8 KB
+constexpr int kKVTile = 2 * kKVHalf;        // 16 KB
+constexpr int kStage = 2 * kKVTile;         // K + V
+constexpr int kPBytes = kRows * 128;        // 128 rows x 64 keys bf16
+constexpr int kTmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
+constexpr int kOCol = 128;
+constexpr int kSmemBytes = 1024 + kQBytes + kStages * kStage + kPBytes + 256;
+constexpr long long kWaitLimit = 4000000000LL;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+// ---- tcgen05 wrappers ----------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   ptx::smem_u32(slot)),
+               "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   ptx::smem_u32(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 in, fp32 accumulate)
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full;
+  uint64_t o_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+    chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                              const __grid_constant__ CUtensorMap tmap_k,
+                              const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
+                              ShapeInfo shp, __nv_bfloat16* __restrict__ o) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = base;
+  uint8_t* kv_s = q_s + kQBytes;
+  uint8_t* p_s = kv_s + kStages * kStage;
+  Bars* bars = reinterpret_cast<Bars*>(p_s + kPBytes);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ChunkTile tile = dp.chunk_tiles[blockIdx.x];
+  const int h = blockIdx.y;
+  const int kvh = h / shp.g;
+  const int B = shp.B;
+  const int n_keys = tile.pos_begin + tile.n_rows;
+  const int n_kv = (n_keys + kKeys - 1) / kKeys;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&bars->kv_full[s], 1);
+      ptx::mbar_init(&bars->kv_empty[s], 1);
+    }
+    ptx::mbar_init(&bars->s_full[0], 1);
+    ptx::mbar_init(&bars->s_full[1], 1);
+    ptx::mbar_init(&bars->p_full, 4 * 32);
+    ptx::mbar_init(&bars->o_done, 1);
+    bars->abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmap_q);
+      ptx::tma_prefetch_desc(&tmap_k);
+      ptx::tma_prefetch_desc(&tmap_v);
+      ptx::mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+      ptx::tma_load_2d(q_s, &tmap_q, h * 128, tile.row_begin, &bars->q_full);
+      ptx::tma_load_2d(q_s + kQHalf, &tmap_q, h * 128 + 64, tile.row_begin, &bars->q_full);
+      const int32_t* table = dp.block_ids + tile.table_off;
+      const int box_rows = B < kKeys ? B : kKeys;
+      int issued = 0;
+      for (int j = 0; j < n_kv && !*abort_flag; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages &&
+            !ptx::mbar_wait(&bars->kv_empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
+          atomicCAS(dp.status, 0, kDevTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* kdst = kv_s + s * kStage;
+        uint8_t* vdst = kdst + kKVTile;
+        int32_t rows[kKeys / 8];
+        int nsub = 0, loads = 0;
+        for (int r = 0; r < kKeys; r += box_rows) {
+          const int key = j * kKeys + r;
+          if (key >= n_keys) break;
+          const int32_t blk = table[key / B];
+          if (blk < 0 || blk >= dp.num_blocks) {
+            atomicCAS(dp.status, 0, kDevBounds);
+            rows[nsub++] = -1;
+            continue;
+          }
+          rows[nsub++] = (blk * shp.H_kv + kvh) * B + (key % B);
+          ++loads;
+        }
+        ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 4));
+        for (int i = 0; i < nsub; ++i) {
+          if (rows[i] < 0) continue;
+          const int off = i * box_rows * 128;
+          ptx::tma_load_2d(kdst + off, &tmap_k, 0, rows[i], &bars->kv_full[s]);
+          ptx::tma_load_2d(kdst + kKVHalf + off, &tmap_k, 64, rows[i], &bars->kv_full[s]);
+          ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &bars->kv_full[s]);
+          ptx::tma_load_2d(vdst + kKVHalf + off, &tmap_v, 64, rows[i], &bars->kv_full[s]);
+        }
+        issued = j + 1;
+      }
+      // every copy must land before the CTA may exit
+      ptx::mbar_wait(&bars->q_full, 0, kWaitLimit);
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        ptx::mbar_wait(&bars->kv_full[j % kStages], (j / kStages) & 1, kWaitLimit);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
+      constexpr uint32_t idesc_o = instr_desc(kRows, 128, 1);
+      const uint32_t q_addr = ptx::smem_u32(q_s);
+      const uint32_t kv_addr = ptx::smem_u32(kv_s);
+      const uint32_t p_addr = ptx::smem_u32(p_s);
+      bool ok = ptx::mbar_wait(&bars->q_full, 0, kWaitLimit);
+      int pv_issued = 0;
+      auto issue_qk = [&](int j) {
+        const uint32_t kt = kv_addr + (j % kStages) * kStage;
+        const uint32_t d = tmem + (j & 1) * kKeys;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
+          tc_mma(d, smem_desc(q_addr + qo, 16, 1024), smem_desc(kt + ko, 16, 1024), idesc_s,
+                 kk > 0);
+        }
+        tc_commit(&bars->s_full[j & 1]);
+      };
+      if (ok && n_kv > 0) {
+        ok = ptx::mbar_wait(&bars->kv_full[0], 0, kWaitLimit);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(0);
+        }
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv) {
+          if (!ptx::mbar_wait(&bars->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
+                              kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(j + 1);
+        }
+        if (!ptx::mbar_wait(&bars->p_full, j & 1, kWaitLimit) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vt = kv_addr + (j % kStages) * kStage + kKVTile;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          tc_mma(tmem + kOCol, smem_desc(p_addr + kk * 32, 16, 1024),
+                 smem_desc(vt + kk * 2048, kKVHalf, 1024), idesc_o, j > 0 || kk > 0);
+        }
+        tc_commit(&bars->o_done);
+        tc_commit(&bars->kv_empty[j % kStages]);
+        pv_issued = j + 1;
+      }
+      if (!ok) {
+        atomicCAS(dp.status, 0, kDevTimeout);
+        *abort_flag = 1;
+      }
+      // the last PV must finish before TMEM can be released
+      if (pv_issued > 0) ptx::mbar_wait(&bars->o_done, (pv_issued - 1) & 1, kWaitLimit);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int row = threadIdx.x;                      // 0..127 = TMEM lane
+    const int pos = tile.pos_begin + row;             // position of this query row
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float qk_scale = shp.scale * kLog2e;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      // tcgen05.ld/st are warp-collective: every decision below is warp-uniform
+      const bool got = ptx::mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *abort_flag != 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sc[64];
+      tmem_ld32(lane_base + (j & 1) * kKeys, sc);
+      tmem_ld32(lane_base + (j & 1) * kKeys + 32, sc + 32);
+      tmem_wait_ld();
+      const int key0 = j * kKeys;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int key = key0 + c;
+        sc[c] = (key <= pos && key < n_keys) ? sc[c] * qk_scale : -INFINITY;
+        mt = fmaxf(mt, sc[c]);
+      }
+      float corr = 1.f;
+      const bool raise = mt > m_ref + kRescaleThreshold;
+      if (raise) {
+        corr = exp2f(m_ref - mt);
+        m_ref = mt;
+      }
+      float ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        sc[c] = exp2f(sc[c] - m_ref);
+        ps += sc[c];
+      }
+      l = l * corr + ps;
+      // P and the O accumulator are busy until the previous PV completes
+      if (j > 0) {
+        const bool done = ptx::mbar_wait(&bars->o_done, (j - 1) & 1, kWaitLimit);
+        if (!__all_sync(0xffffffffu, done)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float ov[32];
+            tmem_ld32(lane_base + kOCol + c4 * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] *= corr;
+            tmem_st32(lane_base + kOCol + c4 * 32, ov);
+          }
+          tmem_wait_st();
+        }
+      }
+      if (j == n_kv - 1 && (n_keys % kKeys) != 0) {
+        // keys past the last row may be anything (unwritten slots): zero their V rows
+        const int s = j % kStages;
+        ptx::mbar_wait(&bars->kv_full[s], (j / kStages) & 1, kWaitLimit);
+        uint8_t* vt = kv_s + s * kStage + kKVTile;
+        const int valid = n_keys - key0;
+        for (int e = row; e < (kKeys - valid) * 16; e += kRows) {
+          const int key = valid + e / 16, c = e % 16;
+          *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVHalf + key * 128 + ((c & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      // P row -> shared memory, 128-byte swizzled K-major operand layout
+      uint8_t* prow = p_s + row * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 v;
+        v.x = ptx::pack_bf16x2(sc[c8 * 8 + 0], sc[c8 * 8 + 1]);
+        v.y = ptx::pack_bf16x2(sc[c8 * 8 + 2], sc[c8 * 8 + 3]);
+        v.z = ptx::pack_bf16x2(sc[c8 * 8 + 4], sc[c8 * 8 + 5]);
+        v.w = ptx::pack_bf16x2(sc[c8 * 8 + 6], sc[c8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = v;
+      }
+      ptx::fence_proxy_async_smem();
+      tc_fence_before();
+      ptx::mbar_arrive(&bars->p_full);
+    }
+    bool fin = ok && n_kv > 0;
+    if (fin) fin = ptx::mbar_wait(&bars->o_done, (n_kv - 1) & 1, kWaitLimit);
+    if (__all_sync(0xffffffffu, fin)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = row < tile.n_rows;
+      __nv_bfloat16* orow = o + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float ov[32];
+        tmem_ld32(lane_base + kOCol + c4 * 32, ov);
+        tmem_wait_ld();
+        if (store) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 v;
+            v.x = ptx::pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
+            v.y = ptx::pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
+            v.z = ptx::pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
+            v.w = ptx::pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = v;
+          }
+        }
+      }
+    } else if (!ok || n_kv > 0) {
+      atomicCAS(dp.status, 0, kDevTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  // all roles done (every wait above is bounded): release TMEM
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool chunk_fast_supported(const ShapeInfo& s) {
+  const bool block_ok = (s.B % kKeys == 0) || (kKeys % s.B == 0 && s.B % 8 == 0);
+  return s.dtype == 0 && s.D == 128 && block_ok;
+}
+
+cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
+                              const void* k_cache, const void* v_cache, void* o,
+                              cudaStream_t st) {
+  if (!chunk_fast_supported(s)) return cudaErrorNotSupported;
+  if (dp.n_chunk == 0) return cudaSuccess;
+  if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+    return cudaErrorMisalignedAddress;
+  const int64_t rows = (int64_t)dp.num_blocks * s.H_kv * s.B;
+  const int box_rows = s.B < kKeys ? s.B : kKeys;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
+  if (e == cudaSuccess) e = make_cache_tmap(&tv, v_cache, rows, s.D, box_rows);
+  if (e != cudaSuccess) return e;
+  // Q as [T][H_q * 128] rows; boxes of 64 columns x 128 rows (rows past T read as zero)
+  e = make_tmap_2d(&tq, q, dp.num_tokens, (int64_t)s.H_q * s.D, kRows);
+  if (e != cudaSuccess) return e;
+  static bool attr_done = false;
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(chunk_attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid(dp.n_chunk, s.H_q);
+  chunk_attn_tcgen05_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, dp, s,
+                                                                (__nv_bfloat16*)o);
+  return cudaGetLastError();
 }
 
 }  // namespace rbkv

@@ -9,10 +9,11 @@
 //  - a producer warp streams 64-key K and V tiles of the paged cache with TMA
 //    (2-D tiled loads through the block table, 128-byte swizzle) into a
 //    5-stage shared-memory ring guarded by mbarriers;
-//  - four consumer warps take the tiles of a unit in turn; each multiplies the
-//    group's query rows (padded to 16) by the tile with warp-level bf16 MMAs
-//    (fp32 accumulation), runs the online softmax in registers with quad
-//    shuffles, and accumulates P.V with MMAs;
+//  - four consumer warps share every tile, 16 keys each (so each warp consumes
+//    the ring strictly in order); each multiplies the group's query rows
+//    (padded to 16) by its keys with warp-level bf16 MMAs (fp32 accumulation),
+//    runs the online softmax in registers with quad shuffles, and accumulates
+//    P.V with MMAs;
 //  - at the end of a unit the four warps merge their (max, sum, O) states in
 //    shared memory and write either O (bf16) or the fp32 partial output and
 //    base-2 log-sum-exp for the combine kernel.
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
-      ptx::mbar_init(&sm.empty[s], 1);
+      ptx::mbar_init(&sm.empty[s], kConsumers);
     }
     abort_flag = 0;
     ptx::fence_barrier_init();
@@ -188,7 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc_o[i][0] = acc_o[i][1] = acc_o[i][2] = acc_o[i][3] = 0.f;
 
-    for (int j = warp; j < nt && !abort_flag; j += kConsumers) {
+    // every warp takes 16 keys (rows 16*warp .. 16*warp+15) of every tile, so
+    // each warp consumes the stages strictly in order
+    const int wk = warp * 16;
+    for (int j = 0; j < nt && !abort_flag; ++j) {
       const uint32_t idx = tile_base + j;
       const int s = idx % kStages;
       if (!ptx::mbar_wait(&sm.full[s], (idx / kStages) & 1, kWaitLimit)) {
@@ -199,90 +203,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int k0 = it.key_begin + j * kKeys;
-      const int valid = min(kKeys, it.key_end - k0);
+      const int valid = min(kKeys, it.key_end - k0) - wk;   // valid keys of this warp's 16
       const uint32_t kt = stages_u32 + s * kStage;
       const uint32_t vt = kt + kTile;
-      if (valid < kKeys) {
+      if (valid < 16) {
         // rows past the unit's last key may hold anything (unwritten cache
-        // slots, stale tiles): zero their V rows so 0 * V stays 0
+        // slots, stale tiles): zero this warp's such V rows so 0 * V stays 0
         uint8_t* vrow = sm.stages + s * kStage + kTile;
-        for (int e = lane; e < (kKeys - valid) * 16; e += 32) {
-          const int key = valid + e / 16, c = e % 16;
+        const int first = valid < 0 ? 0 : valid;
+        for (int e = lane; e < (16 - first) * 16; e += 32) {
+          const int key = wk + first + e / 16, c = e % 16;
           *reinterpret_cast<uint4*>(vrow + (c >> 3) * kHalf + key * 128 + ((c & 7) << 4)) =
               make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
-
-      // S = Q K^T over the 64 keys: 8 n-tiles of 8 keys
-      float sc[8][4];
+      if (valid > 0) {
+        // S = Q K^T over this warp's 16 keys: 2 n-tiles of 8 keys
+        float sc[2][4];
+        sc[0][0] = sc[0][1] = sc[0][2] = sc[0][3] = 0.f;
+        sc[1][0] = sc[1][1] = sc[1][2] = sc[1][3] = 0.f;
+        const int mi = lane >> 3;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          const int mi = lane >> 3;
-          const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
+        for (int kk = 0; kk < 8; ++kk) {
+          const int key = wk + (mi >> 1) * 8 + (lane & 7);
           const int d = kk * 16 + (mi & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ptx::ldsm_x4(kt + tile_off(key, d), b0, b1, b2, b3);
-          ptx::mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
-          ptx::mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
+          ptx::mma_bf16_16816(sc[0], qa[kk], b0, b1);
+          ptx::mma_bf16_16816(sc[1], qa[kk], b2, b3);
         }
-      }
-      // scale, mask keys past the unit, online softmax (rows r0 and r1)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+        // scale, mask keys past the unit, online softmax (rows r0 and r1)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const int key = n * 8 + cq;
-        sc[n][0] = key < valid ? sc[n][0] * qk_scale : -INFINITY;
-        sc[n][1] = key + 1 < valid ? sc[n][1] * qk_scale : -INFINITY;
-        sc[n][2] = key < valid ? sc[n][2] * qk_scale : -INFINITY;
-        sc[n][3] = key + 1 < valid ? sc[n][3] * qk_scale : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float ps0 = 0.f, ps1 = 0.f;
-      uint32_t pa[4][4];
+        for (int n = 0; n < 2; ++n) {
+          const int key = n * 8 + cq;
+          sc[n][0] = key < valid ? sc[n][0] * qk_scale : -INFINITY;
+          sc[n][1] = key + 1 < valid ? sc[n][1] * qk_scale : -INFINITY;
+          sc[n][2] = key < valid ? sc[n][2] * qk_scale : -INFINITY;
+          sc[n][3] = key + 1 < valid ? sc[n][3] * qk_scale : -INFINITY;
+          mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+          mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p00 = exp2f(sc[0][0] - mn0), p01 = exp2f(sc[0][1] - mn0);
+        const float p02 = exp2f(sc[0][2] - mn1), p03 = exp2f(sc[0][3] - mn1);
+        const float p10 = exp2f(sc[1][0] - mn0), p11 = exp2f(sc[1][1] - mn0);
+        const float p12 = exp2f(sc[1][2] - mn1), p13 = exp2f(sc[1][3] - mn1);
+        l0 = l0 * c0 + (p00 + p01 + p10 + p11);
+        l1 = l1 * c1 + (p02 + p03 + p12 + p13);
+        uint32_t pa[4];
+        pa[0] = ptx::pack_bf16x2(p00, p01);
+        pa[1] = ptx::pack_bf16x2(p02, p03);
+        pa[2] = ptx::pack_bf16x2(p10, p11);
+        pa[3] = ptx::pack_bf16x2(p12, p13);
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const float p0 = exp2f(sc[n][0] - mn0), p1 = exp2f(sc[n][1] - mn0);
-        const float p2 = exp2f(sc[n][2] - mn1), p3 = exp2f(sc[n][3] - mn1);
-        ps0 += p0 + p1;
-        ps1 += p2 + p3;
-        pa[n >> 1][(n & 1) * 2 + 0] = ptx::pack_bf16x2(p0, p1);
-        pa[n >> 1][(n & 1) * 2 + 1] = ptx::pack_bf16x2(p2, p3);
-      }
-      l0 = l0 * c0 + ps0;
-      l1 = l1 * c1 + ps1;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        acc_o[i][0] *= c0;
-        acc_o[i][1] *= c0;
-        acc_o[i][2] *= c1;
-        acc_o[i][3] *= c1;
-      }
-      // O += P V: 4 k-steps of 16 keys, 16 n-tiles of 8 head-dim columns
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+        for (int i = 0; i < 16; ++i) {
+          acc_o[i][0] *= c0;
+          acc_o[i][1] *= c0;
+          acc_o[i][2] *= c1;
+          acc_o[i][3] *= c1;
+        }
+        // O += P V over the 16 keys: 16 n-tiles of 8 head-dim columns
 #pragma unroll
         for (int dp2 = 0; dp2 < 8; ++dp2) {
-          const int mi = lane >> 3;
-          const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
+          const int key = wk + (mi & 1) * 8 + (lane & 7);
           const int d = dp2 * 16 + (mi >> 1) * 8;
           uint32_t b0, b1, b2, b3;
           ptx::ldsm_x4_t(vt + tile_off(key, d), b0, b1, b2, b3);
-          ptx::mma_bf16_16816(acc_o[2 * dp2], pa[kk], b0, b1);
-          ptx::mma_bf16_16816(acc_o[2 * dp2 + 1], pa[kk], b2, b3);
+          ptx::mma_bf16_16816(acc_o[2 * dp2], pa, b0, b1);
+          ptx::mma_bf16_16816(acc_o[2 * dp2 + 1], pa, b2, b3);
         }
       }
       __syncwarp();
@@ -363,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
-    ptx::named_bar_sync(1, kConsumers * 32);
-    if (abort_flag) return;
+    // all consumer warps leave together if anyone gave up
+    if (ptx::named_bar_or(1, kConsumers * 32, abort_flag != 0)) return;
   }
 }
 
@@ -390,20 +387,26 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// Rows of a [num_blocks][H_kv][B][head_dim] bf16 cache as a 2-D tensor
-// (head_dim columns), boxes of 64 columns x box_rows rows, 128-byte swizzle.
-cudaError_t make_cache_tmap(CUtensorMap* m, const void* cache, int64_t rows, int head_dim,
-                            int box_rows) {
+// A row-major bf16 matrix [rows][cols] as a 2-D TMA tensor: boxes of 64
+// columns (128 bytes) x box_rows rows, 128-byte swizzle; rows past the end
+// read as zero.
+cudaError_t make_tmap_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                         int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides,
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_cache_tmap(CUtensorMap* m, const void* cache, int64_t rows, int head_dim,
+                            int box_rows) {
+  return make_tmap_2d(m, cache, rows, head_dim, box_rows);
 }
 
 bool decode_fast_supported(const ShapeInfo& s) {

@@ -5,6 +5,8 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+struct CUtensorMap_st;  // cuda.h's tensor-map type
+
 namespace rbkv {
 
 // One unit of split attention work: the keys [key_begin, key_end) of one
@@ -88,8 +90,11 @@ constexpr int kChunkTileKeys = 64;       // keys per tensor-core KV tile
 bool decode_fast_supported(const ShapeInfo& s);
 // 2-D view of a bf16 [num_blocks][H_kv][B][head_dim] cache for TMA: `rows`
 // rows of head_dim elements, boxes of 64 columns x box_rows rows, 128 B swizzle.
-cudaError_t make_cache_tmap(struct CUtensorMap_st* m, const void* cache, int64_t rows,
+cudaError_t make_cache_tmap(::CUtensorMap_st* m, const void* cache, int64_t rows,
                             int head_dim, int box_rows);
+// Any row-major bf16 [rows][cols] matrix, same box width and swizzle.
+cudaError_t make_tmap_2d(::CUtensorMap_st* m, const void* ptr, int64_t rows, int64_t cols,
+                         int box_rows);
 bool chunk_fast_supported(const ShapeInfo& s);
 
 // Kernel launchers (return the launch's cudaError_t).
