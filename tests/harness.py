@@ -95,6 +95,8 @@ class Pair:
             q, k, v = ten
         else:
             k, v = ten
+        # inputs and caches were made on the default stream: order after them
+        self.stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(self.stream):
             kd, vd = k.cuda(), v.cuda()
             self.rbkv.kv_append(p, kd, vd, self.kc, self.vc, stream=self.stream)
@@ -112,6 +114,7 @@ class Pair:
         oracle.kv_append(m, ok, ov, self.okc, self.ovc, only_seqs=self.only)
         res["plan"] = p.plan()
         if attend:
+            self.stream.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(self.stream):
                 qd = q.cuda()
                 o = self.rbkv.ragged_attention(p, qd, self.kc, self.vc, stream=self.stream)

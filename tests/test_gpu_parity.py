@@ -71,6 +71,7 @@ def test_empty_pass_and_repeat_determinism(rbkv):
     _ok(r1)
     p = r1["pass"]
     q = workloads.make_qkv(shape, p.num_tokens, 0, 1, which="q")[0].cuda()
+    torch.cuda.synchronize()
     o1 = rbkv.ragged_attention(p, q, pair.kc, pair.vc)
     o2 = rbkv.ragged_attention(p, q, pair.kc, pair.vc)
     torch.cuda.synchronize()
