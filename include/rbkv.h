@@ -215,6 +215,26 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
                                   const void* v_cache, void* o, void* workspace,
                                   size_t workspace_bytes, rbkv_stream stream);
 
+/* Ragged attention that allocates nothing.  No counterpart in the paper: this
+ * is for callers that cannot call cudaMalloc or any other allocator where they
+ * run attention (a fixed device-memory budget handed out up front, a runtime
+ * that owns all device memory through its own pool, or a step that must not
+ * block or fail on an allocation).  Same computation, inputs and outputs as
+ * rbkv_ragged_attention, but the split-KV scratch is a 16 MiB array inside the
+ * library (held on every GPU that loads the library until the process exits)
+ * instead of a caller workspace.
+ *  - The pass must already be on the device: call rbkv_kv_append for it first
+ *    (that call uploads its metadata); otherwise RBKV_ERR_INVALID.
+ *  - A pass whose scratch need (rbkv_attention_workspace_bytes) exceeds
+ *    16 MiB is rejected with RBKV_ERR_WORKSPACE.
+ *  - The first call on a device looks up the array's device address for that
+ *    device; make that first call before any stream capture.
+ *  - All calls share the one array: calls whose kernels overlap on the GPU
+ *    race on it.  Order them on one stream (or with events).
+ * Calls no cudaMalloc, cudaFree or other allocating routine. */
+rbkv_status rbkv_ragged_attention_noalloc(rbkv_pass* p, const void* q, const void* k_cache,
+                                          const void* v_cache, void* o, rbkv_stream stream);
+
 /* Wait for `stream`, then read and clear the pass's device status word:
  * RBKV_OK, RBKV_ERR_DEVICE_BOUNDS (a kernel met a block id outside the pool and
  * skipped that access) or RBKV_ERR_TIMEOUT (a bounded wait gave up). */

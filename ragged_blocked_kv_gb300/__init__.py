@@ -83,6 +83,7 @@ SIGNATURES = {
     "rbkv_attention_workspace_bytes": (C.c_size_t, [_P]),
     "rbkv_ragged_attention": (C.c_int, [_P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "rbkv_pass_device_status": (C.c_int, [_P, _P]),
+    "rbkv_ragged_attention_noalloc": (C.c_int, [_P, _P, _P, _P, _P, _P]),
     "rbkv_kernel_launches": (C.c_int64, []),
     "rbkv_profile_enable": (None, [C.c_int32]),
     "rbkv_profile_read": (C.c_int, [C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
@@ -315,6 +316,23 @@ def ragged_attention(p: Pass, q, k_cache, v_cache, o=None, workspace=None, strea
     return o
 
 
+def ragged_attention_noalloc(p: Pass, q, k_cache, v_cache, o, stream=None):
+    """Ragged attention with the library's own static scratch instead of a
+    workspace: for callers that must not allocate device memory.  ``o`` must
+    be given (this call allocates nothing) and the pass must already have been
+    through ``kv_append``.  Calls that overlap on the GPU share the scratch and
+    race; keep them ordered on one stream."""
+    c = p.config
+    T = p.num_tokens
+    dt = c.torch_dtype
+    qshape = (T, c.num_heads_q, c.head_dim)
+    _check(lib().rbkv_ragged_attention_noalloc(p._h, _dev_ptr(q, "q", dt, qshape),
+                                               _dev_ptr(k_cache, "k_cache", dt, c.cache_shape()),
+                                               _dev_ptr(v_cache, "v_cache", dt, c.cache_shape()),
+                                               _dev_ptr(o, "o", dt, qshape), _stream(stream)))
+    return o
+
+
 def kernel_launches() -> int:
     """Kernels launched through the library by this process so far."""
     return int(lib().rbkv_kernel_launches())
@@ -338,5 +356,5 @@ def profile_read() -> dict:
     return out
 
 
-__all__ = ["kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+__all__ = ["ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
            "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

@@ -437,6 +437,64 @@ rbkv_status check_config(const rbkv_config* c) {
 
 }  // namespace
 
+// ---- attention on a pass already on the device, with a given scratch ---------
+// Used by the entry point that allocates nothing (rbkv_noalloc.cu): unlike
+// rbkv_ragged_attention it never uploads metadata (that would allocate), so
+// the pass must already have been on the device (its rbkv_kv_append call).
+namespace rbkv {
+
+rbkv_status set_error(rbkv_status st, const char* msg) { return fail(st, msg); }
+
+rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache,
+                                const void* v_cache, void* o, void* scratch,
+                                size_t scratch_bytes, cudaStream_t st) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (p->slot.empty()) return RBKV_OK;
+  if (!q || !k_cache || !v_cache || !o) return fail(RBKV_ERR_INVALID, "NULL tensor");
+  if (!p->dev)
+    return fail(RBKV_ERR_INVALID,
+                "the pass is not on the device yet: call rbkv_kv_append for it first "
+                "(this entry point allocates nothing, so it cannot upload metadata)");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != p->device) return fail(RBKV_ERR_INVALID, "pass is bound to another device");
+  const size_t need = workspace_bytes_of(*p);
+  if (need > scratch_bytes)
+    return fail(RBKV_ERR_WORKSPACE, "this pass needs " + std::to_string(need) +
+                                        " bytes of scratch; the static scratch holds " +
+                                        std::to_string(scratch_bytes));
+  if (st != p->upload_stream) {
+    e = cudaStreamWaitEvent(st, p->upload_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  p->last_stream = st;
+  const ShapeInfo s = shape_of(p->cfg);
+  float* part_o = (float*)scratch;
+  float* part_lse = (float*)((char*)scratch + partial_o_bytes(p->plan.n_parts, s));
+  const DevPass& dp = p->dp;
+  e = cudaSuccess;
+  int launched = 0;
+  if (dp.n_chunk) { e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, st); ++launched; }
+  if (e == cudaSuccess && dp.n_decode) {
+    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    ++launched;
+  }
+  if (e == cudaSuccess && dp.n_generic) {
+    e = launch_generic_attention(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    ++launched;
+  }
+  if (e == cudaSuccess && dp.n_combine) {
+    e = launch_combine(dp, s, part_o, part_lse, o, st);
+    ++launched;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  return RBKV_OK;
+}
+
+}  // namespace rbkv
+
 // ============================================================================
 // C ABI
 // ============================================================================

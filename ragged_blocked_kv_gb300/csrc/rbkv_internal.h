@@ -5,6 +5,8 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include "rbkv.h"
+
 struct CUtensorMap_st;  // cuda.h's tensor-map type
 
 namespace rbkv {
@@ -112,4 +114,12 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
 
+// Host helpers for the entry point that allocates nothing (rbkv_noalloc.cu).
+// attention_on_device: rbkv_ragged_attention for a pass whose metadata is
+// already on the current device, with `scratch` as its workspace; it never
+// allocates.  set_error: record a message for rbkv_last_error.
+rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache,
+                                const void* v_cache, void* o, void* scratch,
+                                size_t scratch_bytes, cudaStream_t st);
+rbkv_status set_error(rbkv_status st, const char* msg);
 }  // namespace rbkv
