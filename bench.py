@@ -4,12 +4,13 @@
 Workload (default): the Llama-2-7B attention shape - 32 query heads, 32 KV
 heads, head_dim 128, bf16, KV block 64, token budget 512, chunk cap 512.  A
 4096-token prompt is carried through 9 passes (8 chunks of 497 tokens and one
-of 120) next to 15 decode sequences whose contexts start at round(N(2600,
-780^2)) clipped to [64, 8192] and grow by one token per pass; when a prompt
-completes it is released and a fresh one starts, so every pass mixes a prompt
-chunk with the decodes.  A step is one whole pass of the hot path: host
-composition and block allocation, the metadata upload, kv_append and ragged
-attention (tensor-core chunk tiles, split-KV decode, log-sum-exp combine).
+of 120) next to 15 decode sequences whose contexts are round(N(2600, 780^2))
+clipped to [64, 8192] and grow by one token per pass.  After the 9th pass the
+cycle's passes are rolled back on the composer, so every cycle is the same 9
+passes (the decodes return to their starting contexts, the prompt starts
+again).  A step is one whole pass of the hot path: host composition and block
+allocation, the metadata upload, kv_append and ragged attention (tensor-core
+chunk tiles, split-KV decode, log-sum-exp combine).
 
 Output: one JSON line (rank 0).  ``value`` is pass tokens per second with
 inputs already resident in HBM; ``e2e`` is the same through the same calls with
@@ -35,6 +36,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 HBM_FALLBACK_GBS = 6800.0
+# DRAM bytes (read + write) per launch of a kernel, from the ncu captures
+# summarised under profiles/ (None where no capture of the current kernel)
+TRAFFIC_BYTES = {}
 BF16_FALLBACK_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -42,8 +46,8 @@ L2_BYTES = 129 * 1024 * 1024
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=18)
-    ap.add_argument("--warmup", type=int, default=9)
+    ap.add_argument("--steps", type=int, default=3600)
+    ap.add_argument("--warmup", type=int, default=90)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama2_7b",
                     choices=["llama2_7b", "decode_stress", "mistral_7b"])
@@ -54,46 +58,29 @@ def parse_args():
 
 
 # ---------------------------------------------------------------------------
-# pass stream: the workload's passes, one after another
+# the workload's cycle of passes
 # ---------------------------------------------------------------------------
-class PassStream:
-    """Yields the states of successive passes of a scenario.
-
-    llama2_7b: the prompt is re-issued under a new id once it completes.
-    decode_stress / mistral_7b: the same pass shape every step (decodes grow
-    by one token; prompt chunks restart at their first chunk under new ids).
-    """
-
-    def __init__(self, scn):
-        self.scn = scn
-        self.states = list(scn.requests)
-        self.next_id = 10_000_000
-        self.initial = {s: (pl, seen) for s, pl, seen in scn.requests}
-
-    def advance(self, seq_ids, n_new, release):
-        n = dict(zip([int(x) for x in seq_ids], [int(x) for x in n_new]))
-        out = []
-        for sid, pl, seen in self.states:
-            seen2 = seen + n.get(sid, 0)
-            prefilling = seen < pl
-            if prefilling and (seen2 >= pl or self.scn.name != "llama2_7b"):
-                # prompt done (or, for single-pass shapes, chunk done): a fresh
-                # request of the same shape replaces it
-                release(sid)
-                pl0, seen0 = self.initial.get(sid, (pl, 0))
-                if seen0 > 0:
-                    # a prompt with a cached prefix: keep the prefix sequence
-                    # itself and restart from its prefix is not possible, so a
-                    # new id is registered with the prefix by the caller
-                    out.append(("reprefix", sid, pl0, seen0))
-                else:
-                    nid = self.next_id
-                    self.next_id += 1
-                    self.initial[nid] = (pl0, 0)
-                    out.append((nid, pl0, 0))
-                continue
-            out.append((sid, pl, seen2))
-        self.states = out
+def cycle_states(scn, compose, rollback):
+    """States of one cycle of passes, found by composing them once and rolling
+    them back.  llama2_7b: the passes that carry the prompt from its first to
+    its last chunk next to the decodes (9 passes).  Other workloads: one pass.
+    Returns ([states per pass], [metadata per pass])."""
+    states = list(scn.requests)
+    out, metas, made = [], [], []
+    while True:
+        m = compose(scn.budget, scn.max_chunk, states)
+        made.append(m)
+        meta = m.meta if hasattr(m, "meta") else m
+        out.append(list(states))
+        metas.append(meta)
+        n = dict(zip([int(x) for x in meta.seq_ids], [int(x) for x in meta.n_new]))
+        states = [(sid, pl, seen + n.get(sid, 0)) for sid, pl, seen in states]
+        prompts_left = any(seen < pl for _, pl, seen in states)
+        if scn.name != "llama2_7b" or not prompts_left:
+            break
+    for m in reversed(made):
+        rollback(m)
+    return out, metas
 
 
 # ---------------------------------------------------------------------------
@@ -131,7 +118,7 @@ def read_peaks():
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -148,12 +135,14 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen between wall-clock
+        times t0 and t1 (all samples when not given)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -162,19 +151,24 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
+        import datetime
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, cmax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                if t0 is not None and not (t0 <= ts <= t1):
+                    continue
+                sm.append(clk)
+                mx.append(cmax)
+                for n, v in zip(names, parts[6:10]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
         os.unlink(self.path)
@@ -219,14 +213,18 @@ def step_work(meta, shape):
 # our arm
 # ---------------------------------------------------------------------------
 class GpuRunner:
+    """Runs the workload's cycle of passes through the library, again and
+    again: after the last pass of a cycle the cycle's passes are rolled back on
+    the composer (newest first), so every cycle composes, appends and attends
+    exactly the same passes.  Each step is one whole pass."""
+
     def __init__(self, rbkv, scn, seed, device):
         import torch
         import workloads
         self.torch = torch
         self.rbkv = rbkv
         self.scn = scn
-        self.shape = scn.shape
-        sh = scn.shape
+        self.shape = sh = scn.shape
         self.cfg = rbkv.Config(sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.block_size,
                                sh.dtype, scn.num_blocks)
         self.comp = rbkv.Composer(self.cfg)
@@ -236,73 +234,66 @@ class GpuRunner:
         self.device = device
         self.seed = seed
         self.stream = torch.cuda.current_stream()
+        self.h_stream = rbkv._P(self.stream.cuda_stream)
         b, st = scn.registration()
         if b:
             p = self.comp.compose(b, 0, st)
             k, v = workloads.make_qkv(sh, p.num_tokens, seed, 0, device=device, which="kv")
             rbkv.kv_append(p, k, v, self.kc, self.vc)
-            del k, v
-        self.ps = PassStream(scn)
-        self.max_T = scn.budget
+            torch.cuda.synchronize()
+            del k, v, p
+        states, metas = cycle_states(scn, self.comp.compose, self.comp.rollback)
+        self.cycle = [rbkv.seq_states(st) for st in states]
+        self.work = [step_work(m, sh) for m in metas]
+        self.T = [int(m.q_start[-1]) for m in metas]
+        self.max_T = max(self.T)
+        self.pending = []
         self.ws = torch.empty(256 << 20, dtype=torch.uint8, device=device)
         self.o = torch.empty((self.max_T, sh.num_heads_q, sh.head_dim), dtype=dt, device=device)
+        # one input set per pass of the cycle, reused every cycle
+        self.inputs = []
+        for k in range(len(self.cycle)):
+            q, kk, vv = workloads.make_qkv(sh, self.T[k], seed, 100 + k, device=device)
+            self.inputs.append((q, kk, vv, self.o[:self.T[k]]))
         torch.cuda.synchronize()
 
-    def make_inputs(self, n, base_index):
-        import workloads
+    def step(self, i, host=None):
+        """Pass i of the run (position i % cycle length).  With ``host`` =
+        (q_h, k_h, v_h, o_h) pinned tensors, Q/K/V are copied in and O out."""
+        rbkv = self.rbkv
+        kpos = i % len(self.cycle)
+        q, k, v, o = self.inputs[kpos]
+        p = self.comp.compose(self.scn.budget, self.scn.max_chunk, self.cycle[kpos])
+        if host is not None:
+            q_h, k_h, v_h, o_h = host[kpos]
+            q.copy_(q_h, non_blocking=True)
+            k.copy_(k_h, non_blocking=True)
+            v.copy_(v_h, non_blocking=True)
+        rbkv.kv_append(p, k, v, self.kc, self.vc, stream=self.h_stream)
+        rbkv.ragged_attention(p, q, self.kc, self.vc, o=o, workspace=self.ws,
+                              stream=self.h_stream)
+        if host is not None:
+            o_h.copy_(o, non_blocking=True)
+        self.pending.append(p)
+        if kpos == len(self.cycle) - 1:
+            for pp in reversed(self.pending):
+                self.comp.rollback(pp)
+            self.pending.clear()
+        return self.T[kpos]
+
+    def host_sets(self):
         sets = []
-        for i in range(n):
-            sets.append(workloads.make_qkv(self.shape, self.max_T, self.seed, base_index + i,
-                                           device=self.device))
+        for q, k, v, o in self.inputs:
+            sets.append((q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory(),
+                         self.torch.empty(o.shape, dtype=o.dtype).pin_memory()))
         return sets
 
-    def _resolve_states(self):
-        # a prompt with a cached prefix is re-registered under a new id
-        states = []
-        for st in self.ps.states:
-            if st[0] == "reprefix":
-                _, old, pl, seen0 = st
-                nid = self.ps.next_id
-                self.ps.next_id += 1
-                p = self.comp.compose(seen0, 0, [(nid, seen0, 0)])
-                import workloads
-                k, v = workloads.make_qkv(self.shape, seen0, self.seed, 1, device=self.device,
-                                          which="kv")
-                self.rbkv.kv_append(p, k, v, self.kc, self.vc, stream=self.stream)
-                self.ps.initial[nid] = (pl, seen0)
-                states.append((nid, pl, seen0))
-            else:
-                states.append(st)
-        self.ps.states = states
-        return states
-
-    def step(self, inputs, work_acc=None, host=None):
-        """One pass.  ``inputs`` = (q, k, v) device tensors of max_T rows, or
-        with ``host`` = (q_h, k_h, v_h, o_h) pinned tensors copied in and out."""
-        rbkv = self.rbkv
-        states = self._resolve_states()
-        p = self.comp.compose(self.scn.budget, self.scn.max_chunk, states)
-        T = p.num_tokens
-        q, k, v = inputs
-        if host is not None:
-            q_h, k_h, v_h, o_h = host
-            q[:T].copy_(q_h[:T], non_blocking=True)
-            k[:T].copy_(k_h[:T], non_blocking=True)
-            v[:T].copy_(v_h[:T], non_blocking=True)
-        rbkv.kv_append(p, k[:T], v[:T], self.kc, self.vc, stream=self.stream)
-        need = p.workspace_bytes()
-        if need > self.ws.numel():
-            raise RuntimeError(f"workspace {need} > {self.ws.numel()}")
-        rbkv.ragged_attention(p, q[:T], self.kc, self.vc, o=self.o[:T], workspace=self.ws,
-                              stream=self.stream)
-        if host is not None:
-            o_h[:T].copy_(self.o[:T], non_blocking=True)
-        if work_acc is not None:
-            w = step_work(p.meta, self.shape)
-            for kk, vv in w.items():
-                work_acc[kk] = work_acc.get(kk, 0) + vv
-        self.ps.advance(p.meta.seq_ids, p.meta.n_new, self.comp.release)
-        return T
+    def work_of(self, first, count):
+        acc = {}
+        for i in range(first, first + count):
+            for kk, vv in self.work[i % len(self.work)].items():
+                acc[kk] = acc.get(kk, 0) + vv
+        return acc
 
 
 def run_ours(args, rank, world, local_rank):
@@ -321,68 +312,72 @@ def run_ours(args, rank, world, local_rank):
     scn = workloads.SCENARIOS[args.workload](args.seed)
     run = GpuRunner(rbkv, scn, args.seed, device)
     W, K = args.warmup, args.steps
-    inputs = run.make_inputs(W + K, 100)
+    ncyc = len(run.cycle)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    for i in range(W):
-        run.step(inputs[i])
+    i = 0
+    for _ in range(W):
+        run.step(i)
+        i += 1
     torch.cuda.synchronize()
 
     # ---- timed region: K passes, inputs resident in HBM -----------------
     rbkv.profile_reset()
     rbkv.profile_enable(True)
     clocks = ClockSampler(local_rank)
-    work = {}
     barrier()
     torch.cuda.synchronize()
     clocks.start()
+    time.sleep(0.5)                      # the sampler starts before the timed region
     launches0 = rbkv.kernel_launches()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    first = i
+    wall_t0 = time.time()
     wall0 = time.perf_counter()
     t_start.record(run.stream)
     tokens = 0
-    for i in range(K):
-        tokens += run.step(inputs[W + i], work)
+    for _ in range(K):
+        tokens += run.step(i)
+        i += 1
     t_end.record(run.stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    wall_t1 = time.time()
     barrier()
     launches = rbkv.kernel_launches() - launches0
-    clk = clocks.stop()
+    clk = clocks.stop(wall_t0, wall_t1)
     rbkv.profile_enable(False)
     prof = rbkv.profile_read()
     ms = t_start.elapsed_time(t_end)
+    work = run.work_of(first, K)
 
-    # ---- e2e: same passes through the same calls, host buffers ----------
-    del inputs
-    dev_bufs = run.make_inputs(1, 5000)[0]
-    host_sets = []
-    for i in range(min(K, 6)):
-        q, k, v = run.make_inputs(1, 6000 + i)[0]
-        host_sets.append((q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory(),
-                          torch.empty(run.o.shape, dtype=run.o.dtype).pin_memory()))
-    for i in range(2):
-        run.step(dev_bufs, host=host_sets[i % len(host_sets)])
+    # ---- e2e: the same passes through the same calls, host buffers ------
+    host = run.host_sets()
+    for _ in range(ncyc):
+        run.step(i, host=host)
+        i += 1
     torch.cuda.synchronize()
-    e2e_work = {}
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_first = i
     e0.record(run.stream)
     e2e_tokens = 0
-    for i in range(K):
-        e2e_tokens += run.step(dev_bufs, e2e_work, host=host_sets[i % len(host_sets)])
+    for _ in range(K):
+        e2e_tokens += run.step(i, host=host)
+        i += 1
     e1.record(run.stream)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1)
     sh = scn.shape
     esz = 2 if sh.dtype == "bf16" else 4
+    e2e_work = run.work_of(e2e_first, K)
     h2d = e2e_work["tokens"] * (sh.num_heads_q + 2 * sh.num_heads_kv) * sh.head_dim * esz / K
     d2h = e2e_work["tokens"] * sh.num_heads_q * sh.head_dim * esz / K
 
@@ -391,9 +386,9 @@ def run_ours(args, rank, world, local_rank):
                      device=device)
     if world > 1:
         mx = t.clone()
-        torch.distributed.all_reduce(mx[:2], op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
         sm = t.clone()
-        torch.distributed.all_reduce(sm[2:], op=torch.distributed.ReduceOp.SUM)
+        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
         ms, e2e_ms = float(mx[0]), float(mx[1])
         tot_tokens, tot_e2e = float(sm[2]), float(sm[3])
     else:
@@ -402,26 +397,25 @@ def run_ours(args, rank, world, local_rank):
         return
 
     hbm, bf16, bf16_sus, src = read_peaks()
-    # dominant kernel by device time
     kinds = {k: v for k, v in prof.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
     avg_s = dom_ms / dom_n / 1e3
-    if dom in ("chunk",):
+    if dom == "chunk":
         per_launch = work["chunk_flops"] / dom_n
-        achieved = per_launch / avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_sus, "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": per_launch / avg_s / 1e12, "peak": bf16_sus,
+                "unit": "TFLOP/s"}
     else:
         key = {"decode": "decode_bytes", "generic": "kv_read_bytes",
                "kv_append": "append_bytes", "combine": "decode_bytes"}[dom]
         per_launch = work[key] / dom_n
-        achieved = per_launch / avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": per_launch / avg_s / 1e9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = TRAFFIC_BYTES.get((args.workload, dom))
     roof["kernel"] = dom
     roof["peak_source"] = src
     roof["avg_launch_us"] = avg_s * 1e6
+    roof["algorithmic_per_launch"] = per_launch
 
     line = {
         "metric": "ragged SplitFuse attention pass tokens/s",
@@ -439,11 +433,13 @@ def run_ours(args, rank, world, local_rank):
         "config": {
             "workload": f"{scn.name}: {sh.num_heads_q}q/{sh.num_heads_kv}kv heads, head_dim "
                         f"{sh.head_dim}, block {sh.block_size}, budget {scn.budget}, chunk cap "
-                        f"{scn.max_chunk}",
+                        f"{scn.max_chunk}; a cycle of {ncyc} passes repeated (rolled back "
+                        "on the composer after each cycle)",
             "tokens_per_step": tot_tokens / K / world,
             "kv_read_gb_per_step": work["kv_read_bytes"] / K / 1e9,
             "kv_read_gbs": work["kv_read_bytes"] / (ms / 1e3) / 1e9,
             "kv_read_frac_of_hbm": work["kv_read_bytes"] / (ms / 1e3) / 1e9 / hbm,
+            "chunk_tflops": work["chunk_flops"] / (kinds.get("chunk", (1e30, 1))[0] / 1e3) / 1e12,
             "l2": "inputs larger than L2 (each pass reads "
                   f"{work['kv_read_bytes'] / K / 1e6:.0f} MB of KV > 129 MB L2); no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -466,12 +462,14 @@ def run_ours(args, rank, world, local_rank):
 # the oracle on the host cores (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 class OracleRunner:
-    """The fp64 oracle driven through the same pass stream.
+    """The fp64 oracle driven through the same cycle of passes (rolled back on
+    the oracle composer after each cycle).
 
     A step is one pass: oracle composition and appending of the whole pass,
-    and oracle attention for a sample of its rows - every decode row and every
-    32nd prompt-chunk row - so that one step costs about a second.  Tokens
-    counted are the rows whose outputs were computed."""
+    then oracle attention for ``pairs`` (row, query head) outputs of it, taken
+    in row-major order and continuing from step to step, so that every row and
+    head of the cycle is covered in turn.  A token counts as 1/H_q per output
+    pair computed."""
 
     def __init__(self, scn, seed):
         import numpy as np
@@ -479,11 +477,8 @@ class OracleRunner:
         import workloads
         self.np = np
         self.oracle = oracle
-        self.workloads = workloads
         self.scn = scn
-        sh = scn.shape
-        self.shape = sh
-        self.seed = seed
+        self.shape = sh = scn.shape
         self.comp = oracle.Composer(sh.block_size, scn.num_blocks)
         storage = np.uint16 if sh.dtype == "bf16" else np.float32
         self.kc = oracle.BlockedCache(sh.num_heads_kv, sh.block_size, sh.head_dim, storage)
@@ -493,8 +488,15 @@ class OracleRunner:
             m = self.comp.compose(b, 0, st)
             k, v = workloads.make_qkv(sh, m.num_tokens, seed, 0, which="kv")
             oracle.kv_append(m, self._st(k), self._st(v), self.kc, self.vc)
-        self.ps = PassStream(scn)
-        self.q, self.k, self.v = workloads.make_qkv(sh, scn.budget, seed, 100)
+        self.cycle, metas = cycle_states(scn, self.comp.compose, self.comp.rollback)
+        self.inputs = []
+        for k in range(len(self.cycle)):
+            T = int(metas[k].q_start[-1])
+            q, kk, vv = workloads.make_qkv(sh, T, seed, 100 + k)
+            self.inputs.append((self._st(q), self._st(kk), self._st(vv)))
+        self.pending = []
+        self.i = 0
+        self.cursor = 0      # next (row * H_q + head) to compute, per pass
 
     def _st(self, t):
         import torch
@@ -503,52 +505,50 @@ class OracleRunner:
             return t.view(torch.int16).numpy().view(self.np.uint16)
         return t.numpy()
 
-    def _resolve(self):
-        states = []
-        for st in self.ps.states:
-            if st[0] == "reprefix":
-                _, old, pl, seen0 = st
-                nid = self.ps.next_id
-                self.ps.next_id += 1
-                m = self.comp.compose(seen0, 0, [(nid, seen0, 0)])
-                k, v = self.workloads.make_qkv(self.shape, seen0, self.seed, 1, which="kv")
-                self.oracle.kv_append(m, self._st(k), self._st(v), self.kc, self.vc)
-                self.ps.initial[nid] = (pl, seen0)
-                states.append((nid, pl, seen0))
-            else:
-                states.append(st)
-        self.ps.states = states
-        return states
-
-    def step(self):
-        states = self._resolve()
-        m = self.comp.compose(self.scn.budget, self.scn.max_chunk, states)
-        T = m.num_tokens
-        k, v, q = self._st(self.k[:T]), self._st(self.v[:T]), self._st(self.q[:T])
+    def step(self, pairs):
+        kpos = self.i % len(self.cycle)
+        self.i += 1
+        m = self.comp.compose(self.scn.budget, self.scn.max_chunk, self.cycle[kpos])
+        q, k, v = self.inputs[kpos]
         self.oracle.kv_append(m, k, v, self.kc, self.vc)
-        rows = []
-        for s in range(m.num_seqs):
-            a, n = m.q_start[s], m.n_new[s]
-            rows.extend(range(a, a + n) if n == 1 else range(a, a + n, 32))
-        self.oracle.blocked_attention(m, q, self.kc, self.vc, self.shape.num_heads_q, tokens=rows)
-        self.ps.advance(m.seq_ids, m.n_new, self.comp.release)
-        return len(rows)
+        H = self.shape.num_heads_q
+        total = m.num_tokens * H
+        done = 0
+        while done < pairs and total:
+            c = self.cursor % total
+            t, h0 = divmod(c, H)
+            n = min(pairs - done, H - h0)
+            self.oracle.blocked_attention(m, q, self.kc, self.vc, H, tokens=[t],
+                                          heads=range(h0, h0 + n))
+            done += n
+            self.cursor += n
+        self.pending.append(m)
+        if kpos == len(self.cycle) - 1:
+            for mm in reversed(self.pending):
+                self.comp.rollback(mm)
+            self.pending.clear()
+        return done / H
 
 
-def oracle_measure(workload, seed, steps, warmup):
+def oracle_measure(workload, seed, steps, warmup, pair_budget=2000):
+    """Time ``steps`` oracle steps after ``warmup``; each step computes
+    max(1, pair_budget // (steps + warmup)) output pairs, so the whole run
+    stays within a few minutes whatever the step count."""
     import workloads
     scn = workloads.SCENARIOS[workload](seed)
+    pairs = max(1, pair_budget // max(1, steps + warmup))
     t0 = time.perf_counter()
     r = OracleRunner(scn, seed)
     setup = time.perf_counter() - t0
     for _ in range(warmup):
-        r.step()
+        r.step(pairs)
     t0 = time.perf_counter()
-    rows = 0
+    tokens = 0.0
     for _ in range(steps):
-        rows += r.step()
+        tokens += r.step(pairs)
     dt = time.perf_counter() - t0
-    return {"value": rows / dt, "rows": rows, "seconds": dt, "setup_seconds": setup}
+    return {"value": tokens / dt, "tokens": tokens, "pairs_per_step": pairs, "seconds": dt,
+            "setup_seconds": setup}
 
 
 def cpu_env():
@@ -570,9 +570,9 @@ def cpu_baseline_subprocess(args, steps=5, warmup=1):
                 "sample": f"failed: {e}"}
     return {"value": res["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{steps} passes after {warmup} warm-up; per pass the oracle composes and "
-                      "appends the whole pass and computes attention for every decode row and "
-                      f"every 32nd prompt-chunk row ({res['rows']} rows in {res['seconds']:.1f} s); "
-                      "value = rows / s; one thread (BLAS threads = 1)"}
+                      f"appends the whole pass and computes {res['pairs_per_step']} (row, head) "
+                      f"outputs ({res['tokens']:.1f} tokens in {res['seconds']:.1f} s; a token "
+                      "counts 1/H_q per output); one thread (BLAS threads = 1)"}
 
 
 def run_reference(args, rank):
@@ -601,9 +601,9 @@ def run_reference(args, rank):
                                f"{sh.head_dim}, block {sh.block_size}, budget {scn.budget}, chunk "
                                f"cap {scn.max_chunk}"},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "per pass: whole-pass composition and append, attention for "
-                                   "every decode row and every 32nd prompt-chunk row; value = "
-                                   "rows / s; one thread"},
+                         "sample": f"per pass: whole-pass composition and append, then "
+                                   f"{res['pairs_per_step']} (row, head) outputs; a token counts "
+                                   "1/H_q per output; one thread (BLAS threads = 1)"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

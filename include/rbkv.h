@@ -156,6 +156,14 @@ rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t ma
                               const rbkv_seq_state* states, int32_t n_states,
                               rbkv_pass** out);
 
+/* Undo what composing pass p did to the composer: each of its sequences goes
+ * back to its `seen` tokens and returns the blocks the pass gave it (a
+ * sequence first seen in p is forgotten).  The caller's cache contents are not
+ * touched.  Passes must be rolled back newest first; if a sequence of p was
+ * changed by a later pass, returns RBKV_ERR_INVALID and changes nothing.
+ * Composing the same states again afterwards yields the same metadata. */
+rbkv_status rbkv_pass_rollback(rbkv_composer* c, const rbkv_pass* p);
+
 /* Return every block of seq_id to the pool and forget the sequence.
  * Errors: RBKV_ERR_INVALID for an unknown id. */
 rbkv_status rbkv_release_seq(rbkv_composer* c, int64_t seq_id);

@@ -156,6 +156,26 @@ class Composer:
                 meta.slot.append(blocks[p // B] * B + p % B)
         return meta
 
+    def rollback(self, meta: PassMeta) -> None:
+        """Undo composing ``meta``: each of its sequences returns to ``seen``
+        tokens and gives back the blocks the pass allocated (newest last in its
+        list); a sequence that started in this pass is forgotten.  Fails, with
+        no change, if a later pass moved any of them."""
+        for s in range(meta.num_seqs):
+            if self._tokens.get(meta.seq_ids[s]) != meta.ctx[s]:
+                raise InvalidRequest(f"sequence {meta.seq_ids[s]} changed after this pass")
+        B = self.block_size
+        for s in reversed(range(meta.num_seqs)):
+            sid, seen = meta.seq_ids[s], meta.seen[s]
+            held = self._held.get(sid, [])
+            while len(held) > -(-seen // B):
+                heapq.heappush(self._free, held.pop())
+            if seen == 0:
+                self._tokens.pop(sid, None)
+                self._held.pop(sid, None)
+            else:
+                self._tokens[sid] = seen
+
     def release(self, seq_id: int) -> None:
         """Return every block of ``seq_id`` to the pool and forget it."""
         sid = int(seq_id)

@@ -73,6 +73,7 @@ SIGNATURES = {
     "rbkv_compose_pass": (C.c_int, [_P, C.c_int32, C.c_int32, C.POINTER(_SeqState), C.c_int32,
                                     C.POINTER(_P)]),
     "rbkv_release_seq": (C.c_int, [_P, C.c_int64]),
+    "rbkv_pass_rollback": (C.c_int, [_P, _P]),
     "rbkv_composer_free_blocks": (C.c_int32, [_P]),
     "rbkv_pass_get_meta": (C.c_int, [_P, C.POINTER(_PassMeta)]),
     "rbkv_pass_set_split_keys": (C.c_int, [_P, C.c_int32]),
@@ -178,18 +179,23 @@ class Pass:
     def __init__(self, handle: int, config: Config):
         self._h = _P(handle)
         self.config = config
-        m = _PassMeta()
-        _check(lib().rbkv_pass_get_meta(self._h, C.byref(m)))
-        S, T = m.num_seqs, m.num_tokens
-        self.meta = PassMeta(_arr(m.seq_ids, S, np.int64), _arr(m.q_start, S + 1, np.int32),
-                             _arr(m.n_new, S, np.int32), _arr(m.seen, S, np.int32),
-                             _arr(m.ctx, S, np.int32), _arr(m.block_start, S + 1, np.int32),
-                             _arr(m.block_ids, m.num_block_ids, np.int32),
-                             _arr(m.slot, T, np.int32))
+        self._view = _PassMeta()
+        _check(lib().rbkv_pass_get_meta(self._h, C.byref(self._view)))
+        self.num_tokens = int(self._view.num_tokens)
+        self._meta = None
 
     @property
-    def num_tokens(self) -> int:
-        return self.meta.num_tokens
+    def meta(self) -> PassMeta:
+        """Copies of the pass's metadata arrays (made on first access)."""
+        if self._meta is None:
+            m = self._view
+            S, T = m.num_seqs, m.num_tokens
+            self._meta = PassMeta(_arr(m.seq_ids, S, np.int64), _arr(m.q_start, S + 1, np.int32),
+                                  _arr(m.n_new, S, np.int32), _arr(m.seen, S, np.int32),
+                                  _arr(m.ctx, S, np.int32), _arr(m.block_start, S + 1, np.int32),
+                                  _arr(m.block_ids, m.num_block_ids, np.int32),
+                                  _arr(m.slot, T, np.int32))
+        return self._meta
 
     def set_split_keys(self, keys: int) -> None:
         _check(lib().rbkv_pass_set_split_keys(self._h, int(keys)))
@@ -222,6 +228,20 @@ class Pass:
             pass
 
 
+class SeqStates:
+    """A request list in the library's layout (see ``seq_states``)."""
+
+    def __init__(self, arr, n):
+        self.arr, self.n = arr, n
+
+
+def seq_states(states: Sequence[Tuple[int, int, int]]) -> SeqStates:
+    arr = (_SeqState * max(1, len(states)))()
+    for i, (sid, plen, seen) in enumerate(states):
+        arr[i] = _SeqState(int(sid), int(plen), int(seen))
+    return SeqStates(arr, len(states))
+
+
 class Composer:
     """Dynamic SplitFuse composer and block pool of one cache layout."""
 
@@ -232,15 +252,20 @@ class Composer:
         _check(lib().rbkv_composer_create(C.byref(cfg), C.byref(h)))
         self._h = h
 
-    def compose(self, budget: int, max_chunk: int,
-                states: Sequence[Tuple[int, int, int]]) -> Pass:
-        arr = (_SeqState * max(1, len(states)))()
-        for i, (sid, plen, seen) in enumerate(states):
-            arr[i] = _SeqState(int(sid), int(plen), int(seen))
+    def compose(self, budget: int, max_chunk: int, states) -> Pass:
+        """``states``: [(seq_id, prompt_len, seen), ...] in list order, or an
+        array made once with ``seq_states`` (cheaper when reused)."""
+        if not isinstance(states, SeqStates):
+            states = seq_states(states)
         out = _P()
-        _check(lib().rbkv_compose_pass(self._h, int(budget), int(max_chunk), arr, len(states),
+        _check(lib().rbkv_compose_pass(self._h, int(budget), int(max_chunk), states.arr, states.n,
                                        C.byref(out)))
         return Pass(out.value, self.config)
+
+    def rollback(self, p: Pass) -> None:
+        """Undo what composing ``p`` did to the pool and the recorded contexts
+        (newest pass first)."""
+        _check(lib().rbkv_pass_rollback(self._h, p._h))
 
     def release(self, seq_id: int) -> None:
         _check(lib().rbkv_release_seq(self._h, int(seq_id)))
@@ -261,6 +286,8 @@ class Composer:
 
 
 def _stream(stream):
+    if isinstance(stream, _P):
+        return stream
     if stream is None:
         import torch
         return _P(torch.cuda.current_stream().cuda_stream)
@@ -356,5 +383,5 @@ def profile_read() -> dict:
     return out
 
 
-__all__ = ["ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+__all__ = ["seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
            "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_q,
                               const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
-                              ShapeInfo shp, __nv_bfloat16* __restrict__ o) {
+                              ShapeInfo shp, __nv_bfloat16* __restrict__ o,
+                              float* __restrict__ part_o, float* __restrict__ part_lse) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -165,8 +166,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int h = blockIdx.y;
   const int kvh = h / shp.g;
   const int B = shp.B;
-  const int n_keys = tile.pos_begin + tile.n_rows;
-  const int n_kv = (n_keys + kKeys - 1) / kKeys;
+  // keys of this split: [kb, ke); the last row of the tile sees keys < pos_begin + n_rows
+  const int kb = tile.key_begin;
+  const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
+  const int n_kv = (ke - kb + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         int32_t rows[kKeys / 8];
         int nsub = 0, loads = 0;
         for (int r = 0; r < kKeys; r += box_rows) {
-          const int key = j * kKeys + r;
-          if (key >= n_keys) break;
+          const int key = kb + j * kKeys + r;
+          if (key >= ke) break;
           const int32_t blk = table[key / B];
           if (blk < 0 || blk >= dp.num_blocks) {
             atomicCAS(dp.status, 0, kDevBounds);
@@ -323,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld32(lane_base + (j & 1) * kKeys, sc);
       tmem_ld32(lane_base + (j & 1) * kKeys + 32, sc + 32);
       tmem_wait_ld();
-      const int key0 = j * kKeys;
+      const int key0 = kb + j * kKeys;
       float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const int key = key0 + c;
-        sc[c] = (key <= pos && key < n_keys) ? sc[c] * qk_scale : -INFINITY;
+        sc[c] = (key <= pos && key < ke) ? sc[c] * qk_scale : -INFINITY;
         mt = fmaxf(mt, sc[c]);
       }
       float corr = 1.f;
@@ -337,10 +340,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         corr = exp2f(m_ref - mt);
         m_ref = mt;
       }
+      // a row with no key in this split so far keeps m_ref = -inf: its p are 0
+      const float base = m_ref == -INFINITY ? 0.f : m_ref;
       float ps = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        sc[c] = exp2f(sc[c] - m_ref);
+        sc[c] = exp2f(sc[c] - base);
         ps += sc[c];
       }
       l = l * corr + ps;
@@ -365,12 +370,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_wait_st();
         }
       }
-      if (j == n_kv - 1 && (n_keys % kKeys) != 0) {
-        // keys past the last row may be anything (unwritten slots): zero their V rows
+      if (j == n_kv - 1 && (ke % kKeys) != 0) {
+        // keys past the split's end may be anything (unwritten slots): zero their V rows
         const int s = j % kStages;
         ptx::mbar_wait(&bars->kv_full[s], (j / kStages) & 1, kWaitLimit);
         uint8_t* vt = kv_s + s * kStage + kKVTile;
-        const int valid = n_keys - key0;
+        const int valid = ke - key0;
         for (int e = row; e < (kKeys - valid) * 16; e += kRows) {
           const int key = valid + e / 16, c = e % 16;
           *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVHalf + key * 128 + ((c & 7) << 4)) =
@@ -398,13 +403,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool store = row < tile.n_rows;
+      const bool partial = tile.part_base >= 0;
       __nv_bfloat16* orow = o + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128;
+      // partial slot of (row, KV head, split); query head h % g inside it
+      const int64_t slot =
+          ((int64_t)tile.part_base + ((int64_t)row * shp.H_kv + kvh) * tile.nsplit + tile.split) *
+              shp.g + (h % shp.g);
+      float* prow = part_o + slot * 128;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float ov[32];
         tmem_ld32(lane_base + kOCol + c4 * 32, ov);
         tmem_wait_ld();
-        if (store) {
+        if (store && !partial) {
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
             uint4 v;
@@ -414,8 +425,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             v.w = ptx::pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
             *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = v;
           }
+        } else if (store) {
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<float4*>(prow + c4 * 32 + c8 * 4) =
+                make_float4(ov[c8 * 4 + 0] * inv, ov[c8 * 4 + 1] * inv, ov[c8 * 4 + 2] * inv,
+                            ov[c8 * 4 + 3] * inv);
         }
       }
+      if (store && partial) part_lse[slot] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
     } else if (!ok || n_kv > 0) {
       atomicCAS(dp.status, 0, kDevTimeout);
       *abort_flag = 1;
@@ -440,8 +458,8 @@ bool chunk_fast_supported(const ShapeInfo& s) {
 }
 
 cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
-                              const void* k_cache, const void* v_cache, void* o,
-                              cudaStream_t st) {
+                              const void* k_cache, const void* v_cache, void* o, float* part_o,
+                              float* part_lse, cudaStream_t st) {
   if (!chunk_fast_supported(s)) return cudaErrorNotSupported;
   if (dp.n_chunk == 0) return cudaSuccess;
   if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
@@ -464,7 +482,8 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   }
   dim3 grid(dp.n_chunk, s.H_q);
   chunk_attn_tcgen05_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, dp, s,
-                                                                (__nv_bfloat16*)o);
+                                                                (__nv_bfloat16*)o, part_o,
+                                                                part_lse);
   return cudaGetLastError();
 }
 

@@ -268,6 +268,9 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
     split = std::max<int32_t>(512, round_up(std::max<int64_t>(target, 1), gran));
   }
 
+  // prompt-chunk tiles: fixed split length unless the caller forced one
+  const int32_t chunk_split = p.split_keys > 0 ? round_up(p.split_keys, kChunkTileKeys)
+                                               : kChunkSplitKeys;
   std::vector<int32_t> bounds;
   std::vector<WorkItem> decode, generic;
   int32_t max_splits = 0;
@@ -290,9 +293,28 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
     if (p.n_new[i] == 1) {
       add_row(p.q_start[i], p.ctx[i], p.block_start[i], fast_decode ? decode : generic);
     } else if (fast_chunk) {
+      // 128-row tiles; a tile's key range [0, last position + 1) is cut into
+      // 64-key-aligned pieces of at most `chunk_split` keys, merged later by
+      // the log-sum-exp combine like split decode rows
       for (int32_t r = 0; r < p.n_new[i]; r += kChunkTileRows) {
-        int32_t n = std::min(kChunkTileRows, p.n_new[i] - r);
-        pl.chunk.push_back(ChunkTile{p.block_start[i], p.q_start[i] + r, n, p.seen[i] + r});
+        const int32_t n = std::min(kChunkTileRows, p.n_new[i] - r);
+        const int32_t pos0 = p.seen[i] + r;
+        const int32_t n_keys = pos0 + n;
+        split_keys(n_keys, chunk_split, kChunkTileKeys, bounds);
+        const int32_t ns = (int32_t)bounds.size() - 1;
+        max_splits = std::max(max_splits, ns);
+        int32_t part0 = -1;
+        if (ns > 1) {
+          part0 = pl.n_parts;
+          pl.n_parts += n * s.H_kv * ns;
+          for (int32_t rr = 0; rr < n; ++rr)
+            for (int32_t h = 0; h < s.H_kv; ++h)
+              pl.combine.push_back(
+                  CombineRow{p.q_start[i] + r + rr, h, part0 + (rr * s.H_kv + h) * ns, ns});
+        }
+        for (int32_t k = 0; k < ns; ++k)
+          pl.chunk.push_back(ChunkTile{p.block_start[i], p.q_start[i] + r, n, pos0, bounds[k],
+                                       bounds[k + 1], part0, k, ns, {0, 0, 0}});
       }
     } else {
       for (int32_t j = 0; j < p.n_new[i]; ++j)
@@ -304,6 +326,9 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   };
   std::stable_sort(decode.begin(), decode.end(), longer);
   std::stable_sort(generic.begin(), generic.end(), longer);
+  std::stable_sort(pl.chunk.begin(), pl.chunk.end(), [](const ChunkTile& a, const ChunkTile& b) {
+    return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+  });
   int32_t grid = (int32_t)std::min<int64_t>((int64_t)decode.size(),
                                             (int64_t)std::max(1, num_sms) * kDecodeCtasPerSm);
   if (grid > 0) snake_order(decode, grid);
@@ -475,7 +500,10 @@ rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache
   const DevPass& dp = p->dp;
   e = cudaSuccess;
   int launched = 0;
-  if (dp.n_chunk) { e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, st); ++launched; }
+  if (dp.n_chunk) {
+    e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    ++launched;
+  }
   if (e == cudaSuccess && dp.n_decode) {
     e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
     ++launched;
@@ -614,6 +642,35 @@ rbkv_status rbkv_release_seq(rbkv_composer* c, int64_t seq_id) {
   return RBKV_OK;
 }
 
+rbkv_status rbkv_pass_rollback(rbkv_composer* c, const rbkv_pass* p) {
+  if (!c || !p) return fail(RBKV_ERR_INVALID, "composer or pass is NULL");
+  const size_t S = p->seq_ids.size();
+  // all-or-nothing: every sequence must still be exactly where this pass left it
+  for (size_t i = 0; i < S; ++i) {
+    auto it = c->tokens.find(p->seq_ids[i]);
+    if (it == c->tokens.end() || it->second != p->ctx[i])
+      return fail(RBKV_ERR_INVALID, "sequence " + std::to_string(p->seq_ids[i]) +
+                                        " changed after this pass; roll back later passes first");
+  }
+  const int32_t B = c->cfg.block_size;
+  for (size_t i = S; i-- > 0;) {
+    const int64_t sid = p->seq_ids[i];
+    std::vector<int32_t>& held = c->held[sid];
+    const size_t keep = (size_t)ceil_div(p->seen[i], B);
+    while (held.size() > keep) {
+      c->pool.give_back(held.back());
+      held.pop_back();
+    }
+    if (p->seen[i] == 0) {
+      c->tokens.erase(sid);
+      c->held.erase(sid);
+    } else {
+      c->tokens[sid] = p->seen[i];
+    }
+  }
+  return RBKV_OK;
+}
+
 rbkv_status rbkv_pass_get_meta(const rbkv_pass* p, rbkv_pass_meta* v) {
   if (!p || !v) return fail(RBKV_ERR_INVALID, "pass or view is NULL");
   v->num_seqs = (int32_t)p->seq_ids.size();
@@ -703,8 +760,9 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
   const DevPass& dp = p->dp;
   cudaError_t e = cudaSuccess;
   if (dp.n_chunk)
-    e = launch_counted(RBKV_KERNEL_CHUNK, st,
-                       [&] { return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, st); });
+    e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
+      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    });
   if (e == cudaSuccess && dp.n_decode)
     e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
       return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);

@@ -34,15 +34,26 @@ struct CombineRow {
   int32_t nsplit;
 };
 
-// Up to 128 consecutive rows of one prompt chunk (one sequence).  Row r of the
-// tile is pass row row_begin + r at position pos_begin + r; it sees keys
-// 0 .. pos_begin + r.
+// Up to 128 consecutive rows of one prompt chunk (one sequence), over the keys
+// [key_begin, key_end) of one split of their key range.  Row r of the tile is
+// pass row row_begin + r at position pos_begin + r; it sees keys
+// key_begin .. min(key_end, pos_begin + r + 1) - 1.
+// part_base < 0: the tile covers all keys; write O.  Otherwise the partial
+// output of row r, KV head k goes to slot part_base + (r * H_kv + k) * nsplit
+// + split (each slot holds the g query heads of the KV head).
 struct ChunkTile {
   int32_t table_off;
   int32_t row_begin;
   int32_t n_rows;
   int32_t pos_begin;
+  int32_t key_begin;
+  int32_t key_end;
+  int32_t part_base;
+  int32_t split;
+  int32_t nsplit;
+  int32_t pad[3];
 };
+static_assert(sizeof(ChunkTile) == 48, "ChunkTile is 12 int32");
 
 // Device view of a pass (pointers into its uploaded metadata buffer).
 struct DevPass {
@@ -88,6 +99,7 @@ constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decod
 constexpr int kDecodeCtasPerSm = 1;
 constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
 constexpr int kChunkTileKeys = 64;       // keys per tensor-core KV tile
+constexpr int kChunkSplitKeys = 2048;    // automatic key-split length of prompt-chunk tiles
 
 bool decode_fast_supported(const ShapeInfo& s);
 // 2-D view of a bf16 [num_blocks][H_kv][B][head_dim] cache for TMA: `rows`
@@ -110,7 +122,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
                                float* part_o, float* part_lse, cudaStream_t st);
 cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                               const void* k_cache, const void* v_cache, void* o,
-                              cudaStream_t st);
+                              float* part_o, float* part_lse, cudaStream_t st);
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
 

@@ -42,10 +42,13 @@ def test_scaled_scenarios_all_outputs(rbkv, name, factor, split):
     assert r["pair"].cache_equal()
 
 
-def test_chunked_prompt_over_passes(rbkv):
-    """Every pass of a prompt chunked over several passes, with decodes."""
+@pytest.mark.parametrize("split", [None, 64, 192])
+def test_chunked_prompt_over_passes(rbkv, split):
+    """Every pass of a prompt chunked over several passes, with decodes; with a
+    forced split the prompt-chunk tiles' key ranges are cut too (rows whose
+    keys all lie before a split's start get an empty piece)."""
     scn = workloads.scaled(workloads.llama2_7b(1), 8)
-    res = run_scenario(rbkv, scn, passes=9)
+    res = run_scenario(rbkv, scn, passes=9, split_keys=split)
     for r in res:
         _ok(r)
     assert res[-1]["pair"].cache_equal()

@@ -213,3 +213,40 @@ def test_plan_covers_every_row_and_head(rbkv):
     # forcing the split length changes only the plan
     p2 = comp.compose(0, 0, [])
     assert p2.plan_for_sms(152)["decode_items"] + p2.plan_for_sms(152)["generic_items"] == 0
+
+
+def test_rollback_restores_state_bit_exact(rbkv):
+    """Rolling passes back (newest first) restores the pool and contexts on both
+    sides; composing the same states again gives identical metadata."""
+    scn = workloads.scaled(workloads.llama2_7b(2), 4)
+    sh = scn.shape
+    lib_c = rbkv.Composer(rbkv.Config(sh.num_heads_q, sh.num_heads_kv, sh.head_dim,
+                                      sh.block_size, sh.dtype, scn.num_blocks))
+    orc_c = oracle.Composer(sh.block_size, scn.num_blocks)
+    b, st = scn.registration()
+    lib_c.compose(b, 0, st)
+    orc_c.compose(b, 0, st)
+    free0 = lib_c.free_blocks()
+    for cycle in range(3):
+        states = list(scn.requests)
+        passes = []
+        metas = []
+        for _ in range(6):
+            p = lib_c.compose(scn.budget, scn.max_chunk, states)
+            m = orc_c.compose(scn.budget, scn.max_chunk, states)
+            _same(p, m)
+            if cycle == 0:
+                metas.append(p.meta)
+            passes.append((p, m))
+            n = dict(zip(m.seq_ids, m.n_new))
+            states = [(sid, pl, seen + n.get(sid, 0)) for sid, pl, seen in states]
+        # the oldest pass cannot go first
+        with pytest.raises(rbkv.RbkvError):
+            lib_c.rollback(passes[0][0])
+        with pytest.raises(oracle.InvalidRequest):
+            orc_c.rollback(passes[0][1])
+        for p, m in reversed(passes):
+            lib_c.rollback(p)
+            orc_c.rollback(m)
+            assert lib_c.free_blocks() == orc_c.free_blocks()
+        assert lib_c.free_blocks() == free0

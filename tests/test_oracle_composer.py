@@ -200,3 +200,17 @@ def test_trace_conserves_tokens():
     assert npass == len(totals)
     assert sum(totals) == sum(r.prompt_len + r.output_len - 1 for r in reqs)
     assert comp.free_blocks() == workloads.trace_block_pool(reqs, 6, 64)
+
+
+def test_rollback_is_the_inverse_of_compose():
+    comp = Composer(8, 64)
+    comp.compose(20, 0, [(1, 20, 0)])
+    base = (comp.free_blocks(), comp.tokens_of(1), comp.held_blocks(1))
+    m1 = comp.compose(30, 0, [(1, 20, 20), (2, 25, 0)])
+    m2 = comp.compose(30, 10, [(1, 20, 21), (2, 25, 25), (3, 9, 0)])
+    comp.rollback(m2)
+    comp.rollback(m1)
+    assert (comp.free_blocks(), comp.tokens_of(1), comp.held_blocks(1)) == base
+    assert comp.tokens_of(2) == 0 and comp.held_blocks(2) == []
+    again = comp.compose(30, 0, [(1, 20, 20), (2, 25, 0)])
+    assert again == m1
