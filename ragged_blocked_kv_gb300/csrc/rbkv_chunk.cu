@@ -43,7 +43,8 @@ constexpr int kStage = 2 * kKVTile;         // K + V
 constexpr int kPBytes = kRows * 128;        // 128 rows x 64 keys bf16
 constexpr int kTmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
 constexpr int kOCol = 128;
-constexpr int kSmemBytes = 1024 + kQBytes + kStages * kStage + kPBytes + 256;
+// 112.25 KB: two CTAs per SM (or one next to a decode CTA)
+constexpr int kSmemBytes = kQBytes + kStages * kStage + kPBytes + 256;
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -152,9 +153,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                               const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
                               ShapeInfo shp, __nv_bfloat16* __restrict__ o,
                               float* __restrict__ part_o, float* __restrict__ part_lse) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw;
+  if (ptx::smem_u32(smem_raw) & 1023) {
+    // the swizzled operand layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(dp.status, 0, kDevBounds);
+    return;
+  }
   uint8_t* q_s = base;
   uint8_t* kv_s = q_s + kQBytes;
   uint8_t* p_s = kv_s + kStages * kStage;
@@ -477,6 +482,10 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   if (!attr_done) {
     e = cudaFuncSetAttribute(chunk_attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_attn_tcgen05_kernel,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }

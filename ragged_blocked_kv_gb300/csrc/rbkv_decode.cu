@@ -8,7 +8,9 @@
 //    work units (longest first, dealt in snake order so CTAs finish together);
 //  - a producer warp streams 64-key K and V tiles of the paged cache with TMA
 //    (2-D tiled loads through the block table, 128-byte swizzle) into a
-//    5-stage shared-memory ring guarded by mbarriers;
+//    3-stage shared-memory ring guarded by mbarriers (about 105 KB in all, so
+//    that a prompt-chunk CTA fits on the same SM and both kernels run side by
+//    side);
 //  - four consumer warps share every tile, 16 keys each (so each warp consumes
 //    the ring strictly in order); each multiplies the group's query rows
 //    (padded to 16) by its keys with warp-level bf16 MMAs (fp32 accumulation),
@@ -32,7 +34,7 @@ namespace rbkv {
 
 namespace {
 
-constexpr int kStages = 5;
+constexpr int kStages = 3;
 constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kKeys = kDecodeTileKeys;        // 64 keys per tile
@@ -40,29 +42,30 @@ constexpr int kHalf = kKeys * 128;            // 64 rows x 128 B (64 bf16 of hea
 constexpr int kTile = 2 * kHalf;              // K or V tile, head_dim 128
 constexpr int kStage = 2 * kTile;             // K + V
 constexpr int kRowPad = 132;                  // fp32 row stride of the merge scratch
-constexpr int kScratchBytes = kConsumers * 16 * kRowPad * 4;
+constexpr int kScratchBytes = 16 * kRowPad * 4;   // one [16][kRowPad] fp32 merge buffer
 constexpr int kMlBytes = kConsumers * 16 * 2 * 4;
-constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStage + kScratchBytes + kMlBytes +
-                           2 * kStages * 8;
+// about 105 KB: a prompt-chunk CTA fits on the same SM next to this one
+constexpr int kSmemBytes = kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 16;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shared {
   uint8_t* stages;     // kStages x kStage, 1024-aligned
-  float* scratch;      // [kConsumers][16][kRowPad]
+  float* scratch;      // [16][kRowPad]
   float* ml;           // [kConsumers][16][2]
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
+  volatile int* abort_flag;
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* raw) {
   Shared s;
-  uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
-  s.stages = reinterpret_cast<uint8_t*>(base);
+  s.stages = raw;
   s.scratch = reinterpret_cast<float*>(s.stages + kStages * kStage);
-  s.ml = s.scratch + kConsumers * 16 * kRowPad;
+  s.ml = s.scratch + 16 * kRowPad;
   s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * 16 * 2);
   s.empty = s.full + kStages;
+  s.abort_flag = reinterpret_cast<volatile int*>(s.empty + kStages);
   return s;
 }
 
@@ -79,16 +82,21 @@ __device__ __forceinline__ uint32_t tile_off(int key, int d) {
   return half * kHalf + key * 128 + ((chunk ^ (key & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DevPass dp, ShapeInfo shp,
                           const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o,
                           float* __restrict__ part_o, float* __restrict__ part_lse) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   Shared sm = carve(smem_raw);
-  volatile __shared__ int abort_flag;
+  volatile int& abort_flag = *sm.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = shp.g, B = shp.B, H_kv = shp.H_kv;
+  if (ptx::smem_u32(smem_raw) & 1023) {
+    // the swizzled tile layout needs a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(dp.status, 0, kDevBounds);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -317,30 +325,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - M0) / L0;
     const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - M1) / L1;
-    float* scr = sm.scratch + warp * 16 * kRowPad;
+    // the four warps add their scaled O into one buffer, one warp at a time
+    float* scr = sm.scratch;
+    for (int w = 0; w < kConsumers; ++w) {
+      if (warp == w) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int d = i * 8 + cq;
-      if (r0 < g)
-        *reinterpret_cast<float2*>(scr + r0 * kRowPad + d) =
-            make_float2(acc_o[i][0] * f0, acc_o[i][1] * f0);
-      if (r1 < g)
-        *reinterpret_cast<float2*>(scr + r1 * kRowPad + d) =
-            make_float2(acc_o[i][2] * f1, acc_o[i][3] * f1);
+        for (int i = 0; i < 16; ++i) {
+          const int d = i * 8 + cq;
+          if (r0 < g) {
+            float2* a = reinterpret_cast<float2*>(scr + r0 * kRowPad + d);
+            const float2 prev = w ? *a : make_float2(0.f, 0.f);
+            *a = make_float2(prev.x + acc_o[i][0] * f0, prev.y + acc_o[i][1] * f0);
+          }
+          if (r1 < g) {
+            float2* a = reinterpret_cast<float2*>(scr + r1 * kRowPad + d);
+            const float2 prev = w ? *a : make_float2(0.f, 0.f);
+            *a = make_float2(prev.x + acc_o[i][2] * f1, prev.y + acc_o[i][3] * f1);
+          }
+        }
+      }
+      ptx::named_bar_sync(1, kConsumers * 32);
     }
-    ptx::named_bar_sync(1, kConsumers * 32);
     const int t = threadIdx.x;   // 0..127
     for (int e = t; e < g * 32; e += kConsumers * 32) {
       const int r = e >> 5, c4 = (e & 31) * 4;
-      float4 a = *reinterpret_cast<const float4*>(sm.scratch + r * kRowPad + c4);
-#pragma unroll
-      for (int w = 1; w < kConsumers; ++w) {
-        const float4 b = *reinterpret_cast<const float4*>(sm.scratch + (w * 16 + r) * kRowPad + c4);
-        a.x += b.x;
-        a.y += b.y;
-        a.z += b.z;
-        a.w += b.w;
-      }
+      const float4 a = *reinterpret_cast<const float4*>(sm.scratch + r * kRowPad + c4);
       if (it.part < 0) {
         __nv_bfloat16* orow = o + ((int64_t)it.row * shp.H_q + it.kv_head * g + r) * 128 + c4;
         uint2 packed;
@@ -430,6 +439,10 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
   if (!attr_done) {
     e = cudaFuncSetAttribute(decode_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_splitkv_kernel,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
