@@ -7,7 +7,7 @@
 //
 // One CTA owns 128 consecutive rows of one chunk for one query head:
 //  - warp 4 (TMA): loads the 128x128 Q tile once and streams 64-key K and V
-//    tiles of the paged cache into a 2-stage ring (128-byte swizzle);
+//    tiles of the paged cache into a 4-stage ring (128-byte swizzle);
 //  - warp 5 (MMA): allocates 256 TMEM columns; one thread issues
 //    S = Q K^T (M=128, N=64, K=128) into one of two TMEM S buffers and
 //    O += P V (M=128, N=128, K=64) into the TMEM O accumulator, and signals
@@ -17,7 +17,10 @@
 //    raised only when a row's max grows by more than 2^8 (the accumulator in
 //    TMEM is then rescaled in place), writes P as bf16 into shared memory in
 //    the MMA operand layout, and finally normalises O and stores it.
-// Two CTAs fit on an SM (112 KB shared memory, 256 TMEM columns each).
+// P is double-buffered, so the softmax of tile j+1 waits only for the PV of
+// tile j-1 (and for the PV of tile j only when it must rescale O); QK^T of the
+// next tile is queued on the tensor pipe before each PV.  One CTA per SM
+// (about 192 KB of shared memory, 256 TMEM columns).
 // Every wait is bounded; on timeout the kernel records RBKV_ERR_TIMEOUT, lets
 // its copies and MMAs drain (bounded), frees its TMEM and returns.
 #include "rbkv_internal.h"
@@ -33,18 +36,18 @@ namespace {
 
 constexpr int kRows = kChunkTileRows;       // 128 query rows (MMA M)
 constexpr int kKeys = kChunkTileKeys;       // 64 keys per KV tile
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kThreads = 6 * 32;
 constexpr int kQHalf = kRows * 128;         // 16 KB: 128 rows x 64 bf16
 constexpr int kQBytes = 2 * kQHalf;
 constexpr int kKVHalf = kKeys * 128;        // 8 KB
 constexpr int kKVTile = 2 * kKVHalf;        // 16 KB
 constexpr int kStage = 2 * kKVTile;         // K + V
-constexpr int kPBytes = kRows * 128;        // 128 rows x 64 keys bf16
+constexpr int kPBytes = kRows * 128;        // one P buffer: 128 rows x 64 keys bf16 (two of them)
 constexpr int kTmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
 constexpr int kOCol = 128;
-// 112.25 KB: two CTAs per SM (or one next to a decode CTA)
-constexpr int kSmemBytes = kQBytes + kStages * kStage + kPBytes + 256;
+// about 192 KB: one CTA per SM with a 4-deep K/V ring and two P buffers
+constexpr int kSmemBytes = kQBytes + kStages * kStage + 2 * kPBytes + 256;
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -136,18 +139,21 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Every barrier below is waited on in order of its phases and can never run
+// two phases ahead of a waiter (the parity of a wait is then unambiguous): S,
+// P and PV completion each have one barrier per buffer.
 struct Bars {
   uint64_t q_full;
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_done;
+  uint64_t s_full[2];   // QK^T of tile j done: S buffer j & 1
+  uint64_t p_full[2];   // softmax of tile j done: P buffer j & 1 written
+  uint64_t o_done[2];   // PV of tile j done (it read P buffer j & 1)
   uint32_t tmem_base;
   int abort_flag;
 };
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_q,
                               const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
@@ -182,10 +188,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::mbar_init(&bars->kv_full[s], 1);
       ptx::mbar_init(&bars->kv_empty[s], 1);
     }
-    ptx::mbar_init(&bars->s_full[0], 1);
-    ptx::mbar_init(&bars->s_full[1], 1);
-    ptx::mbar_init(&bars->p_full, 4 * 32);
-    ptx::mbar_init(&bars->o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&bars->s_full[b], 1);
+      ptx::mbar_init(&bars->p_full[b], 4 * 32);
+      ptx::mbar_init(&bars->o_done[b], 1);
+    }
     bars->abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -289,18 +296,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           tc_fence_after();
           issue_qk(j + 1);
         }
-        if (!ptx::mbar_wait(&bars->p_full, j & 1, kWaitLimit) || *abort_flag) {
+        if (!ptx::mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, kWaitLimit) || *abort_flag) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t vt = kv_addr + (j % kStages) * kStage + kKVTile;
+        const uint32_t pt = p_addr + (j & 1) * kPBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          tc_mma(tmem + kOCol, smem_desc(p_addr + kk * 32, 16, 1024),
+          tc_mma(tmem + kOCol, smem_desc(pt + kk * 32, 16, 1024),
                  smem_desc(vt + kk * 2048, kKVHalf, 1024), idesc_o, j > 0 || kk > 0);
         }
-        tc_commit(&bars->o_done);
+        tc_commit(&bars->o_done[j & 1]);
         tc_commit(&bars->kv_empty[j % kStages]);
         pv_issued = j + 1;
       }
@@ -308,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         atomicCAS(dp.status, 0, kDevTimeout);
         *abort_flag = 1;
       }
-      // the last PV must finish before TMEM can be released
-      if (pv_issued > 0) ptx::mbar_wait(&bars->o_done, (pv_issued - 1) & 1, kWaitLimit);
+      // the last PV (and so every earlier one) must finish before TMEM is released
+      if (pv_issued > 0)
+        ptx::mbar_wait(&bars->o_done[(pv_issued - 1) & 1], ((pv_issued - 1) >> 1) & 1, kWaitLimit);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -354,15 +363,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         ps += sc[c];
       }
       l = l * corr + ps;
-      // P and the O accumulator are busy until the previous PV completes
-      if (j > 0) {
-        const bool done = ptx::mbar_wait(&bars->o_done, (j - 1) & 1, kWaitLimit);
+      // P buffer j & 1 is free once the PV of tile j - 2 has run
+      if (j >= 2) {
+        const bool done = ptx::mbar_wait(&bars->o_done[j & 1], ((j - 2) >> 1) & 1, kWaitLimit);
+        if (!__all_sync(0xffffffffu, done)) {
+          ok = false;
+          break;
+        }
+      }
+      // rescaling O needs every earlier PV finished (only when a row's max rose)
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        const bool done =
+            ptx::mbar_wait(&bars->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitLimit);
         if (!__all_sync(0xffffffffu, done)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, raise)) {
+        {
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             float ov[32];
@@ -388,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       // P row -> shared memory, 128-byte swizzled K-major operand layout
-      uint8_t* prow = p_s + row * 128;
+      uint8_t* prow = p_s + (j & 1) * kPBytes + row * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         uint4 v;
@@ -400,10 +418,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       ptx::fence_proxy_async_smem();
       tc_fence_before();
-      ptx::mbar_arrive(&bars->p_full);
+      ptx::mbar_arrive(&bars->p_full[j & 1]);
     }
     bool fin = ok && n_kv > 0;
-    if (fin) fin = ptx::mbar_wait(&bars->o_done, (n_kv - 1) & 1, kWaitLimit);
+    if (fin)
+      fin = ptx::mbar_wait(&bars->o_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, kWaitLimit);
     if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;

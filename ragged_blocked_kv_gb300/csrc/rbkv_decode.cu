@@ -8,9 +8,7 @@
 //    work units (longest first, dealt in snake order so CTAs finish together);
 //  - a producer warp streams 64-key K and V tiles of the paged cache with TMA
 //    (2-D tiled loads through the block table, 128-byte swizzle) into a
-//    3-stage shared-memory ring guarded by mbarriers (about 105 KB in all, so
-//    that a prompt-chunk CTA fits on the same SM and both kernels run side by
-//    side);
+//    5-stage shared-memory ring guarded by mbarriers;
 //  - four consumer warps share every tile, 16 keys each (so each warp consumes
 //    the ring strictly in order); each multiplies the group's query rows
 //    (padded to 16) by its keys with warp-level bf16 MMAs (fp32 accumulation),
@@ -34,7 +32,7 @@ namespace rbkv {
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kKeys = kDecodeTileKeys;        // 64 keys per tile
@@ -44,7 +42,7 @@ constexpr int kStage = 2 * kTile;             // K + V
 constexpr int kRowPad = 132;                  // fp32 row stride of the merge scratch
 constexpr int kScratchBytes = 16 * kRowPad * 4;   // one [16][kRowPad] fp32 merge buffer
 constexpr int kMlBytes = kConsumers * 16 * 2 * 4;
-// about 105 KB: a prompt-chunk CTA fits on the same SM next to this one
+// about 170 KB: a 5-deep ring of 32 KB K+V tiles
 constexpr int kSmemBytes = kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 16;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
@@ -82,7 +80,7 @@ __device__ __forceinline__ uint32_t tile_off(int key, int d) {
   return half * kHalf + key * 128 + ((chunk ^ (key & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DevPass dp, ShapeInfo shp,
                           const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o,

@@ -200,8 +200,6 @@ struct rbkv_pass {
   cudaStream_t upload_stream = nullptr;
   cudaStream_t last_stream = nullptr;
   cudaEvent_t upload_ev = nullptr;
-  cudaEvent_t fork_ev = nullptr;   // caller stream -> side stream
-  cudaEvent_t join_ev = nullptr;   // side stream -> caller stream
   DevPass dp{};
 };
 
@@ -358,24 +356,6 @@ size_t workspace_bytes_of(const rbkv_pass& p) {
   if (p.plan.n_parts == 0) return 0;
   ShapeInfo s = shape_of(p.cfg);
   return partial_o_bytes(p.plan.n_parts, s) + partial_lse_bytes(p.plan.n_parts, s);
-}
-
-// One non-blocking side stream per device: prompt-chunk tiles (tensor-core
-// bound) run there while the decode kernel (HBM bound) runs on the caller's
-// stream; both fit on an SM together.
-constexpr int kMaxSideDevices = 64;
-cudaStream_t g_side[kMaxSideDevices];
-std::mutex g_side_mu;
-
-cudaError_t side_stream(int dev, cudaStream_t* out) {
-  if (dev < 0 || dev >= kMaxSideDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_side_mu);
-  if (!g_side[dev]) {
-    cudaError_t e = cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking);
-    if (e != cudaSuccess) return e;
-  }
-  *out = g_side[dev];
-  return cudaSuccess;
 }
 
 rbkv_status ensure_plan(rbkv_pass* p) {
@@ -735,8 +715,6 @@ void rbkv_pass_destroy(rbkv_pass* p) {
   if (!p) return;
   if (p->dev) cudaFreeAsync(p->dev, p->last_stream);
   if (p->upload_ev) cudaEventDestroy(p->upload_ev);
-  if (p->fork_ev) cudaEventDestroy(p->fork_ev);
-  if (p->join_ev) cudaEventDestroy(p->join_ev);
   delete p;
 }
 
@@ -782,34 +760,14 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
   float* part_lse = need ? (float*)((char*)workspace + partial_o_bytes(p->plan.n_parts, s)) : nullptr;
   const DevPass& dp = p->dp;
   cudaError_t e = cudaSuccess;
-  if (dp.n_chunk && dp.n_decode) {
-    // decode on the caller's stream, chunk tiles beside it on the side stream
-    cudaStream_t side = nullptr;
-    e = side_stream(p->device, &side);
-    if (e == cudaSuccess && !p->fork_ev) e = cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming);
-    if (e == cudaSuccess && !p->join_ev) e = cudaEventCreateWithFlags(&p->join_ev, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventRecord(p->fork_ev, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, p->fork_ev, 0);
-    if (e == cudaSuccess)
-      e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
-        return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
-      });
-    if (e == cudaSuccess)
-      e = launch_counted(RBKV_KERNEL_CHUNK, side, [&] {
-        return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, side);
-      });
-    if (e == cudaSuccess) e = cudaEventRecord(p->join_ev, side);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, p->join_ev, 0);
-  } else {
-    if (dp.n_chunk)
-      e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
-        return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
-      });
-    if (e == cudaSuccess && dp.n_decode)
-      e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
-        return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
-      });
-  }
+  if (dp.n_chunk)
+    e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
+      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    });
+  if (e == cudaSuccess && dp.n_decode)
+    e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
+      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    });
   if (e == cudaSuccess && dp.n_generic)
     e = launch_counted(RBKV_KERNEL_GENERIC, st, [&] {
       return launch_generic_attention(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
