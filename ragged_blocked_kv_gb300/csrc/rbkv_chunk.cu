@@ -152,6 +152,9 @@ struct Bars {
   uint32_t tmem_base;
   int abort_flag;
 };
+// shared memory: Q | K/V ring | two P buffers | barriers
+static_assert(kQBytes + kStages * kStage + 2 * kPBytes + (int)sizeof(Bars) <= kSmemBytes,
+              "shared-memory layout overflows its allocation");
 
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_s = base;
   uint8_t* kv_s = q_s + kQBytes;
   uint8_t* p_s = kv_s + kStages * kStage;
-  Bars* bars = reinterpret_cast<Bars*>(p_s + kPBytes);
+  Bars* bars = reinterpret_cast<Bars*>(p_s + 2 * kPBytes);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % kStages;
         if (j >= kStages &&
             !ptx::mbar_wait(&bars->kv_empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
-          atomicCAS(dp.status, 0, kDevTimeout);
+          ptx::report_wait(dp.status, kDevTimeout, 21, j);
           *abort_flag = 1;
           break;
         }
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t p_addr = ptx::smem_u32(p_s);
       bool ok = ptx::mbar_wait(&bars->q_full, 0, kWaitLimit);
       int pv_issued = 0;
+      int site = ok ? 0 : 22, at = 0;
       auto issue_qk = [&](int j) {
         const uint32_t kt = kv_addr + (j % kStages) * kStage;
         const uint32_t d = tmem + (j & 1) * kKeys;
@@ -281,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (ok && n_kv > 0) {
         ok = ptx::mbar_wait(&bars->kv_full[0], 0, kWaitLimit);
+        if (!ok) site = 23;
         if (ok) {
           tc_fence_after();
           issue_qk(0);
@@ -291,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ptx::mbar_wait(&bars->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
                               kWaitLimit)) {
             ok = false;
+            site = 24;
+            at = j + 1;
             break;
           }
           tc_fence_after();
@@ -298,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ptx::mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, kWaitLimit) || *abort_flag) {
           ok = false;
+          site = 25;
+          at = j;
           break;
         }
         tc_fence_after();
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pv_issued = j + 1;
       }
       if (!ok) {
-        atomicCAS(dp.status, 0, kDevTimeout);
+        ptx::report_wait(dp.status, kDevTimeout, site, at);
         *abort_flag = 1;
       }
       // the last PV (and so every earlier one) must finish before TMEM is released
@@ -328,11 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qk_scale = shp.scale * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    int site = 0, at = 0;
     for (int j = 0; j < n_kv; ++j) {
       // tcgen05.ld/st are warp-collective: every decision below is warp-uniform
       const bool got = ptx::mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, kWaitLimit);
       if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *abort_flag != 0)) {
         ok = false;
+        site = 31;
+        at = j;
         break;
       }
       tc_fence_after();
@@ -368,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool done = ptx::mbar_wait(&bars->o_done[j & 1], ((j - 2) >> 1) & 1, kWaitLimit);
         if (!__all_sync(0xffffffffu, done)) {
           ok = false;
+          site = 32;
+          at = j;
           break;
         }
       }
@@ -377,6 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_wait(&bars->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitLimit);
         if (!__all_sync(0xffffffffu, done)) {
           ok = false;
+          site = 33;
+          at = j;
           break;
         }
         tc_fence_after();
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (store && partial) part_lse[slot] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
     } else if (!ok || n_kv > 0) {
-      atomicCAS(dp.status, 0, kDevTimeout);
+      ptx::report_wait(dp.status, kDevTimeout, ok ? 34 : site, ok ? n_kv : at);
       *abort_flag = 1;
     }
   }

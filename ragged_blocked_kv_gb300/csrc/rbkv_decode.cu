@@ -56,6 +56,11 @@ struct Shared {
   volatile int* abort_flag;
 };
 
+// shared memory: K/V ring | merge buffer | (max, sum) per warp and row |
+// full and empty barriers | abort flag
+static_assert(kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 4 <= kSmemBytes,
+              "shared-memory layout overflows its allocation");
+
 __device__ __forceinline__ Shared carve(uint8_t* raw) {
   Shared s;
   s.stages = raw;
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = idx % kStages;
           if (idx >= (uint32_t)kStages &&
               !ptx::mbar_wait(&sm.empty[s], ((idx / kStages) - 1) & 1, kWaitLimit)) {
-            atomicCAS(dp.status, 0, kDevTimeout);
+            ptx::report_wait(dp.status, kDevTimeout, 11, (int)idx);
             abort_flag = 1;
             break;
           }
@@ -204,7 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait(&sm.full[s], (idx / kStages) & 1, kWaitLimit)) {
         // give up on this unit; the merge barriers below are still met by
         // every consumer warp, then all of them leave together
-        if (lane == 0) { atomicCAS(dp.status, 0, kDevTimeout); abort_flag = 1; }
+        if (lane == 0) {
+          ptx::report_wait(dp.status, kDevTimeout, 12, (int)idx);
+          abort_flag = 1;
+        }
         __syncwarp();
         break;
       }

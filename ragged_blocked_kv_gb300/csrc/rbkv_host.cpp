@@ -783,13 +783,18 @@ rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream) {
   if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
   if (!p->dev) return RBKV_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  int32_t word = 0;
+  int32_t words[4] = {0, 0, 0, 0};
   cudaError_t e = cudaStreamSynchronize(st);
-  if (e == cudaSuccess) e = cudaMemcpy(&word, p->dev, sizeof(word), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(p->dev, 0, sizeof(word));
+  if (e == cudaSuccess) e = cudaMemcpy(words, p->dev, sizeof(words), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(p->dev, 0, sizeof(words));
   if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  const int32_t word = words[0];
   if (word == kDevBounds) return fail(RBKV_ERR_DEVICE_BOUNDS, "a kernel met an out-of-range block id");
-  if (word == kDevTimeout) return fail(RBKV_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (word == kDevTimeout)
+    return fail(RBKV_ERR_TIMEOUT, "a bounded device wait gave up (site " + std::to_string(words[1]) +
+                                      ", index " + std::to_string(words[2]) + ", block " +
+                                      std::to_string(words[3] & 0xFFFF) + "," +
+                                      std::to_string(words[3] >> 16) + ")");
   if (word != 0) return fail(RBKV_ERR_CUDA, "unknown device status " + std::to_string(word));
   return RBKV_OK;
 }

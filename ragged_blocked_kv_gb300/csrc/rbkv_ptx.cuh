@@ -57,6 +57,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 
+// Record a given-up wait in a pass's status words: [0] code (first report
+// wins), [1] the wait site, [2] the tile or item index, [3] the block
+// (blockIdx.x | blockIdx.y << 16).
+__device__ __forceinline__ void report_wait(int32_t* status, int32_t code, int32_t site,
+                                            int32_t index) {
+  if (atomicCAS(status, 0, code) == 0) {
+    status[1] = site;
+    status[2] = index;
+    status[3] = (int32_t)(blockIdx.x | (blockIdx.y << 16));
+  }
+}
+
 // ---- TMA --------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
