@@ -353,13 +353,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_base + (j & 1) * kKeys + 32, sc + 32);
       tmem_wait_ld();
       const int key0 = kb + j * kKeys;
-      float mt = -INFINITY;
+      // this row sees the tile's first `lim` keys: those <= its position and
+      // before the split's end (a prefix of the tile, possibly empty or all)
+      const int lim = min(pos + 1, ke) - key0;
+      float mraw = -INFINITY;
+      if (__all_sync(0xffffffffu, lim >= kKeys)) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int key = key0 + c;
-        sc[c] = (key <= pos && key < ke) ? sc[c] * qk_scale : -INFINITY;
-        mt = fmaxf(mt, sc[c]);
+        for (int c = 0; c < 64; ++c) mraw = fmaxf(mraw, sc[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          sc[c] = c < lim ? sc[c] : -INFINITY;
+          mraw = fmaxf(mraw, sc[c]);
+        }
       }
+      // the scale is positive, so the row max scales with it
+      const float mt = mraw * qk_scale;
       float corr = 1.f;
       const bool raise = mt > m_ref + kRescaleThreshold;
       if (raise) {
@@ -367,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = mt;
       }
       // a row with no key in this split so far keeps m_ref = -inf: its p are 0
-      const float base = m_ref == -INFINITY ? 0.f : m_ref;
+      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
       float ps = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        sc[c] = exp2f(sc[c] - base);
+        sc[c] = exp2f(fmaf(sc[c], qk_scale, nbase));
         ps += sc[c];
       }
       l = l * corr + ps;

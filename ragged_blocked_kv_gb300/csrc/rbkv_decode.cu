@@ -40,16 +40,16 @@ constexpr int kHalf = kKeys * 128;            // 64 rows x 128 B (64 bf16 of hea
 constexpr int kTile = 2 * kHalf;              // K or V tile, head_dim 128
 constexpr int kStage = 2 * kTile;             // K + V
 constexpr int kRowPad = 132;                  // fp32 row stride of the merge scratch
-constexpr int kScratchBytes = 16 * kRowPad * 4;   // one [16][kRowPad] fp32 merge buffer
+constexpr int kScratchBytes = kConsumers * 16 * kRowPad * 4;   // [warp][16][kRowPad] fp32
 constexpr int kMlBytes = kConsumers * 16 * 2 * 4;
-// about 170 KB: a 5-deep ring of 32 KB K+V tiles
+// about 195 KB: a 5-deep ring of 32 KB K+V tiles and the merge buffers
 constexpr int kSmemBytes = kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 16;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shared {
   uint8_t* stages;     // kStages x kStage, 1024-aligned
-  float* scratch;      // [16][kRowPad]
+  float* scratch;      // [kConsumers][16][kRowPad]
   float* ml;           // [kConsumers][16][2]
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
@@ -65,7 +65,7 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
   Shared s;
   s.stages = raw;
   s.scratch = reinterpret_cast<float*>(s.stages + kStages * kStage);
-  s.ml = s.scratch + 16 * kRowPad;
+  s.ml = s.scratch + kConsumers * 16 * kRowPad;
   s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * 16 * 2);
   s.empty = s.full + kStages;
   s.abort_flag = reinterpret_cast<volatile int*>(s.empty + kStages);
@@ -331,31 +331,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - M0) / L0;
     const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - M1) / L1;
-    // the four warps add their scaled O into one buffer, one warp at a time
-    float* scr = sm.scratch;
-    for (int w = 0; w < kConsumers; ++w) {
-      if (warp == w) {
+    // each warp stores its rescaled O; then all four are summed per element
+    float* scr = sm.scratch + warp * 16 * kRowPad;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int d = i * 8 + cq;
-          if (r0 < g) {
-            float2* a = reinterpret_cast<float2*>(scr + r0 * kRowPad + d);
-            const float2 prev = w ? *a : make_float2(0.f, 0.f);
-            *a = make_float2(prev.x + acc_o[i][0] * f0, prev.y + acc_o[i][1] * f0);
-          }
-          if (r1 < g) {
-            float2* a = reinterpret_cast<float2*>(scr + r1 * kRowPad + d);
-            const float2 prev = w ? *a : make_float2(0.f, 0.f);
-            *a = make_float2(prev.x + acc_o[i][2] * f1, prev.y + acc_o[i][3] * f1);
-          }
-        }
-      }
-      ptx::named_bar_sync(1, kConsumers * 32);
+    for (int i = 0; i < 16; ++i) {
+      const int d = i * 8 + cq;
+      if (r0 < g)
+        *reinterpret_cast<float2*>(scr + r0 * kRowPad + d) =
+            make_float2(acc_o[i][0] * f0, acc_o[i][1] * f0);
+      if (r1 < g)
+        *reinterpret_cast<float2*>(scr + r1 * kRowPad + d) =
+            make_float2(acc_o[i][2] * f1, acc_o[i][3] * f1);
     }
+    ptx::named_bar_sync(1, kConsumers * 32);
     const int t = threadIdx.x;   // 0..127
     for (int e = t; e < g * 32; e += kConsumers * 32) {
       const int r = e >> 5, c4 = (e & 31) * 4;
-      const float4 a = *reinterpret_cast<const float4*>(sm.scratch + r * kRowPad + c4);
+      float4 a = *reinterpret_cast<const float4*>(sm.scratch + r * kRowPad + c4);
+#pragma unroll
+      for (int w = 1; w < kConsumers; ++w) {
+        const float4 b =
+            *reinterpret_cast<const float4*>(sm.scratch + (w * 16 + r) * kRowPad + c4);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
       if (it.part < 0) {
         __nv_bfloat16* orow = o + ((int64_t)it.row * shp.H_q + it.kv_head * g + r) * 128 + c4;
         uint2 packed;

@@ -269,9 +269,26 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
     split = std::max<int32_t>(512, round_up(std::max<int64_t>(target, 1), gran));
   }
 
-  // prompt-chunk tiles: fixed split length unless the caller forced one
-  const int32_t chunk_split = p.split_keys > 0 ? round_up(p.split_keys, kChunkTileKeys)
-                                               : kChunkSplitKeys;
+  // prompt-chunk tiles (one CTA per 128-row tile and query head, one CTA per
+  // SM): their key ranges are split only when there are fewer tiles x heads
+  // than SMs, into pieces that bring the count up to about one full wave
+  int32_t chunk_split = 0x7fffffff;
+  if (p.split_keys > 0) {
+    chunk_split = round_up(p.split_keys, kChunkTileKeys);
+  } else if (fast_chunk) {
+    int64_t pairs = 0;
+    int32_t max_keys = 0;
+    for (int32_t i = 0; i < S; ++i) {
+      if (p.n_new[i] <= 1) continue;
+      pairs += (int64_t)ceil_div(p.n_new[i], kChunkTileRows) * s.H_q;
+      max_keys = std::max(max_keys, p.ctx[i]);
+    }
+    if (pairs > 0 && pairs < num_sms) {
+      const int32_t per = std::max<int32_t>(1, (int32_t)(num_sms / pairs));
+      chunk_split = std::max<int32_t>(kChunkMinSplitKeys,
+                                      round_up(ceil_div(max_keys, per), kChunkTileKeys));
+    }
+  }
   std::vector<int32_t> bounds;
   std::vector<WorkItem> decode, generic;
   int32_t max_splits = 0;

@@ -99,7 +99,7 @@ constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decod
 constexpr int kDecodeCtasPerSm = 1;
 constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
 constexpr int kChunkTileKeys = 64;       // keys per tensor-core KV tile
-constexpr int kChunkSplitKeys = 2048;    // automatic key-split length of prompt-chunk tiles
+constexpr int kChunkMinSplitKeys = 512;  // shortest automatic key split of prompt-chunk tiles
 
 bool decode_fast_supported(const ShapeInfo& s);
 // 2-D view of a bf16 [num_blocks][H_kv][B][head_dim] cache for TMA: `rows`
