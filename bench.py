@@ -37,8 +37,11 @@ if ROOT not in sys.path:
 
 HBM_FALLBACK_GBS = 6800.0
 # DRAM bytes (read + write) per launch of a kernel, from the ncu captures
-# summarised under profiles/ (None where no capture of the current kernel)
-TRAFFIC_BYTES = {}
+# summarised under profiles/, keyed by (workload, kernel) and valid only for
+# the kernel source they were taken on (sha256 prefix of its .cu file)
+TRAFFIC_BYTES = {
+    ("llama2_7b", "decode"): ("rbkv_decode.cu", "1c21360e02cc", 610_324_480),
+}
 BF16_FALLBACK_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -176,6 +179,24 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+def traffic_bytes(workload, kernel):
+    """ncu DRAM traffic per launch recorded for this kernel and workload, or
+    None when there is none or the kernel source changed since."""
+    import hashlib
+    rec = TRAFFIC_BYTES.get((workload, kernel))
+    if rec is None:
+        return None
+    src, sha, nbytes = rec
+    path = os.path.join(ROOT, "ragged_blocked_kv_gb300", "csrc", src)
+    try:
+        with open(path, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:12] != sha:
+                return None
+    except OSError:
+        return None
+    return nbytes
 
 
 def step_work(meta, shape):
@@ -411,7 +432,7 @@ def run_ours(args, rank, world, local_rank):
         per_launch = work[key] / dom_n
         roof = {"bound": "hbm", "achieved": per_launch / avg_s / 1e9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = TRAFFIC_BYTES.get((args.workload, dom))
+    roof["traffic"] = traffic_bytes(args.workload, dom)
     roof["kernel"] = dom
     roof["peak_source"] = src
     roof["avg_launch_us"] = avg_s * 1e6
