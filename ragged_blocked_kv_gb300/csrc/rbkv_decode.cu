@@ -49,7 +49,7 @@ constexpr int kMlBytes = kConsumers * 16 * 2 * 4;
 // about 214 KB: the K/V ring, one query slot per stage, the merge buffers,
 // stage tags and barriers
 constexpr int kSmemBytes = kStages * kStage + kStages * kQSlot + kScratchBytes + kMlBytes +
-                           kStages * 16 + 2 * kStages * 8 + 8 + 16;
+                           kStages * 32 + 2 * kStages * 8 + 8 + 16;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -58,7 +58,8 @@ struct Shared {
   uint8_t* qslots;     // kStages x kQSlot
   float* scratch;      // [kConsumers][16][kRowPad]
   float* ml;           // [kConsumers][16][2]
-  int4* tag;           // [kStages]: (unit, tile, tiles in unit, -)
+  int4* tag;           // [kStages][2]: (tile, tiles in unit, key_begin, key_end),
+                       //               (row, kv head, partial slot, unit or -1 = stop)
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
   uint64_t* group;     // consumer-group barrier (128 arrivals)
@@ -67,7 +68,7 @@ struct Shared {
 
 // shared memory: K/V ring | query slots | merge buffer | (max, sum) per warp
 // and row | stage tags | full and empty barriers | group barrier | abort flag
-static_assert(kStages * kStage + kStages * kQSlot + kScratchBytes + kMlBytes + kStages * 16 +
+static_assert(kStages * kStage + kStages * kQSlot + kScratchBytes + kMlBytes + kStages * 32 +
                       2 * kStages * 8 + 8 + 4 <= kSmemBytes,
               "shared-memory layout overflows its allocation");
 
@@ -78,7 +79,7 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
   s.scratch = reinterpret_cast<float*>(s.qslots + kStages * kQSlot);
   s.ml = s.scratch + kConsumers * 16 * kRowPad;
   s.tag = reinterpret_cast<int4*>(s.ml + kConsumers * 16 * 2);
-  s.full = reinterpret_cast<uint64_t*>(s.tag + kStages);
+  s.full = reinterpret_cast<uint64_t*>(s.tag + 2 * kStages);
   s.empty = s.full + kStages;
   s.group = s.empty + kStages;
   s.abort_flag = reinterpret_cast<volatile int*>(s.group + 1);
@@ -151,18 +152,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int box_rows = B < kKeys ? B : kKeys;
       uint32_t idx = 0;     // stages handed out so far
       bool done = false;
+      // the next unit is fetched one unit ahead, so its counter round trip
+      // overlaps the current unit's tiles
+      int next = atomicAdd(&dp.counters[0], 1);
       while (!done && !abort_flag) {
-        const int item = atomicAdd(&dp.counters[0], 1);
+        const int item = next;
         const bool end = item >= dp.n_decode;
         WorkItem it{};
         int nt = 1;
         if (!end) {
           it = dp.decode_items[item];
           nt = tiles_of(it);
+          next = atomicAdd(&dp.counters[0], 1);
         }
         const int32_t* table = dp.block_ids + it.table_off;
+        // block ids of the next 16 tiles (blocks of >= 64 keys: one per tile)
+        int32_t blk16[16];
         for (int j = 0; j < nt; ++j) {
           const int s = idx % kStages;
+          const int k0 = it.key_begin + j * kKeys;
+          if (B >= kKeys && !end && (j & 15) == 0) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int key = k0 + u * kKeys;
+              blk16[u] = key < it.key_end ? __ldg(table + key / B) : 0;
+            }
+          }
           if (idx >= (uint32_t)kStages &&
               !ptx::mbar_wait(&sm.empty[s], ((idx / kStages) - 1) & 1, kWaitLimit)) {
             ptx::report_wait(dp.status, kDevTimeout, 11, (int)idx);
@@ -170,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             done = true;
             break;
           }
-          sm.tag[s] = make_int4(end ? -1 : item, j, nt, 0);
+          sm.tag[2 * s] = make_int4(j, nt, it.key_begin, it.key_end);
+          sm.tag[2 * s + 1] = make_int4(it.row, it.kv_head, it.part, end ? -1 : item);
           if (end) {
             // no more work: an empty stage tells the consumers to stop
             ptx::mbar_arrive_expect_tx(&sm.full[s], 0);
@@ -178,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             done = true;
             break;
           }
-          const int k0 = it.key_begin + j * kKeys;
           uint8_t* kdst = sm.stages + s * kStage;
           uint8_t* vdst = kdst + kTile;
           // sub-boxes of box_rows keys; skip those past the unit's last key
@@ -187,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < kKeys; r += box_rows) {
             const int key = k0 + r;
             if (key >= it.key_end) break;
-            const int32_t blk = table[key / B];
+            const int32_t blk = B >= kKeys ? blk16[j & 15] : table[key / B];
             if (blk < 0 || blk >= dp.num_blocks) {
               atomicCAS(dp.status, 0, kDevBounds);
               rows[nsub++] = -1;
@@ -247,11 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       abort_flag = 1;
       return;
     }
-    const int4 tag = sm.tag[s];
-    if (tag.x < 0) return;                    // no more work
-    const int j = tag.y, nt = tag.z;
+    const int4 tag0 = sm.tag[2 * s];
+    const int4 tag1 = sm.tag[2 * s + 1];
+    if (tag1.w < 0) return;                   // no more work
+    const int j = tag0.x, nt = tag0.y;
     if (j == 0) {
-      it = dp.decode_items[tag.x];
+      it.key_begin = tag0.z;
+      it.key_end = tag0.w;
+      it.row = tag1.x;
+      it.kv_head = tag1.y;
+      it.part = tag1.z;
       // the unit's query rows as m16n8k16 A fragments (rows >= g are zero)
       const uint32_t* q0 = reinterpret_cast<const uint32_t*>(sm.qslots + s * kQSlot + r0 * 256);
       const uint32_t* q1 = reinterpret_cast<const uint32_t*>(sm.qslots + s * kQSlot + r1 * 256);
