@@ -4,24 +4,21 @@
 // log-sum-exp; Step 3's split path shows the per-split softmax).
 //
 // GB300 design (HBM-bound: every cached K/V byte is read once):
-//  - persistent grid, one CTA per SM; work units (longest first) are handed
-//    out by a per-pass atomic counter, so CTAs that finish early take more
-//    and all finish together; the last CTA out resets the counter;
+//  - persistent grid, one CTA per SM, each CTA walks a host-ordered list of
+//    work units (longest first, dealt in snake order so CTAs finish together);
 //  - a producer warp streams 64-key K and V tiles of the paged cache with TMA
 //    (2-D tiled loads through the block table, 128-byte swizzle) into a
-//    5-stage shared-memory ring guarded by mbarriers; with a unit's first
-//    tile it also bulk-copies the unit's query rows, and it tags every stage
-//    with (unit, tile, tiles in unit) so the consumers just follow the ring;
-//  - four consumer warps share every tile, 16 keys each; each multiplies the
-//    group's query rows (padded to 16) by its keys with warp-level bf16 MMAs
-//    (fp32 accumulation), runs the online softmax in registers with quad
-//    shuffles, and accumulates P.V with MMAs;
-//  - after a unit's last tile the four warps merge their (max, sum, O) states
-//    in shared memory and write either O (bf16) or the fp32 partial output and
+//    5-stage shared-memory ring guarded by mbarriers;
+//  - four consumer warps share every tile, 16 keys each (so each warp consumes
+//    the ring strictly in order); each multiplies the group's query rows
+//    (padded to 16) by its keys with warp-level bf16 MMAs (fp32 accumulation),
+//    runs the online softmax in registers with quad shuffles, and accumulates
+//    P.V with MMAs;
+//  - at the end of a unit the four warps merge their (max, sum, O) states in
+//    shared memory and write either O (bf16) or the fp32 partial output and
 //    base-2 log-sum-exp for the combine kernel.
-// Every wait is bounded (also the consumers' group barriers, which are
-// mbarriers): on timeout the kernel records RBKV_ERR_TIMEOUT with the wait
-// site in the pass's status words and stops.
+// Every wait is bounded: on timeout the kernel records RBKV_ERR_TIMEOUT in the
+// pass's status word and stops.
 #include "rbkv_internal.h"
 #include "rbkv_ptx.cuh"
 
@@ -42,47 +39,36 @@ constexpr int kKeys = kDecodeTileKeys;        // 64 keys per tile
 constexpr int kHalf = kKeys * 128;            // 64 rows x 128 B (64 bf16 of head_dim)
 constexpr int kTile = 2 * kHalf;              // K or V tile, head_dim 128
 constexpr int kStage = 2 * kTile;             // K + V
-constexpr int kQSlot = 16 * 256;              // query rows of one unit (g <= 16), bf16
 constexpr int kRowPad = 132;                  // fp32 row stride of the merge scratch
 constexpr int kScratchBytes = kConsumers * 16 * kRowPad * 4;   // [warp][16][kRowPad] fp32
 constexpr int kMlBytes = kConsumers * 16 * 2 * 4;
-// about 214 KB: the K/V ring, one query slot per stage, the merge buffers,
-// stage tags and barriers
-constexpr int kSmemBytes = kStages * kStage + kStages * kQSlot + kScratchBytes + kMlBytes +
-                           kStages * 32 + 2 * kStages * 8 + 8 + 16;
+// about 195 KB: a 5-deep ring of 32 KB K+V tiles and the merge buffers
+constexpr int kSmemBytes = kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 16;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shared {
   uint8_t* stages;     // kStages x kStage, 1024-aligned
-  uint8_t* qslots;     // kStages x kQSlot
   float* scratch;      // [kConsumers][16][kRowPad]
   float* ml;           // [kConsumers][16][2]
-  int4* tag;           // [kStages][2]: (tile, tiles in unit, key_begin, key_end),
-                       //               (row, kv head, partial slot, unit or -1 = stop)
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
-  uint64_t* group;     // consumer-group barrier (128 arrivals)
   volatile int* abort_flag;
 };
 
-// shared memory: K/V ring | query slots | merge buffer | (max, sum) per warp
-// and row | stage tags | full and empty barriers | group barrier | abort flag
-static_assert(kStages * kStage + kStages * kQSlot + kScratchBytes + kMlBytes + kStages * 32 +
-                      2 * kStages * 8 + 8 + 4 <= kSmemBytes,
+// shared memory: K/V ring | merge buffer | (max, sum) per warp and row |
+// full and empty barriers | abort flag
+static_assert(kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 4 <= kSmemBytes,
               "shared-memory layout overflows its allocation");
 
 __device__ __forceinline__ Shared carve(uint8_t* raw) {
   Shared s;
   s.stages = raw;
-  s.qslots = s.stages + kStages * kStage;
-  s.scratch = reinterpret_cast<float*>(s.qslots + kStages * kQSlot);
+  s.scratch = reinterpret_cast<float*>(s.stages + kStages * kStage);
   s.ml = s.scratch + kConsumers * 16 * kRowPad;
-  s.tag = reinterpret_cast<int4*>(s.ml + kConsumers * 16 * 2);
-  s.full = reinterpret_cast<uint64_t*>(s.tag + 2 * kStages);
+  s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * 16 * 2);
   s.empty = s.full + kStages;
-  s.group = s.empty + kStages;
-  s.abort_flag = reinterpret_cast<volatile int*>(s.group + 1);
+  s.abort_flag = reinterpret_cast<volatile int*>(s.empty + kStages);
   return s;
 }
 
@@ -97,24 +83,6 @@ __device__ __forceinline__ uint32_t tile_off(int key, int d) {
   const int half = d >> 6;
   const int chunk = (d & 63) >> 3;
   return half * kHalf + key * 128 + ((chunk ^ (key & 7)) << 4);
-}
-
-// 1-D bulk copy global -> shared, completion as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(ptx::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(ptx::smem_u32(bar))
-      : "memory");
-}
-
-// Consumer-group barrier on an mbarrier (128 arrivals per phase), bounded.
-__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase) {
-  ptx::mbar_arrive(bar);
-  const bool ok = ptx::mbar_wait(bar, phase & 1, kWaitLimit);
-  ++phase;
-  return ok;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -138,7 +106,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&sm.full[s], 1);
       ptx::mbar_init(&sm.empty[s], kConsumers);
     }
-    ptx::mbar_init(sm.group, kConsumers * 32);
     abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -149,51 +116,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
+      uint32_t idx = 0;
       const int box_rows = B < kKeys ? B : kKeys;
-      uint32_t idx = 0;     // stages handed out so far
-      bool done = false;
-      // the next unit is fetched one unit ahead, so its counter round trip
-      // overlaps the current unit's tiles
-      int next = atomicAdd(&dp.counters[0], 1);
-      while (!done && !abort_flag) {
-        const int item = next;
-        const bool end = item >= dp.n_decode;
-        WorkItem it{};
-        int nt = 1;
-        if (!end) {
-          it = dp.decode_items[item];
-          nt = tiles_of(it);
-          next = atomicAdd(&dp.counters[0], 1);
-        }
+      for (int item = blockIdx.x; item < dp.n_decode && !abort_flag; item += gridDim.x) {
+        const WorkItem it = dp.decode_items[item];
         const int32_t* table = dp.block_ids + it.table_off;
-        // block ids of the next 16 tiles (blocks of >= 64 keys: one per tile)
-        int32_t blk16[16];
-        for (int j = 0; j < nt; ++j) {
+        const int nt = tiles_of(it);
+        for (int j = 0; j < nt; ++j, ++idx) {
           const int s = idx % kStages;
-          const int k0 = it.key_begin + j * kKeys;
-          if (B >= kKeys && !end && (j & 15) == 0) {
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int key = k0 + u * kKeys;
-              blk16[u] = key < it.key_end ? __ldg(table + key / B) : 0;
-            }
-          }
           if (idx >= (uint32_t)kStages &&
               !ptx::mbar_wait(&sm.empty[s], ((idx / kStages) - 1) & 1, kWaitLimit)) {
             ptx::report_wait(dp.status, kDevTimeout, 11, (int)idx);
             abort_flag = 1;
-            done = true;
             break;
           }
-          sm.tag[2 * s] = make_int4(j, nt, it.key_begin, it.key_end);
-          sm.tag[2 * s + 1] = make_int4(it.row, it.kv_head, it.part, end ? -1 : item);
-          if (end) {
-            // no more work: an empty stage tells the consumers to stop
-            ptx::mbar_arrive_expect_tx(&sm.full[s], 0);
-            ++idx;
-            done = true;
-            break;
-          }
+          const int k0 = it.key_begin + j * kKeys;
           uint8_t* kdst = sm.stages + s * kStage;
           uint8_t* vdst = kdst + kTile;
           // sub-boxes of box_rows keys; skip those past the unit's last key
@@ -202,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < kKeys; r += box_rows) {
             const int key = k0 + r;
             if (key >= it.key_end) break;
-            const int32_t blk = B >= kKeys ? blk16[j & 15] : table[key / B];
+            const int32_t blk = table[key / B];
             if (blk < 0 || blk >= dp.num_blocks) {
               atomicCAS(dp.status, 0, kDevBounds);
               rows[nsub++] = -1;
@@ -212,11 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           int loads = 0;
           for (int i = 0; i < nsub; ++i) loads += rows[i] >= 0;
-          const uint32_t qbytes = j == 0 ? (uint32_t)g * 256u : 0u;
-          ptx::mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(loads * box_rows * 128 * 4) + qbytes);
-          if (j == 0)
-            bulk_load(sm.qslots + s * kQSlot,
-                      q + ((int64_t)it.row * shp.H_q + it.kv_head * g) * 128, qbytes, &sm.full[s]);
+          ptx::mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(loads * box_rows * 128 * 4));
           for (int i = 0; i < nsub; ++i) {
             if (rows[i] < 0) continue;
             const int off = i * box_rows * 128;
@@ -225,18 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &sm.full[s]);
             ptx::tma_load_2d(vdst + kHalf + off, &tmap_v, 64, rows[i], &sm.full[s]);
           }
-          ++idx;
         }
+        if (abort_flag) break;
       }
       // let every load this CTA issued land before the CTA can exit
-      for (uint32_t t = idx > (uint32_t)kStages ? idx - kStages : 0; t < idx; ++t)
+      const uint32_t issued = idx;
+      for (uint32_t t = issued > (uint32_t)kStages ? issued - kStages : 0; t < issued; ++t)
         ptx::mbar_wait(&sm.full[t % kStages], (t / kStages) & 1, kWaitLimit);
-      // the last CTA to finish resets the work counter for the next launch
-      __threadfence();
-      if (atomicAdd(&dp.counters[1], 1) == (int)gridDim.x - 1) {
-        dp.counters[0] = 0;
-        dp.counters[1] = 0;
-      }
     }
     return;
   }
@@ -245,164 +173,164 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float qk_scale = shp.scale * kLog2e;
   const int r0 = lane >> 2, r1 = r0 + 8;      // fragment rows (query heads of the group)
   const int cq = (lane & 3) * 2;              // fragment column pair
-  const int wk = warp * 16;                   // this warp's 16 keys of every tile
-  const int mi = lane >> 3;
+  uint32_t tile_base = 0;
   const uint32_t stages_u32 = ptx::smem_u32(sm.stages);
-  uint32_t idx = 0, gphase = 0;
-  WorkItem it{};
-  uint32_t qa[8][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float acc_o[16][4];
 
-  while (true) {
-    const int s = idx % kStages;
-    const bool got = ptx::mbar_wait(&sm.full[s], (idx / kStages) & 1, kWaitLimit);
-    if (!__all_sync(0xffffffffu, got)) {
-      if (lane == 0) ptx::report_wait(dp.status, kDevTimeout, 12, (int)idx);
-      abort_flag = 1;
-      return;
-    }
-    const int4 tag0 = sm.tag[2 * s];
-    const int4 tag1 = sm.tag[2 * s + 1];
-    if (tag1.w < 0) return;                   // no more work
-    const int j = tag0.x, nt = tag0.y;
-    if (j == 0) {
-      it.key_begin = tag0.z;
-      it.key_end = tag0.w;
-      it.row = tag1.x;
-      it.kv_head = tag1.y;
-      it.part = tag1.z;
-      // the unit's query rows as m16n8k16 A fragments (rows >= g are zero)
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(sm.qslots + s * kQSlot + r0 * 256);
-      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(sm.qslots + s * kQSlot + r1 * 256);
+  for (int item = blockIdx.x; item < dp.n_decode; item += gridDim.x) {
+    const WorkItem it = dp.decode_items[item];
+    const int nt = tiles_of(it);
+
+    // query rows of the group as m16n8k16 A fragments (rows >= g are zero)
+    uint32_t qa[8][4];
+    {
+      const __nv_bfloat16* qbase = q + ((int64_t)it.row * shp.H_q + it.kv_head * g) * 128;
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qbase + r0 * 128);
+      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qbase + r1 * 128);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int c = (kk * 16 + cq) >> 1;
-        qa[kk][0] = r0 < g ? q0[c] : 0u;
-        qa[kk][1] = r1 < g ? q1[c] : 0u;
-        qa[kk][2] = r0 < g ? q0[c + 4] : 0u;
-        qa[kk][3] = r1 < g ? q1[c + 4] : 0u;
+        qa[kk][0] = r0 < g ? __ldg(q0 + c) : 0u;
+        qa[kk][1] = r1 < g ? __ldg(q1 + c) : 0u;
+        qa[kk][2] = r0 < g ? __ldg(q0 + c + 4) : 0u;
+        qa[kk][3] = r1 < g ? __ldg(q1 + c + 4) : 0u;
       }
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) acc_o[i][0] = acc_o[i][1] = acc_o[i][2] = acc_o[i][3] = 0.f;
     }
-    const int k0 = it.key_begin + j * kKeys;
-    const int valid = min(kKeys, it.key_end - k0) - wk;   // valid keys of this warp's 16
-    const uint32_t kt = stages_u32 + s * kStage;
-    const uint32_t vt = kt + kTile;
-    if (valid < 16) {
-      // rows past the unit's last key may hold anything (unwritten cache
-      // slots, stale tiles): zero this warp's such V rows so 0 * V stays 0
-      uint8_t* vrow = sm.stages + s * kStage + kTile;
-      const int first = valid < 0 ? 0 : valid;
-      for (int e = lane; e < (16 - first) * 16; e += 32) {
-        const int key = wk + first + e / 16, c = e % 16;
-        *reinterpret_cast<uint4*>(vrow + (c >> 3) * kHalf + key * 128 + ((c & 7) << 4)) =
-            make_uint4(0, 0, 0, 0);
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc_o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc_o[i][0] = acc_o[i][1] = acc_o[i][2] = acc_o[i][3] = 0.f;
+
+    // every warp takes 16 keys (rows 16*warp .. 16*warp+15) of every tile, so
+    // each warp consumes the stages strictly in order
+    const int wk = warp * 16;
+    for (int j = 0; j < nt && !abort_flag; ++j) {
+      const uint32_t idx = tile_base + j;
+      const int s = idx % kStages;
+      if (!ptx::mbar_wait(&sm.full[s], (idx / kStages) & 1, kWaitLimit)) {
+        // give up on this unit; the merge barriers below are still met by
+        // every consumer warp, then all of them leave together
+        if (lane == 0) {
+          ptx::report_wait(dp.status, kDevTimeout, 12, (int)idx);
+          abort_flag = 1;
+        }
+        __syncwarp();
+        break;
+      }
+      const int k0 = it.key_begin + j * kKeys;
+      const int valid = min(kKeys, it.key_end - k0) - wk;   // valid keys of this warp's 16
+      const uint32_t kt = stages_u32 + s * kStage;
+      const uint32_t vt = kt + kTile;
+      if (valid < 16) {
+        // rows past the unit's last key may hold anything (unwritten cache
+        // slots, stale tiles): zero this warp's such V rows so 0 * V stays 0
+        uint8_t* vrow = sm.stages + s * kStage + kTile;
+        const int first = valid < 0 ? 0 : valid;
+        for (int e = lane; e < (16 - first) * 16; e += 32) {
+          const int key = wk + first + e / 16, c = e % 16;
+          *reinterpret_cast<uint4*>(vrow + (c >> 3) * kHalf + key * 128 + ((c & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      if (valid > 0) {
+        // S = Q K^T over this warp's 16 keys: 2 n-tiles of 8 keys
+        float sc[2][4];
+        sc[0][0] = sc[0][1] = sc[0][2] = sc[0][3] = 0.f;
+        sc[1][0] = sc[1][1] = sc[1][2] = sc[1][3] = 0.f;
+        const int mi = lane >> 3;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int key = wk + (mi >> 1) * 8 + (lane & 7);
+          const int d = kk * 16 + (mi & 1) * 8;
+          uint32_t b0, b1, b2, b3;
+          ptx::ldsm_x4(kt + tile_off(key, d), b0, b1, b2, b3);
+          ptx::mma_bf16_16816(sc[0], qa[kk], b0, b1);
+          ptx::mma_bf16_16816(sc[1], qa[kk], b2, b3);
+        }
+        // scale, mask keys past the unit, online softmax (rows r0 and r1)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const int key = n * 8 + cq;
+          sc[n][0] = key < valid ? sc[n][0] * qk_scale : -INFINITY;
+          sc[n][1] = key + 1 < valid ? sc[n][1] * qk_scale : -INFINITY;
+          sc[n][2] = key < valid ? sc[n][2] * qk_scale : -INFINITY;
+          sc[n][3] = key + 1 < valid ? sc[n][3] * qk_scale : -INFINITY;
+          mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+          mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p00 = exp2f(sc[0][0] - mn0), p01 = exp2f(sc[0][1] - mn0);
+        const float p02 = exp2f(sc[0][2] - mn1), p03 = exp2f(sc[0][3] - mn1);
+        const float p10 = exp2f(sc[1][0] - mn0), p11 = exp2f(sc[1][1] - mn0);
+        const float p12 = exp2f(sc[1][2] - mn1), p13 = exp2f(sc[1][3] - mn1);
+        l0 = l0 * c0 + (p00 + p01 + p10 + p11);
+        l1 = l1 * c1 + (p02 + p03 + p12 + p13);
+        uint32_t pa[4];
+        pa[0] = ptx::pack_bf16x2(p00, p01);
+        pa[1] = ptx::pack_bf16x2(p02, p03);
+        pa[2] = ptx::pack_bf16x2(p10, p11);
+        pa[3] = ptx::pack_bf16x2(p12, p13);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          acc_o[i][0] *= c0;
+          acc_o[i][1] *= c0;
+          acc_o[i][2] *= c1;
+          acc_o[i][3] *= c1;
+        }
+        // O += P V over the 16 keys: 16 n-tiles of 8 head-dim columns
+#pragma unroll
+        for (int dp2 = 0; dp2 < 8; ++dp2) {
+          const int key = wk + (mi & 1) * 8 + (lane & 7);
+          const int d = dp2 * 16 + (mi >> 1) * 8;
+          uint32_t b0, b1, b2, b3;
+          ptx::ldsm_x4_t(vt + tile_off(key, d), b0, b1, b2, b3);
+          ptx::mma_bf16_16816(acc_o[2 * dp2], pa, b0, b1);
+          ptx::mma_bf16_16816(acc_o[2 * dp2 + 1], pa, b2, b3);
+        }
       }
       __syncwarp();
-    }
-    if (valid > 0) {
-      // S = Q K^T over this warp's 16 keys: 2 n-tiles of 8 keys
-      float sc[2][4];
-      sc[0][0] = sc[0][1] = sc[0][2] = sc[0][3] = 0.f;
-      sc[1][0] = sc[1][1] = sc[1][2] = sc[1][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int key = wk + (mi >> 1) * 8 + (lane & 7);
-        const int d = kk * 16 + (mi & 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ptx::ldsm_x4(kt + tile_off(key, d), b0, b1, b2, b3);
-        ptx::mma_bf16_16816(sc[0], qa[kk], b0, b1);
-        ptx::mma_bf16_16816(sc[1], qa[kk], b2, b3);
-      }
-      // scale, mask keys past the unit, online softmax (rows r0 and r1)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        const int key = n * 8 + cq;
-        sc[n][0] = key < valid ? sc[n][0] * qk_scale : -INFINITY;
-        sc[n][1] = key + 1 < valid ? sc[n][1] * qk_scale : -INFINITY;
-        sc[n][2] = key < valid ? sc[n][2] * qk_scale : -INFINITY;
-        sc[n][3] = key + 1 < valid ? sc[n][3] * qk_scale : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      const float p00 = exp2f(sc[0][0] - mn0), p01 = exp2f(sc[0][1] - mn0);
-      const float p02 = exp2f(sc[0][2] - mn1), p03 = exp2f(sc[0][3] - mn1);
-      const float p10 = exp2f(sc[1][0] - mn0), p11 = exp2f(sc[1][1] - mn0);
-      const float p12 = exp2f(sc[1][2] - mn1), p13 = exp2f(sc[1][3] - mn1);
-      l0 = l0 * c0 + (p00 + p01 + p10 + p11);
-      l1 = l1 * c1 + (p02 + p03 + p12 + p13);
-      uint32_t pa[4];
-      pa[0] = ptx::pack_bf16x2(p00, p01);
-      pa[1] = ptx::pack_bf16x2(p02, p03);
-      pa[2] = ptx::pack_bf16x2(p10, p11);
-      pa[3] = ptx::pack_bf16x2(p12, p13);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        acc_o[i][0] *= c0;
-        acc_o[i][1] *= c0;
-        acc_o[i][2] *= c1;
-        acc_o[i][3] *= c1;
-      }
-      // O += P V over the 16 keys: 16 n-tiles of 8 head-dim columns
-#pragma unroll
-      for (int dp2 = 0; dp2 < 8; ++dp2) {
-        const int key = wk + (mi & 1) * 8 + (lane & 7);
-        const int d = dp2 * 16 + (mi >> 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ptx::ldsm_x4_t(vt + tile_off(key, d), b0, b1, b2, b3);
-        ptx::mma_bf16_16816(acc_o[2 * dp2], pa, b0, b1);
-        ptx::mma_bf16_16816(acc_o[2 * dp2 + 1], pa, b2, b3);
+      if (lane == 0) {
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(&sm.empty[s]);
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&sm.empty[s]);
-    }
-    ++idx;
-    if (j != nt - 1) continue;
+    tile_base += nt;
 
-    // ---- the unit's last tile: merge the four warps, write the result -----
-    float L0 = l0, L1 = l1;
-    L0 += __shfl_xor_sync(0xffffffffu, L0, 1);
-    L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
-    L1 += __shfl_xor_sync(0xffffffffu, L1, 1);
-    L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
+    // ---- merge the four warps' states and write the unit's result -------
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     if ((lane & 3) == 0) {
       sm.ml[(warp * 16 + r0) * 2 + 0] = m0;
-      sm.ml[(warp * 16 + r0) * 2 + 1] = L0;
+      sm.ml[(warp * 16 + r0) * 2 + 1] = l0;
       sm.ml[(warp * 16 + r1) * 2 + 0] = m1;
-      sm.ml[(warp * 16 + r1) * 2 + 1] = L1;
+      sm.ml[(warp * 16 + r1) * 2 + 1] = l1;
     }
-    if (!group_sync(sm.group, gphase)) break;
+    ptx::named_bar_sync(1, kConsumers * 32);
     float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumers; ++w) {
       M0 = fmaxf(M0, sm.ml[(w * 16 + r0) * 2]);
       M1 = fmaxf(M1, sm.ml[(w * 16 + r1) * 2]);
     }
-    float S0 = 0.f, S1 = 0.f;
+    float L0 = 0.f, L1 = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumers; ++w) {
       const float mw0 = sm.ml[(w * 16 + r0) * 2], mw1 = sm.ml[(w * 16 + r1) * 2];
-      if (mw0 != -INFINITY) S0 += exp2f(mw0 - M0) * sm.ml[(w * 16 + r0) * 2 + 1];
-      if (mw1 != -INFINITY) S1 += exp2f(mw1 - M1) * sm.ml[(w * 16 + r1) * 2 + 1];
+      if (mw0 != -INFINITY) L0 += exp2f(mw0 - M0) * sm.ml[(w * 16 + r0) * 2 + 1];
+      if (mw1 != -INFINITY) L1 += exp2f(mw1 - M1) * sm.ml[(w * 16 + r1) * 2 + 1];
     }
-    const float f0 = (m0 == -INFINITY || S0 == 0.f) ? 0.f : exp2f(m0 - M0) / S0;
-    const float f1 = (m1 == -INFINITY || S1 == 0.f) ? 0.f : exp2f(m1 - M1) / S1;
+    const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - M0) / L0;
+    const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - M1) / L1;
     // each warp stores its rescaled O; then all four are summed per element
     float* scr = sm.scratch + warp * 16 * kRowPad;
 #pragma unroll
@@ -415,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(scr + r1 * kRowPad + d) =
             make_float2(acc_o[i][2] * f1, acc_o[i][3] * f1);
     }
-    if (!group_sync(sm.group, gphase)) break;
+    ptx::named_bar_sync(1, kConsumers * 32);
     const int t = threadIdx.x;   // 0..127
     for (int e = t; e < g * 32; e += kConsumers * 32) {
       const int r = e >> 5, c4 = (e & 31) * 4;
@@ -448,12 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
-    // the merge buffers are reused by the next unit
-    if (!group_sync(sm.group, gphase)) break;
+    // all consumer warps leave together if anyone gave up
+    if (ptx::named_bar_or(1, kConsumers * 32, abort_flag != 0)) return;
   }
-  // a group barrier gave up
-  if (lane == 0) ptx::report_wait(dp.status, kDevTimeout, 13, (int)idx);
-  abort_flag = 1;
 }
 
 // ---- host: tensor maps -------------------------------------------------------
@@ -510,8 +435,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
                                float* part_lse, cudaStream_t st) {
   if (!decode_fast_supported(s)) return cudaErrorNotSupported;
   if (dp.n_decode == 0) return cudaSuccess;
-  if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
-    return cudaErrorMisalignedAddress;
+  if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15) return cudaErrorMisalignedAddress;
   const int64_t rows = (int64_t)dp.num_blocks * s.H_kv * s.B;
   const int box_rows = s.B < kKeys ? s.B : kKeys;
   CUtensorMap tk, tv;

@@ -227,6 +227,22 @@ void split_keys(int32_t n_keys, int32_t split, int32_t gran, std::vector<int32_t
   bounds.push_back(n_keys);
 }
 
+// Reorder `items` (sorted longest first) so that a persistent grid of G CTAs,
+// CTA c taking items c, c+G, c+2G, ..., receives them in snake order: round r
+// hands sorted items r*G .. r*G+G-1 to CTAs 0..G-1 on even rounds and to
+// G-1..0 on odd rounds.  Long and short units even out across CTAs.
+void snake_order(std::vector<WorkItem>& items, int32_t G) {
+  std::vector<WorkItem> out(items.size());
+  for (size_t i = 0; i < items.size(); ++i) {
+    size_t r = i / G, c = i % G;
+    size_t base = r * G;
+    size_t width = std::min((size_t)G, items.size() - base);
+    size_t src = (r % 2 == 0) ? base + c : base + (width - 1 - c);
+    out[i] = items[src];
+  }
+  items.swap(out);
+}
+
 Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   Plan pl;
   ShapeInfo s = shape_of(p.cfg);
@@ -333,6 +349,7 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   });
   int32_t grid = (int32_t)std::min<int64_t>((int64_t)decode.size(),
                                             (int64_t)std::max(1, num_sms) * kDecodeCtasPerSm);
+  if (grid > 0) snake_order(decode, grid);
   pl.decode_grid = grid;
   pl.decode.swap(decode);
   pl.generic.swap(generic);
@@ -393,7 +410,7 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
   if (rs != RBKV_OK) return rs;
   if (!p->dev) {
     const Plan& pl = p->plan;
-    std::vector<int32_t> w(8, 0);  // 4 status words, 2 decode counters, padding
+    std::vector<int32_t> w(4, 0);  // status words: code, wait site, index, block
     size_t o_slot, o_blocks, o_dec, o_gen, o_chunk, o_comb;
     put(w, o_slot, p->slot);
     put(w, o_blocks, p->block_ids);
@@ -422,7 +439,6 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     int32_t* base = (int32_t*)dev;
     DevPass& dp = p->dp;
     dp.status = base;
-    dp.counters = base + 4;
     dp.slot = base + o_slot;
     dp.block_ids = base + o_blocks;
     dp.decode_items = (const WorkItem*)(base + o_dec);

@@ -58,7 +58,6 @@ static_assert(sizeof(ChunkTile) == 48, "ChunkTile is 12 int32");
 // Device view of a pass (pointers into its uploaded metadata buffer).
 struct DevPass {
   int32_t* status;                 // device status words (rbkv_status code, wait site, ...)
-  int32_t* counters;               // [0] next decode unit, [1] CTAs done (reset by the last)
   const int32_t* slot;             // [T]
   const int32_t* block_ids;        // all block tables
   const WorkItem* decode_items;    // fast decode path
