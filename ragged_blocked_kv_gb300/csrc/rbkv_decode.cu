@@ -113,75 +113,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
-    // The whole warp walks the units.  Lane 0 waits on the ring and issues the
-    // copies; for blocks of >= 64 keys all 32 lanes fetch the block ids of the
-    // next 32 tiles at once (one per lane), so no tile waits on a dependent
-    // global load of its block-table entry.
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
-    }
-    uint32_t idx = 0;
-    const int box_rows = B < kKeys ? B : kKeys;
-    bool stop = false;
-    for (int item = blockIdx.x; item < dp.n_decode && !stop; item += gridDim.x) {
-      const WorkItem it = dp.decode_items[item];
-      const int32_t* table = dp.block_ids + it.table_off;
-      const int nt = tiles_of(it);
-      int32_t my_blk = 0;
-      for (int j = 0; j < nt; ++j, ++idx) {
-        if (B >= kKeys && (j & 31) == 0) {
-          const int key = it.key_begin + (j + lane) * kKeys;
-          my_blk = key < it.key_end ? __ldg(table + key / B) : 0;
-        }
-        const int32_t tile_blk = __shfl_sync(0xffffffffu, my_blk, j & 31);
-        int bail = 0;
-        if (lane == 0) {
+      uint32_t idx = 0;
+      const int box_rows = B < kKeys ? B : kKeys;
+      for (int item = blockIdx.x; item < dp.n_decode && !abort_flag; item += gridDim.x) {
+        const WorkItem it = dp.decode_items[item];
+        const int32_t* table = dp.block_ids + it.table_off;
+        const int nt = tiles_of(it);
+        for (int j = 0; j < nt; ++j, ++idx) {
           const int s = idx % kStages;
-          if (abort_flag ||
-              (idx >= (uint32_t)kStages &&
-               !ptx::mbar_wait(&sm.empty[s], ((idx / kStages) - 1) & 1, kWaitLimit))) {
-            if (!abort_flag) ptx::report_wait(dp.status, kDevTimeout, 11, (int)idx);
+          if (idx >= (uint32_t)kStages &&
+              !ptx::mbar_wait(&sm.empty[s], ((idx / kStages) - 1) & 1, kWaitLimit)) {
+            ptx::report_wait(dp.status, kDevTimeout, 11, (int)idx);
             abort_flag = 1;
-            bail = 1;
-          } else {
-            const int k0 = it.key_begin + j * kKeys;
-            uint8_t* kdst = sm.stages + s * kStage;
-            uint8_t* vdst = kdst + kTile;
-            // sub-boxes of box_rows keys; skip those past the unit's last key
-            int nsub = 0;
-            int32_t rows[kKeys / 8];
-            for (int r = 0; r < kKeys; r += box_rows) {
-              const int key = k0 + r;
-              if (key >= it.key_end) break;
-              const int32_t blk = B >= kKeys ? tile_blk : table[key / B];
-              if (blk < 0 || blk >= dp.num_blocks) {
-                atomicCAS(dp.status, 0, kDevBounds);
-                rows[nsub++] = -1;
-                continue;
-              }
-              rows[nsub++] = (blk * H_kv + it.kv_head) * B + (key % B);
+            break;
+          }
+          const int k0 = it.key_begin + j * kKeys;
+          uint8_t* kdst = sm.stages + s * kStage;
+          uint8_t* vdst = kdst + kTile;
+          // sub-boxes of box_rows keys; skip those past the unit's last key
+          int nsub = 0;
+          int32_t rows[kKeys / 8];
+          for (int r = 0; r < kKeys; r += box_rows) {
+            const int key = k0 + r;
+            if (key >= it.key_end) break;
+            const int32_t blk = table[key / B];
+            if (blk < 0 || blk >= dp.num_blocks) {
+              atomicCAS(dp.status, 0, kDevBounds);
+              rows[nsub++] = -1;
+              continue;
             }
-            int loads = 0;
-            for (int i = 0; i < nsub; ++i) loads += rows[i] >= 0;
-            ptx::mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(loads * box_rows * 128 * 4));
-            for (int i = 0; i < nsub; ++i) {
-              if (rows[i] < 0) continue;
-              const int off = i * box_rows * 128;
-              ptx::tma_load_2d(kdst + off, &tmap_k, 0, rows[i], &sm.full[s]);
-              ptx::tma_load_2d(kdst + kHalf + off, &tmap_k, 64, rows[i], &sm.full[s]);
-              ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &sm.full[s]);
-              ptx::tma_load_2d(vdst + kHalf + off, &tmap_v, 64, rows[i], &sm.full[s]);
-            }
+            rows[nsub++] = (blk * H_kv + it.kv_head) * B + (key % B);
+          }
+          int loads = 0;
+          for (int i = 0; i < nsub; ++i) loads += rows[i] >= 0;
+          ptx::mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(loads * box_rows * 128 * 4));
+          for (int i = 0; i < nsub; ++i) {
+            if (rows[i] < 0) continue;
+            const int off = i * box_rows * 128;
+            ptx::tma_load_2d(kdst + off, &tmap_k, 0, rows[i], &sm.full[s]);
+            ptx::tma_load_2d(kdst + kHalf + off, &tmap_k, 64, rows[i], &sm.full[s]);
+            ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &sm.full[s]);
+            ptx::tma_load_2d(vdst + kHalf + off, &tmap_v, 64, rows[i], &sm.full[s]);
           }
         }
-        if (__shfl_sync(0xffffffffu, bail, 0)) {
-          stop = true;
-          break;
-        }
+        if (abort_flag) break;
       }
-    }
-    if (lane == 0) {
       // let every load this CTA issued land before the CTA can exit
       const uint32_t issued = idx;
       for (uint32_t t = issued > (uint32_t)kStages ? issued - kStages : 0; t < issued; ++t)
