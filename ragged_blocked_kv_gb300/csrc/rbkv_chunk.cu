@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(p_s + 2 * kPBytes);
   volatile int* abort_flag = &bars->abort_flag;
 
+  // the decode kernel that follows may start on SMs this grid leaves free
+  ptx::pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ChunkTile tile = dp.chunk_tiles[blockIdx.x];
   const int h = blockIdx.y;

@@ -91,6 +91,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o,
                           float* __restrict__ part_o, float* __restrict__ part_lse) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The kernel may run beside the prompt-chunk kernel that precedes it (it
+  // reads only the cache and Q, and writes rows and partial slots the chunk
+  // kernel does not); it lets the combine kernel launch early, and waits for
+  // the chunk kernel before it ends so that its completion covers both.
+  ptx::pdl_launch_dependents();
   Shared sm = carve(smem_raw);
   volatile int& abort_flag = *sm.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t t = issued > (uint32_t)kStages ? issued - kStages : 0; t < issued; ++t)
         ptx::mbar_wait(&sm.full[t % kStages], (t / kStages) & 1, kWaitLimit);
     }
+    ptx::pdl_wait_previous();
     return;
   }
 
@@ -377,8 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
     // all consumer warps leave together if anyone gave up
-    if (ptx::named_bar_or(1, kConsumers * 32, abort_flag != 0)) return;
+    if (ptx::named_bar_or(1, kConsumers * 32, abort_flag != 0)) break;
   }
+  ptx::pdl_wait_previous();
 }
 
 // ---- host: tensor maps -------------------------------------------------------
@@ -432,7 +439,7 @@ bool decode_fast_supported(const ShapeInfo& s) {
 
 cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                                const void* k_cache, const void* v_cache, void* o, float* part_o,
-                               float* part_lse, cudaStream_t st) {
+                               float* part_lse, cudaStream_t st, bool overlap_previous) {
   if (!decode_fast_supported(s)) return cudaErrorNotSupported;
   if (dp.n_decode == 0) return cudaSuccess;
   if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15) return cudaErrorMisalignedAddress;
@@ -453,9 +460,18 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  decode_splitkv_kernel<<<dp.decode_grid, kThreads, kSmemBytes, st>>>(
-      tk, tv, dp, s, (const __nv_bfloat16*)q, (__nv_bfloat16*)o, part_o, part_lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dp.decode_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel, tk, tv, dp, s, (const __nv_bfloat16*)q,
+                            (__nv_bfloat16*)o, part_o, part_lse);
 }
 
 }  // namespace rbkv

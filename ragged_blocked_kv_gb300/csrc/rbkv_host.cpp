@@ -523,7 +523,7 @@ rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache
     ++launched;
   }
   if (e == cudaSuccess && dp.n_decode) {
-    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, dp.n_chunk > 0);
     ++launched;
   }
   if (e == cudaSuccess && dp.n_generic) {
@@ -783,7 +783,8 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
     });
   if (e == cudaSuccess && dp.n_decode)
     e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
-      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st,
+                                dp.n_chunk > 0 && !g_prof.on);
     });
   if (e == cudaSuccess && dp.n_generic)
     e = launch_counted(RBKV_KERNEL_GENERIC, st, [&] {

@@ -161,6 +161,9 @@ template <class T>
 __global__ void __launch_bounds__(128)
     combine_kernel(DevPass dp, ShapeInfo s, const float* __restrict__ part_o,
                    const float* __restrict__ part_lse, T* __restrict__ o) {
+  // launched to overlap the attention kernels' tail: the partials are only
+  // complete once they have finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (w >= (int64_t)dp.n_combine * s.g) return;
@@ -236,12 +239,19 @@ cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* p
   const int64_t warps = (int64_t)dp.n_combine * s.g;
   if (warps == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((warps * 32 + 127) / 128);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (s.dtype == 0)
-    combine_kernel<__nv_bfloat16><<<blocks, 128, 0, st>>>(dp, s, part_o, part_lse,
-                                                          (__nv_bfloat16*)o);
-  else
-    combine_kernel<float><<<blocks, 128, 0, st>>>(dp, s, part_o, part_lse, (float*)o);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, dp, s, part_o, part_lse,
+                              (__nv_bfloat16*)o);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, dp, s, part_o, part_lse, (float*)o);
 }
 
 }  // namespace rbkv

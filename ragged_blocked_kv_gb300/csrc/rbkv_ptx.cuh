@@ -69,6 +69,18 @@ __device__ __forceinline__ void report_wait(int32_t* status, int32_t code, int32
   }
 }
 
+// ---- programmatic dependent launch --------------------------------------------
+// Let the next kernel in the stream be scheduled once every CTA of this grid
+// has started (its prologue then overlaps this grid's tail).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the previous grid in the stream has completed and its memory is
+// visible (returns at once when this grid was launched without overlap).
+__device__ __forceinline__ void pdl_wait_previous() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- TMA --------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
