@@ -175,8 +175,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(p_s + 2 * kPBytes);
   volatile int* abort_flag = &bars->abort_flag;
 
-  // the decode kernel that follows may start on SMs this grid leaves free
-  ptx::pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ChunkTile tile = dp.chunk_tiles[blockIdx.x];
   const int h = blockIdx.y;
@@ -205,6 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // The grid may have been launched while the cache append before it still
+  // runs: wait for it here, after the set-up.  Only then let the decode
+  // kernel that follows start (on SMs this grid leaves free), so that it
+  // never sees a cache still being written.
+  ptx::pdl_wait_previous();
+  if (threadIdx.x == 0) ptx::pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -510,7 +514,7 @@ bool chunk_fast_supported(const ShapeInfo& s) {
 
 cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                               const void* k_cache, const void* v_cache, void* o, float* part_o,
-                              float* part_lse, cudaStream_t st) {
+                              float* part_lse, cudaStream_t st, bool overlap_previous) {
   if (!chunk_fast_supported(s)) return cudaErrorNotSupported;
   if (dp.n_chunk == 0) return cudaSuccess;
   if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
@@ -536,10 +540,18 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
     attr_done = true;
   }
   dim3 grid(dp.n_chunk, s.H_q);
-  chunk_attn_tcgen05_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, dp, s,
-                                                                (__nv_bfloat16*)o, part_o,
-                                                                part_lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tcgen05_kernel, tq, tk, tv, dp, s,
+                            (__nv_bfloat16*)o, part_o, part_lse);
 }
 
 }  // namespace rbkv

@@ -89,12 +89,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DevPass dp, ShapeInfo shp,
                           const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o,
-                          float* __restrict__ part_o, float* __restrict__ part_lse) {
+                          float* __restrict__ part_o, float* __restrict__ part_lse,
+                          int wait_first) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The kernel may run beside the prompt-chunk kernel that precedes it (it
-  // reads only the cache and Q, and writes rows and partial slots the chunk
-  // kernel does not); it lets the combine kernel launch early, and waits for
-  // the chunk kernel before it ends so that its completion covers both.
+  // reads only the cache, Q and the pass metadata, and writes rows and
+  // partial slots the chunk kernel does not; the chunk kernel lets it start
+  // only once everything before the chunk kernel has finished).  With any
+  // other predecessor (`wait_first`) it waits for it before anything else.
+  // It lets the combine kernel launch early, and waits for its predecessor
+  // before ending, so that its completion covers both attention kernels.
+  if (wait_first) ptx::pdl_wait_previous();
   ptx::pdl_launch_dependents();
   Shared sm = carve(smem_raw);
   volatile int& abort_flag = *sm.abort_flag;
@@ -439,7 +444,8 @@ bool decode_fast_supported(const ShapeInfo& s) {
 
 cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                                const void* k_cache, const void* v_cache, void* o, float* part_o,
-                               float* part_lse, cudaStream_t st, bool overlap_previous) {
+                               float* part_lse, cudaStream_t st, bool overlap_previous,
+                               bool wait_first) {
   if (!decode_fast_supported(s)) return cudaErrorNotSupported;
   if (dp.n_decode == 0) return cudaSuccess;
   if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15) return cudaErrorMisalignedAddress;
@@ -471,7 +477,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel, tk, tv, dp, s, (const __nv_bfloat16*)q,
-                            (__nv_bfloat16*)o, part_o, part_lse);
+                            (__nv_bfloat16*)o, part_o, part_lse, wait_first ? 1 : 0);
 }
 
 }  // namespace rbkv

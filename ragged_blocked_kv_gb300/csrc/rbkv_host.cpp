@@ -519,11 +519,12 @@ rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache
   e = cudaSuccess;
   int launched = 0;
   if (dp.n_chunk) {
-    e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+    e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, false);
     ++launched;
   }
   if (e == cudaSuccess && dp.n_decode) {
-    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, dp.n_chunk > 0);
+    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, dp.n_chunk > 0,
+                           false);
     ++launched;
   }
   if (e == cudaSuccess && dp.n_generic) {
@@ -777,14 +778,21 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
   float* part_lse = need ? (float*)((char*)workspace + partial_o_bytes(p->plan.n_parts, s)) : nullptr;
   const DevPass& dp = p->dp;
   cudaError_t e = cudaSuccess;
+  // Kernels overlap their predecessor in the stream through programmatic
+  // dependent launch (not while per-launch events are recorded).  Each waits
+  // for its predecessor before touching memory it might share with it: the
+  // chunk kernel before any global access; the decode kernel too, unless its
+  // predecessor is this call's chunk kernel (which lets it start only once
+  // everything before the chunk kernel has finished).
+  const bool overlap = !g_prof.on;
   if (dp.n_chunk)
     e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
-      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st);
+      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap);
     });
   if (e == cudaSuccess && dp.n_decode)
     e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
-      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st,
-                                dp.n_chunk > 0 && !g_prof.on);
+      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
+                                dp.n_chunk == 0);
     });
   if (e == cudaSuccess && dp.n_generic)
     e = launch_counted(RBKV_KERNEL_GENERIC, st, [&] {

@@ -117,15 +117,18 @@ cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* 
 cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
                                      const void* k_cache, const void* v_cache, void* o,
                                      float* part_o, float* part_lse, cudaStream_t st);
-// overlap_previous: the kernel before it in the stream is this pass's chunk
-// kernel, which it may run beside (programmatic dependent launch)
+// Programmatic dependent launch: overlap_previous lets the kernel start
+// before its predecessor in the stream ends; wait_first (decode) makes it
+// wait for that predecessor before any global access, for when the
+// predecessor is not this call's chunk kernel.
 cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                                const void* k_cache, const void* v_cache, void* o,
                                float* part_o, float* part_lse, cudaStream_t st,
-                               bool overlap_previous);
+                               bool overlap_previous, bool wait_first);
 cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                               const void* k_cache, const void* v_cache, void* o,
-                              float* part_o, float* part_lse, cudaStream_t st);
+                              float* part_o, float* part_lse, cudaStream_t st,
+                              bool overlap_previous);
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
 

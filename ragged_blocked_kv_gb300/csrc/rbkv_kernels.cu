@@ -47,6 +47,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(DevPass dp, int32_t H_kv
                                                         const uint4* __restrict__ v_new,
                                                         uint4* __restrict__ k_cache,
                                                         uint4* __restrict__ v_cache) {
+  // the attention kernels may launch now; they wait for this grid before
+  // reading the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t total = (int64_t)dp.num_tokens * H_kv * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {

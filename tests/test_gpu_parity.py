@@ -120,3 +120,22 @@ def test_full_size_sampled(rbkv, name):
         if m.seq_ids[s] in sample:
             blocks.extend(m.blocks_of(s))
     assert pair.cache_equal(blocks)
+
+
+@pytest.mark.parametrize("name,factor", [("decode_stress", 16), ("llama2_7b", 8)])
+def test_q_written_by_a_kernel_just_before_attention(rbkv, name, factor):
+    """The attention kernels start early (programmatic dependent launch); a Q
+    written by the caller's own kernel right before the call must still be
+    read only after that kernel has finished."""
+    scn = workloads.scaled(workloads.SCENARIOS[name](0), factor)
+    (r,) = run_scenario(rbkv, scn)
+    _ok(r)
+    p, pair = r["pass"], r["pair"]
+    q = workloads.make_qkv(scn.shape, p.num_tokens, 0, 1, which="q")[0].cuda()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        q2 = torch.full_like(q, float("nan"))
+        torch.mul(q * 2, 0.5, out=q2)           # exact; runs just before the call
+        o2 = rbkv.ragged_attention(p, q2, pair.kc, pair.vc)
+        torch.cuda.synchronize()
+        assert torch.equal(o2.view(torch.int16), r["o"].view(torch.int16))
