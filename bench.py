@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=90)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama2_7b",
-                    choices=["llama2_7b", "decode_stress", "mistral_7b"])
+                    choices=["llama2_7b", "decode_stress", "mistral_7b", "trace"])
+    ap.add_argument("--layers", type=int, default=32, help="layers per pass (trace workload)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
@@ -491,6 +492,128 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------------------------------
+# trace workload: closed-loop SplitFuse serving of 512 requests
+# ---------------------------------------------------------------------------
+def run_trace_bench(args, rank, world, local_rank):
+    """512 requests from 32 closed-loop clients (prompt lengths round(N(2600,
+    780^2)), output lengths round(N(60, 18^2)), at least 1), composed into
+    512-token passes until every request has finished.  Each pass runs
+    kv_append and ragged attention for every layer (Llama-2-7B attention
+    shape, one K/V cache per layer, one block table shared by all layers).
+    Reports pass tokens per second over the whole trace and the distribution
+    of per-pass latency (all layers of a pass, CUDA events)."""
+    import torch
+    import workloads
+    from ragged_blocked_kv_gb300 import build as _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    import ragged_blocked_kv_gb300 as rbkv
+    rbkv.lib()
+    device = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    L = args.layers
+    shape = workloads.Shape(32, 32, 128, 64, "bf16", 1.0 / math.sqrt(128.0))
+    reqs = workloads.trace_requests(seed=args.seed)
+    nb = workloads.trace_block_pool(reqs, 32, shape.block_size)
+    cfg = rbkv.Config(32, 32, 128, 64, "bf16", nb)
+    caches = [(torch.zeros(cfg.cache_shape(), dtype=torch.bfloat16, device=device),
+               torch.zeros(cfg.cache_shape(), dtype=torch.bfloat16, device=device))
+              for _ in range(L)]
+    budget = 512
+    inputs = [workloads.make_qkv(shape, budget, args.seed, 1000 + l, device=device)
+              for l in range(L)]
+    o = torch.empty((budget, 32, 128), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    hs = rbkv._P(stream.cuda_stream)
+    torch.cuda.synchronize()
+
+    def drive(trace_reqs, comp, record):
+        events, tokens = [], []
+
+        def compose(b, M, states):
+            p = comp.compose(b, M, states)
+            T = p.num_tokens
+            if T:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for l in range(L):
+                    q, k, v = inputs[l]
+                    kc, vc = caches[l]
+                    rbkv.kv_append(p, k[:T], v[:T], kc, vc, stream=hs)
+                    rbkv.ragged_attention(p, q[:T], kc, vc, o=o[:T], workspace=ws, stream=hs)
+                e1.record(stream)
+                if record:
+                    events.append((e0, e1))
+                    tokens.append(T)
+            return p.meta
+        n = workloads.run_trace(trace_reqs, 32, budget, budget, compose, comp.release)
+        return n, events, tokens
+
+    # warm-up: a short trace of the same shape on its own composer
+    warm = workloads.trace_requests(seed=args.seed + 1, num_requests=64, num_clients=32)
+    drive(warm, rbkv.Composer(cfg), False)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.5)
+    comp = rbkv.Composer(cfg)
+    launches0 = rbkv.kernel_launches()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    wall_t0 = time.time()
+    t0.record(stream)
+    npass, events, tokens = drive(reqs, comp, True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall_t1 = time.time()
+    clk = clocks.stop(wall_t0, wall_t1)
+    launches = rbkv.kernel_launches() - launches0
+    total_ms = t0.elapsed_time(t1)
+    lat = sorted(a.elapsed_time(b) for a, b in events)
+
+    def pct(x):
+        return lat[min(len(lat) - 1, int(round(x / 100.0 * (len(lat) - 1))))]
+
+    if rank != 0:
+        return
+    ntok = sum(tokens)
+    line = {
+        "metric": "ragged SplitFuse attention pass tokens/s",
+        "value": ntok / (total_ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": npass,
+        "warmup": 0,
+        "ms_per_step": total_ms / max(1, npass),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"trace: {len(reqs)} requests, 32 closed-loop clients, budget 512, "
+                        f"chunk cap 512, {L} layers of 32q/32kv heads, head_dim 128, block 64",
+            "passes": npass,
+            "pass_tokens": ntok,
+            "expected_tokens": sum(r.prompt_len + r.output_len - 1 for r in reqs),
+            "latency_ms": {"p50": pct(50), "p90": pct(90), "p99": pct(99), "max": lat[-1],
+                           "mean": sum(lat) / len(lat)},
+            "kv_cache_gb": 2 * L * caches[0][0].numel() * 2 / 1e9,
+            "l2": "KV of every layer exceeds L2; no flush",
+            "warmup": "a separate 64-request trace on its own composer",
+        },
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # the oracle on the host cores (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 class OracleRunner:
@@ -662,7 +785,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.workload == "trace":
+            run_trace_bench(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

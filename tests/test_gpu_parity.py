@@ -139,3 +139,28 @@ def test_q_written_by_a_kernel_just_before_attention(rbkv, name, factor):
         o2 = rbkv.ragged_attention(p, q2, pair.kc, pair.vc)
         torch.cuda.synchronize()
         assert torch.equal(o2.view(torch.int16), r["o"].view(torch.int16))
+
+
+def test_closed_loop_trace_every_pass(rbkv):
+    """A small closed-loop trace (requests finish, are released, and clients
+    send their next ones): every pass's metadata, cache and outputs against
+    the oracle, the pool back to full at the end."""
+    reqs = workloads.trace_requests(seed=4, num_requests=12, num_clients=4,
+                                    prompt_mean=160.0, output_mean=6.0)
+    shape = workloads.Shape(32, 32, 128, 64, "bf16", 1.0 / np.sqrt(128.0))
+    nb = workloads.trace_block_pool(reqs, 4, 64)
+    pair = Pair(rbkv, shape, nb)
+    results = []
+
+    def compose(budget, max_chunk, states):
+        r = pair.step(budget, max_chunk, states)
+        results.append(r)
+        return r["meta"]
+
+    n = workloads.run_trace(reqs, 4, 64, 64, compose, pair.release)
+    assert n == len(results) and n > 10
+    for r in results:
+        if r["tokens"]:
+            _ok(r)
+    assert pair.cache_equal()
+    assert pair.lib.free_blocks() == nb
