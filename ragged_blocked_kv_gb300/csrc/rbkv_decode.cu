@@ -16,9 +16,7 @@
 //    P.V with MMAs;
 //  - at the end of a unit the four warps merge their (max, sum, O) states in
 //    shared memory and write either O (bf16) or the fp32 partial output and
-//    base-2 log-sum-exp; the CTA that finishes the last unit of a split row
-//    (per-row arrival counters in the pass metadata, reset by that CTA) merges
-//    the row's partials itself, so no combine launch is needed for decodes.
+//    base-2 log-sum-exp for the combine kernel.
 // Every wait is bounded: on timeout the kernel records RBKV_ERR_TIMEOUT in the
 // pass's status word and stops.
 #include "rbkv_internal.h"
@@ -56,12 +54,11 @@ struct Shared {
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
   volatile int* abort_flag;
-  volatile int* last_flag;   // this CTA finished the last unit of a split row
 };
 
 // shared memory: K/V ring | merge buffer | (max, sum) per warp and row |
 // full and empty barriers | abort flag
-static_assert(kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 8 <= kSmemBytes,
+static_assert(kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 4 <= kSmemBytes,
               "shared-memory layout overflows its allocation");
 
 __device__ __forceinline__ Shared carve(uint8_t* raw) {
@@ -72,7 +69,6 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
   s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * 16 * 2);
   s.empty = s.full + kStages;
   s.abort_flag = reinterpret_cast<volatile int*>(s.empty + kStages);
-  s.last_flag = s.abort_flag + 1;
   return s;
 }
 
@@ -390,48 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mw != -INFINITY) L += exp2f(mw - M) * sm.ml[(w * 16 + t) * 2 + 1];
       }
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
-    }
-    if (it.part >= 0) {
-      // One of several units of a (row, KV head): the last to finish merges
-      // their partial outputs (log-sum-exp combine, splits in index order, as
-      // the combine kernel does) and writes O.
-      __threadfence();
-      ptx::named_bar_sync(1, kConsumers * 32);
-      if (t == 0) {
-        const int nsplit = dp.decode_comb[it.comb].nsplit;
-        *sm.last_flag = atomicAdd(&dp.arrivals[it.comb], 1) == nsplit - 1;
-      }
-      ptx::named_bar_sync(1, kConsumers * 32);
-      if (*sm.last_flag) {
-        __threadfence();
-        const CombineRow cr = dp.decode_comb[it.comb];
-        for (int e = t; e < g * 32; e += kConsumers * 32) {
-          const int r = e >> 5, c4 = (e & 31) * 4;
-          float M = -INFINITY;
-          for (int i = 0; i < cr.nsplit; ++i)
-            M = fmaxf(M, __ldcg(part_lse + (int64_t)(cr.part_begin + i) * g + r));
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          float wsum = 0.f;
-          for (int i = 0; i < cr.nsplit; ++i) {
-            const int64_t slot = (int64_t)(cr.part_begin + i) * g + r;
-            const float lse = __ldcg(part_lse + slot);
-            const float wi = lse == -INFINITY ? 0.f : exp2f(lse - M);
-            wsum += wi;
-            const float4 po = __ldcg(reinterpret_cast<const float4*>(part_o + slot * 128 + c4));
-            acc.x = fmaf(wi, po.x, acc.x);
-            acc.y = fmaf(wi, po.y, acc.y);
-            acc.z = fmaf(wi, po.z, acc.z);
-            acc.w = fmaf(wi, po.w, acc.w);
-          }
-          const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-          __nv_bfloat16* orow = o + ((int64_t)cr.row * shp.H_q + cr.kv_head * g + r) * 128 + c4;
-          uint2 packed;
-          packed.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
-          packed.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(orow) = packed;
-        }
-        if (t == 0) dp.arrivals[it.comb] = 0;   // ready for the next launch
-      }
     }
     // all consumer warps leave together if anyone gave up
     if (ptx::named_bar_or(1, kConsumers * 32, abort_flag != 0)) break;

@@ -167,8 +167,7 @@ struct Plan {
   rbkv_plan_info info{};
   std::vector<WorkItem> decode, generic;
   std::vector<ChunkTile> chunk;
-  std::vector<CombineRow> combine;      // combine kernel
-  std::vector<CombineRow> decode_comb;  // merged inside the decode kernel
+  std::vector<CombineRow> combine;
   int32_t n_parts = 0;
   int32_t decode_grid = 0;
 };
@@ -298,21 +297,14 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
       split_keys(n_keys, split, gran, bounds);
       int32_t ns = (int32_t)bounds.size() - 1;
       max_splits = std::max(max_splits, ns);
-      int32_t part0 = -1, comb = -1;
+      int32_t part0 = -1;
       if (ns > 1) {
         part0 = pl.n_parts;
         pl.n_parts += ns;
-        // split decode units merge in the decode kernel; others in the combine kernel
-        if (&dst == &decode) {
-          comb = (int32_t)pl.decode_comb.size();
-          pl.decode_comb.push_back(CombineRow{row, h, part0, ns});
-        } else {
-          pl.combine.push_back(CombineRow{row, h, part0, ns});
-        }
+        pl.combine.push_back(CombineRow{row, h, part0, ns});
       }
       for (int32_t k = 0; k < ns; ++k)
-        dst.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1,
-                               table_off, comb, 0});
+        dst.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1, table_off});
     }
   };
   for (int32_t i = 0; i < S; ++i) {
@@ -426,9 +418,6 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     put(w, o_gen, pl.generic);
     put(w, o_chunk, pl.chunk);
     put(w, o_comb, pl.combine);
-    size_t o_dcomb, o_arr;
-    put(w, o_dcomb, pl.decode_comb);
-    put(w, o_arr, std::vector<int32_t>(pl.decode_comb.size(), 0));
     size_t bytes = w.size() * 4;
     PinnedBuf pin;
     cudaError_t e = p->pinned->acquire(bytes, pin);
@@ -456,14 +445,11 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     dp.generic_items = (const WorkItem*)(base + o_gen);
     dp.chunk_tiles = (const ChunkTile*)(base + o_chunk);
     dp.combine_rows = (const CombineRow*)(base + o_comb);
-    dp.decode_comb = (const CombineRow*)(base + o_dcomb);
-    dp.arrivals = base + o_arr;
     dp.num_tokens = (int32_t)p->slot.size();
     dp.n_decode = (int32_t)pl.decode.size();
     dp.n_generic = (int32_t)pl.generic.size();
     dp.n_chunk = (int32_t)pl.chunk.size();
     dp.n_combine = (int32_t)pl.combine.size();
-    dp.n_decode_comb = (int32_t)pl.decode_comb.size();
     dp.n_parts = pl.n_parts;
     dp.num_blocks = p->cfg.num_blocks;
     dp.decode_grid = pl.decode_grid;

@@ -23,11 +23,8 @@ struct WorkItem {
   int32_t key_end;
   int32_t part;
   int32_t table_off;  // offset of the sequence's block table in block_ids
-  int32_t comb;       // split units of the decode kernel: index of their merge row
-                      // in DevPass::decode_comb (the last unit to finish merges)
-  int32_t pad;
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem is 8 int32");
+static_assert(sizeof(WorkItem) == 24, "WorkItem is 6 int32");
 
 // (row, kv head) whose keys were split: partial slots [part_begin, part_begin+nsplit).
 struct CombineRow {
@@ -66,15 +63,12 @@ struct DevPass {
   const WorkItem* decode_items;    // fast decode path
   const WorkItem* generic_items;   // CUDA-core path
   const ChunkTile* chunk_tiles;    // tensor-core prompt path
-  const CombineRow* combine_rows;  // merged by the combine kernel (chunk and CUDA-core splits)
-  const CombineRow* decode_comb;   // merged inside the decode kernel
-  int32_t* arrivals;               // [n_decode_comb] units done per merge row (reset to 0 by the last)
+  const CombineRow* combine_rows;
   int32_t num_tokens;
   int32_t n_decode;
   int32_t n_generic;
   int32_t n_chunk;
   int32_t n_combine;
-  int32_t n_decode_comb;
   int32_t n_parts;
   int32_t num_blocks;
   int32_t decode_grid;             // CTAs of the persistent decode launch
