@@ -362,17 +362,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this row sees the tile's first `lim` keys: those <= its position and
       // before the split's end (a prefix of the tile, possibly empty or all)
       const int lim = min(pos + 1, ke) - key0;
-      float mraw = -INFINITY;
+      // row max over 8 independent partial maxima (no 64-long dependent chain)
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
       if (__all_sync(0xffffffffu, lim >= kKeys)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mraw = fmaxf(mraw, sc[c]);
+        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
       } else {
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           sc[c] = c < lim ? sc[c] : -INFINITY;
-          mraw = fmaxf(mraw, sc[c]);
+          mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
         }
       }
+      const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // the scale is positive, so the row max scales with it
       const float mt = mraw * qk_scale;
       float corr = 1.f;
@@ -383,12 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // a row with no key in this split so far keeps m_ref = -inf: its p are 0
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-      float ps = 0.f;
+      float ps8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         sc[c] = exp2f(fmaf(sc[c], qk_scale, nbase));
-        ps += sc[c];
+        ps8[c & 7] += sc[c];
       }
+      const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       l = l * corr + ps;
       // P buffer j & 1 is free once the PV of tile j - 2 has run
       if (j >= 2) {

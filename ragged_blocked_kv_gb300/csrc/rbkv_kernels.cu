@@ -1,9 +1,9 @@
 // kv_append, the CUDA-core attention path and the log-sum-exp combine.
 //
 // kv_append: FastGen guide, "Paged KV Memory Management" - new K/V rows go to
-//   fixed-size blocks reached through the block table.  One thread moves 16
-//   bytes of K and 16 bytes of V; consecutive threads cover consecutive bytes
-//   of a row, so loads and stores are fully coalesced 16-byte accesses.
+//   fixed-size blocks reached through the block table.  One warp per (token,
+//   KV head) row pair: half the warp copies the K row, half the V row, with
+//   coalesced 16-byte loads and stores.
 // generic attention: exact softmax attention of one (row, KV head, key split)
 //   work unit per CTA, online softmax over 32-key chunks (one key per lane),
 //   fp32 arithmetic.  Used for fp32 layers and for shapes outside the
@@ -41,31 +41,34 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // ---------------------------------------------------------------------------
 // kv_append
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) kv_append_kernel(DevPass dp, int32_t H_kv, int32_t B,
-                                                        int32_t vec_per_row,
-                                                        const uint4* __restrict__ k_new,
-                                                        const uint4* __restrict__ v_new,
-                                                        uint4* __restrict__ k_cache,
-                                                        uint4* __restrict__ v_cache) {
+// One warp per (token, KV head): the first half of the warp copies the K row,
+// the second half the V row, 16 bytes per lane per step (32-bit index math).
+constexpr int kAppendWarps = 8;
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    kv_append_kernel(DevPass dp, int32_t H_kv, int32_t B, int32_t vec_per_row,
+                     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache) {
   // the attention kernels may launch now; they wait for this grid before
   // reading the cache
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t total = (int64_t)dp.num_tokens * H_kv * vec_per_row;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t v = (int32_t)(i % vec_per_row);
-    const int64_t th = i / vec_per_row;         // t * H_kv + h
-    const int32_t h = (int32_t)(th % H_kv);
-    const int32_t t = (int32_t)(th / H_kv);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const uint4* __restrict__ src = half ? v_new : k_new;
+  uint4* __restrict__ dst = half ? v_cache : k_cache;
+  const uint32_t rows = (uint32_t)dp.num_tokens * (uint32_t)H_kv;
+  for (uint32_t r = blockIdx.x * kAppendWarps + warp; r < rows; r += gridDim.x * kAppendWarps) {
+    const uint32_t t = r / (uint32_t)H_kv;
+    const uint32_t h = r - t * (uint32_t)H_kv;
     const int32_t slot = dp.slot[t];
-    const int32_t blk = slot / B, off = slot - (slot / B) * B;
+    const int32_t blk = slot / B, off = slot - blk * B;
     if (slot < 0 || blk >= dp.num_blocks) {
-      report(dp.status, kDevBounds);
+      if (lane == 0) report(dp.status, kDevBounds);
       continue;
     }
-    const int64_t dst = (((int64_t)blk * H_kv + h) * B + off) * vec_per_row + v;
-    k_cache[dst] = k_new[i];
-    v_cache[dst] = v_new[i];
+    const uint4* s_row = src + (size_t)r * vec_per_row;
+    uint4* d_row = dst + (((size_t)blk * H_kv + h) * B + off) * vec_per_row;
+    for (int v = hl; v < vec_per_row; v += 16) d_row[v] = s_row[v];
   }
 }
 
@@ -209,14 +212,15 @@ cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* 
                              const void* v_new, void* k_cache, void* v_cache, cudaStream_t st) {
   const int esz = s.dtype == 0 ? 2 : 4;
   const int vec = s.D * esz / 16;
-  const int64_t total = (int64_t)dp.num_tokens * s.H_kv * vec;
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = (int64_t)num_sms_current() * 16;
+  const int64_t rows = (int64_t)dp.num_tokens * s.H_kv;
+  if (rows == 0) return cudaSuccess;
+  if (rows >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
+  const int64_t cap = (int64_t)num_sms_current() * 8;
   if (blocks > cap) blocks = cap;
-  kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(dp, s.H_kv, s.B, vec, (const uint4*)k_new,
-                                                     (const uint4*)v_new, (uint4*)k_cache,
-                                                     (uint4*)v_cache);
+  kv_append_kernel<<<(unsigned)blocks, kAppendWarps * 32, 0, st>>>(
+      dp, s.H_kv, s.B, vec, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
+      (uint4*)v_cache);
   return cudaGetLastError();
 }
 
