@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float corr = 1.f;
       const bool raise = mt > m_ref + kRescaleThreshold;
       if (raise) {
-        corr = exp2f(m_ref - mt);
+        corr = ptx::ex2(m_ref - mt);
         m_ref = mt;
       }
       // a row with no key in this split so far keeps m_ref = -inf: its p are 0
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        sc[c] = exp2f(fmaf(sc[c], qk_scale, nbase));
+        sc[c] = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
         ps8[c & 7] += sc[c];
       }
       const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));

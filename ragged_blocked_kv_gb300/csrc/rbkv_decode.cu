@@ -275,13 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        const float c0 = ptx::ex2(m0 - mn0), c1 = ptx::ex2(m1 - mn1);
         m0 = mn0;
         m1 = mn1;
-        const float p00 = exp2f(sc[0][0] - mn0), p01 = exp2f(sc[0][1] - mn0);
-        const float p02 = exp2f(sc[0][2] - mn1), p03 = exp2f(sc[0][3] - mn1);
-        const float p10 = exp2f(sc[1][0] - mn0), p11 = exp2f(sc[1][1] - mn0);
-        const float p12 = exp2f(sc[1][2] - mn1), p13 = exp2f(sc[1][3] - mn1);
+        const float p00 = ptx::ex2(sc[0][0] - mn0), p01 = ptx::ex2(sc[0][1] - mn0);
+        const float p02 = ptx::ex2(sc[0][2] - mn1), p03 = ptx::ex2(sc[0][3] - mn1);
+        const float p10 = ptx::ex2(sc[1][0] - mn0), p11 = ptx::ex2(sc[1][1] - mn0);
+        const float p12 = ptx::ex2(sc[1][2] - mn1), p13 = ptx::ex2(sc[1][3] - mn1);
         l0 = l0 * c0 + (p00 + p01 + p10 + p11);
         l1 = l1 * c1 + (p02 + p03 + p12 + p13);
         uint32_t pa[4];
@@ -337,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int w = 0; w < kConsumers; ++w) {
       const float mw0 = sm.ml[(w * 16 + r0) * 2], mw1 = sm.ml[(w * 16 + r1) * 2];
-      if (mw0 != -INFINITY) L0 += exp2f(mw0 - M0) * sm.ml[(w * 16 + r0) * 2 + 1];
-      if (mw1 != -INFINITY) L1 += exp2f(mw1 - M1) * sm.ml[(w * 16 + r1) * 2 + 1];
+      if (mw0 != -INFINITY) L0 += ptx::ex2(mw0 - M0) * sm.ml[(w * 16 + r0) * 2 + 1];
+      if (mw1 != -INFINITY) L1 += ptx::ex2(mw1 - M1) * sm.ml[(w * 16 + r1) * 2 + 1];
     }
-    const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - M0) / L0;
-    const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - M1) / L1;
+    const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : ptx::ex2(m0 - M0) / L0;
+    const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : ptx::ex2(m1 - M1) / L1;
     // each warp stores its rescaled O; then all four are summed per element
     float* scr = sm.scratch + warp * 16 * kRowPad;
 #pragma unroll
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, sm.ml[(w * 16 + t) * 2]);
       for (int w = 0; w < kConsumers; ++w) {
         const float mw = sm.ml[(w * 16 + t) * 2];
-        if (mw != -INFINITY) L += exp2f(mw - M) * sm.ml[(w * 16 + t) * 2 + 1];
+        if (mw != -INFINITY) L += ptx::ex2(mw - M) * sm.ml[(w * 16 + t) * 2 + 1];
       }
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
