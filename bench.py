@@ -183,6 +183,20 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def over_ranks(times, counts, world, device="cpu"):
+    """Replicas: the job's time is the slowest rank's, its work the sum of all
+    ranks' (max of ``times``, sum of ``counts``).  One rank: unchanged."""
+    if world <= 1:
+        return [float(x) for x in times], [float(x) for x in counts]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64, device=device)
+    c = torch.tensor([float(x) for x in counts], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(c, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], [float(x) for x in c.tolist()]
+
+
 def traffic_bytes(workload, kernel):
     """ncu DRAM traffic per launch recorded for this kernel and workload, or
     None when there is none or the kernel source changed since."""
@@ -416,17 +430,8 @@ def run_ours(args, rank, world, local_rank):
     d2h = e2e_work["tokens"] * sh.num_heads_q * sh.head_dim * esz / K
 
     # ---- max over ranks --------------------------------------------------
-    t = torch.tensor([ms, e2e_ms, float(tokens), float(e2e_tokens)], dtype=torch.float64,
-                     device=device)
-    if world > 1:
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        sm = t.clone()
-        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
-        ms, e2e_ms = float(mx[0]), float(mx[1])
-        tot_tokens, tot_e2e = float(sm[2]), float(sm[3])
-    else:
-        tot_tokens, tot_e2e = float(tokens), float(e2e_tokens)
+    (ms, e2e_ms), (tot_tokens, tot_e2e) = over_ranks([ms, e2e_ms], [tokens, e2e_tokens],
+                                                     world, device)
     if rank != 0:
         return
 
@@ -580,9 +585,9 @@ def run_trace_bench(args, rank, world, local_rank):
     def pct(x):
         return lat[min(len(lat) - 1, int(round(x / 100.0 * (len(lat) - 1))))]
 
+    (total_ms,), (ntok,) = over_ranks([total_ms], [sum(tokens)], world, device)
     if rank != 0:
         return
-    ntok = sum(tokens)
     line = {
         "metric": "ragged SplitFuse attention pass tokens/s",
         "value": ntok / (total_ms / 1e3),
@@ -600,7 +605,7 @@ def run_trace_bench(args, rank, world, local_rank):
             "workload": f"trace: {len(reqs)} requests, 32 closed-loop clients, budget 512, "
                         f"chunk cap 512, {L} layers of 32q/32kv heads, head_dim 128, block 64",
             "passes": npass,
-            "pass_tokens": ntok,
+            "pass_tokens": int(ntok),
             "expected_tokens": sum(r.prompt_len + r.output_len - 1 for r in reqs),
             "latency_ms": {"p50": pct(50), "p90": pct(90), "p99": pct(99), "max": lat[-1],
                            "mean": sum(lat) / len(lat)},
@@ -686,13 +691,72 @@ class OracleRunner:
         return done / H
 
 
+class OracleTraceRunner:
+    """The oracle over the trace workload (one layer): each step is the next
+    pass of the closed-loop trace - oracle composition and appending of the
+    whole pass, then ``pairs`` (row, query head) outputs of it."""
+
+    def __init__(self, seed):
+        import numpy as np
+        import oracle
+        import workloads
+        self.np, self.oracle, self.workloads = np, oracle, workloads
+        self.shape = workloads.Shape(32, 32, 128, 64, "bf16", 1.0 / math.sqrt(128.0))
+        self.reqs = workloads.trace_requests(seed=seed)
+        nb = workloads.trace_block_pool(self.reqs, 32, 64)
+        self.comp = oracle.Composer(64, nb)
+        self.kc = oracle.BlockedCache(32, 64, 128, np.uint16)
+        self.vc = oracle.BlockedCache(32, 64, 128, np.uint16)
+        q, k, v = workloads.make_qkv(self.shape, 512, seed, 1000)
+        self.inputs = [t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+                       for t in (q, k, v)]
+        self.seed = seed
+
+    def run(self, steps, pairs, on_step):
+        q, k, v = self.inputs
+        H = self.shape.num_heads_q
+
+        def compose(b, M, states):
+            m = self.comp.compose(b, M, states)
+            T = m.num_tokens
+            self.oracle.kv_append(m, k[:T], v[:T], self.kc, self.vc)
+            done = 0
+            c = 0
+            while done < pairs and T:
+                t, h0 = divmod(c % (T * H), H)
+                n = min(pairs - done, H - h0)
+                self.oracle.blocked_attention(m, q[:T], self.kc, self.vc, H, tokens=[t],
+                                              heads=range(h0, h0 + n))
+                done += n
+                c += n
+            on_step(done / H)
+            return m
+        self.workloads.run_trace(self.reqs, 32, 512, 512, compose, self.comp.release,
+                                 max_passes=steps)
+
+
 def oracle_measure(workload, seed, steps, warmup, pair_budget=2000):
     """Time ``steps`` oracle steps after ``warmup``; each step computes
     max(1, pair_budget // (steps + warmup)) output pairs, so the whole run
     stays within a few minutes whatever the step count."""
     import workloads
-    scn = workloads.SCENARIOS[workload](seed)
     pairs = max(1, pair_budget // max(1, steps + warmup))
+    if workload == "trace":
+        t0 = time.perf_counter()
+        tr = OracleTraceRunner(seed)
+        setup = time.perf_counter() - t0
+        marks = []
+
+        def on_step(tok):
+            marks.append((time.perf_counter(), tok))
+        tr.run(steps + warmup, pairs, on_step)
+        timed = marks[warmup:]
+        t_start = marks[warmup - 1][0] if warmup else (marks[0][0] - 1e-9)
+        dt = timed[-1][0] - t_start
+        tokens = sum(x[1] for x in timed)
+        return {"value": tokens / dt, "tokens": tokens, "pairs_per_step": pairs, "seconds": dt,
+                "setup_seconds": setup}
+    scn = workloads.SCENARIOS[workload](seed)
     t0 = time.perf_counter()
     r = OracleRunner(scn, seed)
     setup = time.perf_counter() - t0
@@ -736,7 +800,11 @@ def run_reference(args, rank):
         return
     import workloads
     res = oracle_measure(args.workload, args.seed, args.steps, args.warmup)
-    scn = workloads.SCENARIOS[args.workload](args.seed)
+    if args.workload == "trace":
+        scn = workloads.Scenario("trace", workloads.Shape(32, 32, 128, 64, "bf16", 1.0), 512,
+                                 512, [], [], 0)
+    else:
+        scn = workloads.SCENARIOS[args.workload](args.seed)
     sh = scn.shape
     v = res["value"]
     line = {

@@ -81,10 +81,17 @@ def test_empty_pass_and_repeat_determinism(rbkv):
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
-@pytest.mark.parametrize("hq,hkv,B", [(16, 16, 64), (32, 8, 64), (64, 8, 64), (16, 1, 64),
-                                      (8, 2, 16), (8, 2, 32), (8, 4, 128)])
-def test_shapes_and_block_sizes(rbkv, hq, hkv, B):
-    shape = workloads.Shape(hq, hkv, 128, B, "bf16", 1.0 / np.sqrt(128.0))
+@pytest.mark.parametrize("hq,hkv,B,D,dt", [
+    (16, 16, 64, 128, "bf16"), (32, 8, 64, 128, "bf16"), (64, 8, 64, 128, "bf16"),
+    (16, 1, 64, 128, "bf16"),                     # g = 16: the largest group on the MMA decode path
+    (64, 2, 64, 128, "bf16"),                     # g = 32: decode on the CUDA-core path
+    (8, 2, 16, 128, "bf16"), (8, 2, 32, 128, "bf16"), (8, 4, 128, 128, "bf16"),
+    (8, 2, 256, 128, "bf16"),                     # blocks larger than a key tile
+    (8, 2, 64, 64, "bf16"),                       # head_dim 64: CUDA-core path
+    (16, 4, 64, 128, "f32"),                      # fp32 with grouped heads
+])
+def test_shapes_and_block_sizes(rbkv, hq, hkv, B, D, dt):
+    shape = workloads.Shape(hq, hkv, D, B, dt, 1.0 / np.sqrt(D))
     rng = np.random.default_rng(hq * 131 + hkv * 7 + B)
     # contexts at and around block/tile boundaries, a 1-token prompt, a chunk
     hist = [(10 + i, c) for i, c in enumerate([1, 63, 64, 65, 127, 128, 129, 300,
@@ -95,6 +102,19 @@ def test_shapes_and_block_sizes(rbkv, hq, hkv, B):
     (r,) = run_scenario(rbkv, scn)
     _ok(r)
     assert r["pair"].cache_equal()
+
+
+def test_long_context_decode_and_chunk(rbkv):
+    """A 40k-token decode context and a 700-row chunk behind a 30k prefix."""
+    shape = workloads.Shape(16, 4, 128, 64, "bf16", 1.0 / np.sqrt(128.0))
+    hist = [(10, 40000), (11, 30000), (12, 777)]
+    nb = sum(-(-(c + 800) // 64) for _, c in hist) + 16
+    scn = workloads.Scenario("long", shape, 702, 700, hist,
+                             [(10, 40000, 40000), (11, 30700, 30000), (12, 777, 777)], nb)
+    (r,) = run_scenario(rbkv, scn, only_seqs={10, 11, 12}, input_device="cuda")
+    assert r["meta_equal"] and r["finite"]
+    assert r["max_abs"] <= MAX_ABS_TOL and r["mean_abs"] <= MEAN_ABS_TOL
+    assert r["plan"]["max_splits"] >= 1
 
 
 @pytest.mark.parametrize("name", ["decode_stress", "mistral_7b", "llama2_7b"])
