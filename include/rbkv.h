@@ -164,6 +164,42 @@ rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t ma
  * Composing the same states again afterwards yields the same metadata. */
 rbkv_status rbkv_pass_rollback(rbkv_composer* c, const rbkv_pass* p);
 
+/* Chunk policies for rbkv_compose_pass_policy. */
+typedef enum {
+  RBKV_CHUNK_GREEDY = 0, /* a prefilling request takes min(remaining prompt, max_chunk,
+                            remaining budget): the pass holds exactly the budget when
+                            demand allows (rbkv_compose_pass) */
+  RBKV_CHUNK_EQUAL = 1   /* a prompt longer than what the pass allows it (a = min(max_chunk,
+                            remaining budget)) is cut into the fewest chunks of at most a
+                            tokens, all of near-equal size: this pass takes
+                            ceil(r / ceil(r / a)) of its r remaining tokens */
+} rbkv_chunk_policy;
+
+/* rbkv_compose_pass with a chunk policy.  RBKV_CHUNK_EQUAL follows the FastGen
+ * paper summary page, idea I2: throughput is concave in the tokens of a pass,
+ * so a pool of prompt tokens is best spread evenly over the passes it needs.
+ * The prompt still finishes in the same number of passes as with
+ * RBKV_CHUNK_GREEDY; a pass may then hold fewer tokens than the budget.
+ * Errors: as rbkv_compose_pass, and RBKV_ERR_INVALID for an unknown policy. */
+rbkv_status rbkv_compose_pass_policy(rbkv_composer* c, int32_t token_budget, int32_t max_chunk,
+                                     int32_t chunk_policy, const rbkv_seq_state* states,
+                                     int32_t n_states, rbkv_pass** out);
+
+/* A latency-bounded token budget (FastGen paper summary page, idea I1: the
+ * latency of a forward pass depends mainly on its token count; FastGen guide,
+ * "Prompt-Decode Decoupling": keep each iteration under a latency bound).
+ * tokens[0..n-1] (strictly increasing, >= 0) and latency[0..n-1] are a measured
+ * profile; the predicted latency of t tokens is the linear interpolation
+ * between the two profile points around t (rbkv_latency_at).  Returns the
+ * largest t in [tokens[0], tokens[n-1]] whose predicted latency is <= bound,
+ * 0 if there is none, -1 for a bad profile (n < 2, not increasing, NULL). */
+int32_t rbkv_budget_for_latency(const int32_t* tokens, const double* latency, int32_t n,
+                                double bound);
+
+/* Predicted latency of t tokens from a profile (as above; t within the profile
+ * range, the profile valid). */
+double rbkv_latency_at(const int32_t* tokens, const double* latency, int32_t n, int32_t t);
+
 /* Return every block of seq_id to the pool and forget the sequence.
  * Errors: RBKV_ERR_INVALID for an unknown id. */
 rbkv_status rbkv_release_seq(rbkv_composer* c, int64_t seq_id);

@@ -30,7 +30,7 @@ split invariance and chunk invariance.  Block ids follow a stated rule (lowest
 free id first, in layout order) that the pages do not fix: parity of block ids
 is pinned only by that rule.
 """
-from .composer import Composer, PassMeta, InvalidRequest, NoBlocks  # noqa: F401
+from .composer import Composer, PassMeta, InvalidRequest, NoBlocks, budget_for_latency, latency_at  # noqa: F401
 from .cache import BlockedCache, kv_append  # noqa: F401
 from .attention import (  # noqa: F401
     widen,

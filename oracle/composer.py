@@ -16,7 +16,9 @@ The pages fix the goal, not the order of the steps.  Readings taken here:
    prompt).
 3. Then each prefilling sequence, in list order, takes
    ``min(prompt_len - seen, max_chunk, remaining)`` tokens (no cap when
-   ``max_chunk <= 0``).
+   ``max_chunk <= 0``).  Under the "equal" policy a prompt longer than that
+   allowance ``a`` takes ``ceil(r / ceil(r / a))`` of its ``r`` remaining
+   tokens instead (same number of passes, near-equal chunks).
 4. The pass lays out the scheduled sequences in list order.
 5. Each laid-out sequence receives ``ceil(ctx / B) - held`` new blocks, lowest
    free id first, sequences in layout order.  If the pool is short the call
@@ -88,8 +90,17 @@ class Composer:
 
     # -- the pass -------------------------------------------------------------
     def compose(self, budget: int, max_chunk: int,
-                states: Sequence[Tuple[int, int, int]]) -> PassMeta:
-        """Compose one pass from ``states`` = [(seq_id, prompt_len, seen), ...]."""
+                states: Sequence[Tuple[int, int, int]], policy: str = "greedy") -> PassMeta:
+        """Compose one pass from ``states`` = [(seq_id, prompt_len, seen), ...].
+
+        ``policy`` "greedy": a prefilling request takes min(remaining prompt,
+        max_chunk, remaining budget).  "equal" (paper summary page, idea I2:
+        throughput is concave in tokens per pass, so a pool of tokens is best
+        spread evenly): a prompt longer than what it is allowed this pass
+        (a = min(max_chunk, remaining budget)) is cut into the fewest chunks of
+        at most a tokens, all of near-equal size."""
+        if policy not in ("greedy", "equal"):
+            raise InvalidRequest("unknown chunk policy")
         if budget < 0:
             raise InvalidRequest("token budget must be >= 0")
         ids = [int(s[0]) for s in states]
@@ -112,10 +123,12 @@ class Composer:
         # step 3: prompt chunks, list order
         for i, (_, plen, seen) in enumerate(states):
             if seen < plen:
-                n = plen - seen
-                if max_chunk > 0:
-                    n = min(n, max_chunk)
-                n = min(n, remaining)
+                rem = plen - seen
+                allow = remaining if max_chunk <= 0 else min(remaining, max_chunk)
+                n = min(rem, allow)
+                if policy == "equal" and allow > 0 and rem > allow:
+                    k = -(-rem // allow)          # fewest chunks of at most `allow`
+                    n = -(-rem // k)              # their (near-)equal size
                 take[i] = n
                 remaining -= n
 
@@ -184,3 +197,27 @@ class Composer:
         for b in self._held.pop(sid, []):
             heapq.heappush(self._free, b)
         self._tokens.pop(sid, None)
+
+
+def latency_at(tokens: Sequence[int], latency: Sequence[float], t: int) -> float:
+    """Predicted latency of t tokens: linear interpolation between the two
+    profile points around t (paper summary page, idea I1: latency of a pass
+    follows its token count)."""
+    i = 0
+    while i + 2 < len(tokens) and t > tokens[i + 1]:
+        i += 1
+    f = float(t - tokens[i]) / float(tokens[i + 1] - tokens[i])
+    return latency[i] + (latency[i + 1] - latency[i]) * f
+
+
+def budget_for_latency(tokens: Sequence[int], latency: Sequence[float], bound: float) -> int:
+    """Largest token count in the profile's range whose predicted latency is
+    within ``bound`` (FastGen guide, "Prompt-Decode Decoupling": keep each
+    iteration under a latency bound); 0 if none; -1 for a bad profile."""
+    n = len(tokens)
+    if n < 2 or any(tokens[i + 1] <= tokens[i] for i in range(n - 1)) or tokens[0] < 0:
+        return -1
+    for t in range(tokens[-1], tokens[0] - 1, -1):
+        if latency_at(tokens, latency, t) <= bound:
+            return t
+    return 0

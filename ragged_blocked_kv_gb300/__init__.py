@@ -73,6 +73,12 @@ SIGNATURES = {
     "rbkv_compose_pass": (C.c_int, [_P, C.c_int32, C.c_int32, C.POINTER(_SeqState), C.c_int32,
                                     C.POINTER(_P)]),
     "rbkv_release_seq": (C.c_int, [_P, C.c_int64]),
+    "rbkv_compose_pass_policy": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32,
+                                           C.POINTER(_SeqState), C.c_int32, C.POINTER(_P)]),
+    "rbkv_budget_for_latency": (C.c_int32, [C.POINTER(C.c_int32), C.POINTER(C.c_double),
+                                            C.c_int32, C.c_double]),
+    "rbkv_latency_at": (C.c_double, [C.POINTER(C.c_int32), C.POINTER(C.c_double), C.c_int32,
+                                     C.c_int32]),
     "rbkv_pass_rollback": (C.c_int, [_P, _P]),
     "rbkv_composer_free_blocks": (C.c_int32, [_P]),
     "rbkv_pass_get_meta": (C.c_int, [_P, C.POINTER(_PassMeta)]),
@@ -252,14 +258,20 @@ class Composer:
         _check(lib().rbkv_composer_create(C.byref(cfg), C.byref(h)))
         self._h = h
 
-    def compose(self, budget: int, max_chunk: int, states) -> Pass:
+    def compose(self, budget: int, max_chunk: int, states, policy: str = "greedy") -> Pass:
         """``states``: [(seq_id, prompt_len, seen), ...] in list order, or an
-        array made once with ``seq_states`` (cheaper when reused)."""
+        array made once with ``seq_states`` (cheaper when reused).  ``policy``:
+        "greedy" (fill the budget) or "equal" (near-equal prompt chunks)."""
         if not isinstance(states, SeqStates):
             states = seq_states(states)
         out = _P()
-        _check(lib().rbkv_compose_pass(self._h, int(budget), int(max_chunk), states.arr, states.n,
-                                       C.byref(out)))
+        if policy == "greedy":
+            _check(lib().rbkv_compose_pass(self._h, int(budget), int(max_chunk), states.arr,
+                                           states.n, C.byref(out)))
+        else:
+            pol = {"equal": 1}.get(policy, -1)
+            _check(lib().rbkv_compose_pass_policy(self._h, int(budget), int(max_chunk), pol,
+                                                  states.arr, states.n, C.byref(out)))
         return Pass(out.value, self.config)
 
     def rollback(self, p: Pass) -> None:
@@ -360,6 +372,18 @@ def ragged_attention_noalloc(p: Pass, q, k_cache, v_cache, o, stream=None):
     return o
 
 
+def budget_for_latency(tokens, latency, bound: float) -> int:
+    """Largest token count whose latency, interpolated from a measured
+    (tokens, latency) profile, stays within ``bound`` (0 if none)."""
+    n = len(tokens)
+    t = (C.c_int32 * n)(*[int(x) for x in tokens])
+    l = (C.c_double * n)(*[float(x) for x in latency])
+    r = int(lib().rbkv_budget_for_latency(t, l, n, float(bound)))
+    if r < 0:
+        raise RbkvError(ERR_INVALID, "bad latency profile")
+    return r
+
+
 def kernel_launches() -> int:
     """Kernels launched through the library by this process so far."""
     return int(lib().rbkv_kernel_launches())
@@ -383,5 +407,5 @@ def profile_read() -> dict:
     return out
 
 
-__all__ = ["seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+__all__ = ["budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
            "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

@@ -36,7 +36,7 @@ def nvcc() -> str:
 
 
 def _flags(verbose: bool):
-    f = ["-O3", "-std=c++17", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC,-O3",
+    f = ["-O3", "-std=c++17", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC,-O3,-ffp-contract=off",
          f"-I{INCLUDE}", f"-I{CSRC}"]
     if verbose:
         f += ["-Xptxas", "-v"]

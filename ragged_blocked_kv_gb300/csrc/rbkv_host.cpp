@@ -569,7 +569,16 @@ int32_t rbkv_composer_free_blocks(const rbkv_composer* c) { return c ? c->pool.f
 
 rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t max_chunk,
                               const rbkv_seq_state* states, int32_t n_states, rbkv_pass** out) {
+  return rbkv_compose_pass_policy(c, token_budget, max_chunk, RBKV_CHUNK_GREEDY, states,
+                                  n_states, out);
+}
+
+rbkv_status rbkv_compose_pass_policy(rbkv_composer* c, int32_t token_budget, int32_t max_chunk,
+                                     int32_t chunk_policy, const rbkv_seq_state* states,
+                                     int32_t n_states, rbkv_pass** out) {
   if (!c || !out) return fail(RBKV_ERR_INVALID, "composer or out is NULL");
+  if (chunk_policy != RBKV_CHUNK_GREEDY && chunk_policy != RBKV_CHUNK_EQUAL)
+    return fail(RBKV_ERR_INVALID, "unknown chunk policy");
   if (token_budget < 0) return fail(RBKV_ERR_INVALID, "token budget must be >= 0");
   if (n_states < 0 || (n_states > 0 && !states))
     return fail(RBKV_ERR_INVALID, "states must hold n_states entries");
@@ -598,9 +607,15 @@ rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t ma
     for (int32_t i = 0; i < n_states; ++i) {
       const rbkv_seq_state& q = states[i];
       if (q.seen >= q.prompt_len) continue;
-      int32_t n = q.prompt_len - q.seen;
-      if (max_chunk > 0 && n > max_chunk) n = max_chunk;
-      if (n > left) n = left;
+      const int32_t rem = q.prompt_len - q.seen;
+      int32_t allow = left;
+      if (max_chunk > 0 && allow > max_chunk) allow = max_chunk;
+      int32_t n = rem < allow ? rem : allow;
+      if (chunk_policy == RBKV_CHUNK_EQUAL && allow > 0 && rem > allow) {
+        // the fewest chunks of at most `allow` tokens, all of (near-)equal size
+        const int32_t k = ceil_div(rem, allow);
+        n = ceil_div(rem, k);
+      }
       take[i] = n;
       left -= n;
     }
@@ -645,6 +660,24 @@ rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t ma
     return fail(RBKV_ERR_INVALID, "out of host memory");
   }
   return RBKV_OK;
+}
+
+double rbkv_latency_at(const int32_t* tokens, const double* latency, int32_t n, int32_t t) {
+  // piecewise-linear interpolation of a measured (tokens, latency) profile
+  int32_t i = 0;
+  while (i + 2 < n && t > tokens[i + 1]) ++i;
+  const double f = (double)(t - tokens[i]) / (double)(tokens[i + 1] - tokens[i]);
+  return latency[i] + (latency[i + 1] - latency[i]) * f;
+}
+
+int32_t rbkv_budget_for_latency(const int32_t* tokens, const double* latency, int32_t n,
+                                double bound) {
+  if (!tokens || !latency || n < 2) return -1;
+  for (int32_t i = 0; i + 1 < n; ++i)
+    if (tokens[i + 1] <= tokens[i] || tokens[i] < 0) return -1;
+  for (int32_t t = tokens[n - 1]; t >= tokens[0]; --t)
+    if (rbkv_latency_at(tokens, latency, n, t) <= bound) return t;
+  return 0;
 }
 
 rbkv_status rbkv_release_seq(rbkv_composer* c, int64_t seq_id) {

@@ -250,3 +250,108 @@ def test_rollback_restores_state_bit_exact(rbkv):
             orc_c.rollback(m)
             assert lib_c.free_blocks() == orc_c.free_blocks()
         assert lib_c.free_blocks() == free0
+
+
+# -- chunk policy "equal" and the latency-bounded budget --------------------
+
+
+class BothPolicy(Both):
+    def __init__(self, rbkv, B, num_blocks, policy, shape=(8, 2, 64, "f32")):
+        super().__init__(rbkv, B, num_blocks, shape)
+        self.policy = policy
+
+    def compose(self, budget, max_chunk, states):
+        p = self.lib.compose(budget, max_chunk, states, policy=self.policy)
+        m = self.orc.compose(budget, max_chunk, states, policy=self.policy)
+        _same(p, m)
+        assert self.lib.free_blocks() == self.orc.free_blocks()
+        return m
+
+
+def _prefill_passes(both, budget, max_chunk, states):
+    """Compose until every prompt is consumed; return [{seq_id: n_new}]."""
+    out = []
+    for _ in range(10_000):
+        m = both.compose(budget, max_chunk, states)
+        if all(seen >= pl for _, pl, seen in states):
+            break
+        n = dict(zip(m.seq_ids, m.n_new))
+        out.append(n)
+        assert sum(n.values()) <= budget
+        states = [(sid, pl, seen + n.get(sid, 0)) for sid, pl, seen in states]
+    return out
+
+
+def test_equal_chunks_llama2_7b(rbkv):
+    """4096-token prompt behind 15 decodes, budget 512, cap 512: the greedy
+    policy cuts 8 x 497 + 120; the equal policy keeps the same 9 passes with
+    chunks that differ by at most one token (4096 = 456 + 8 x 455)."""
+    scn = workloads.llama2_7b(0)
+    sh = scn.shape
+    both = BothPolicy(rbkv, sh.block_size, scn.num_blocks, "equal",
+                      (sh.num_heads_q, sh.num_heads_kv, sh.head_dim, sh.dtype))
+    b, st = scn.registration()
+    both.compose(b, 0, st)
+    passes = _prefill_passes(both, scn.budget, scn.max_chunk, list(scn.requests))
+    chunks = [p[1] for p in passes]
+    assert len(chunks) == 9 and sum(chunks) == 4096
+    assert max(chunks) - min(chunks) <= 1
+    assert chunks == [456] + [455] * 8
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_equal_policy_random_bit_exact(rbkv, seed):
+    rng = np.random.default_rng(700 + seed)
+    B = int(rng.choice([1, 16, 64]))
+    both = BothPolicy(rbkv, B, 100_000, "equal")
+    states = [(i + 1, int(rng.integers(1, 3000)), 0) for i in range(int(rng.integers(1, 8)))]
+    budget = int(rng.integers(1, 700))
+    M = int(rng.choice([0, 64, 256, 512]))
+    passes = _prefill_passes(both, budget, M, states)
+    # with one prompt the equal policy needs no more passes than greedy
+    if len(states) == 1:
+        g = BothPolicy(rbkv, B, 100_000, "greedy")
+        assert len(_prefill_passes(g, budget, M, states)) == len(passes)
+        ch = [p[1] for p in passes]
+        assert max(ch) - min(ch) <= 1
+
+
+def test_unknown_policy_rejected(rbkv):
+    c = rbkv.Composer(rbkv.Config(8, 2, 64, 16, "f32", 10))
+    with pytest.raises(rbkv.RbkvError):
+        c.compose(10, 0, [(1, 5, 0)], policy="bogus")
+    with pytest.raises(oracle.InvalidRequest):
+        oracle.Composer(16, 10).compose(10, 0, [(1, 5, 0)], policy="bogus")
+
+
+def test_budget_for_latency_pins(rbkv):
+    """Closed forms: a linear profile l(t) = a + b t gives floor((L - a) / b);
+    below the first point gives 0; above the last gives the last token count;
+    a flat segment at the bound keeps its far end."""
+    tok, lat = [0, 1000], [2.0, 12.0]          # 2 ms + 0.01 ms per token
+    for L, want in [(7.0, 500), (2.0, 0), (1.0, 0), (12.0, 1000), (50.0, 1000), (7.005, 500)]:
+        assert oracle.budget_for_latency(tok, lat, L) == want
+        assert rbkv.budget_for_latency(tok, lat, L) == want
+    tok, lat = [64, 128, 512, 2048], [3.0, 3.0, 5.0, 14.0]
+    assert oracle.budget_for_latency(tok, lat, 3.0) == 128
+    assert oracle.budget_for_latency(tok, lat, 2.0) == 0
+    assert oracle.budget_for_latency(tok, lat, 5.0) == 512
+    assert oracle.budget_for_latency(tok, [5.0, 3.0, 9.0, 1.0], 4.0) == 2048  # not monotone
+    assert oracle.budget_for_latency([5, 5], [1.0, 2.0], 3.0) == -1
+    with pytest.raises(rbkv.RbkvError):
+        rbkv.budget_for_latency([5, 5], [1.0, 2.0], 3.0)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_budget_for_latency_random_bit_exact(rbkv, seed):
+    rng = np.random.default_rng(900 + seed)
+    n = int(rng.integers(2, 9))
+    tok = np.sort(rng.choice(5000, size=n, replace=False)).tolist()
+    lat = np.cumsum(rng.random(n) * 3).tolist()
+    for L in rng.random(6) * (lat[-1] + 1):
+        a = oracle.budget_for_latency(tok, lat, float(L))
+        assert rbkv.budget_for_latency(tok, lat, float(L)) == a
+        if a > 0:
+            assert oracle.latency_at(tok, lat, a) <= L
+            if a < tok[-1]:
+                assert oracle.latency_at(tok, lat, a + 1) > L
