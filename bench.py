@@ -54,8 +54,21 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=90)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama2_7b",
-                    choices=["llama2_7b", "decode_stress", "mistral_7b", "trace"])
-    ap.add_argument("--layers", type=int, default=32, help="layers per pass (trace workload)")
+                    choices=["llama2_7b", "decode_stress", "mistral_7b", "trace", "profile"])
+    ap.add_argument("--layers", type=int, default=32,
+                    help="layers per pass (trace and profile workloads)")
+    ap.add_argument("--layer", choices=["attention", "full"], default="attention",
+                    help="per layer: the library's append + attention, or a whole "
+                         "random-weight decoder layer (trace and profile workloads)")
+    ap.add_argument("--policy", choices=["greedy", "equal"], default="greedy",
+                    help="prompt chunk policy (trace workload)")
+    ap.add_argument("--budget", type=int, default=512,
+                    help="tokens per pass (trace workload); 0 = from the latency profile")
+    ap.add_argument("--latency-bound", type=float, default=30.0,
+                    help="pass latency bound in ms for --budget 0 and the profile workload")
+    ap.add_argument("--ttft-sla", type=float, default=1000.0, help="TTFT bound, ms")
+    ap.add_argument("--pace-sla", type=float, default=25.0,
+                    help="bound on a request's mean interval between tokens, ms")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
@@ -500,14 +513,62 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 # trace workload: closed-loop SplitFuse serving of 512 requests
 # ---------------------------------------------------------------------------
-def run_trace_bench(args, rank, world, local_rank):
-    """512 requests from 32 closed-loop clients (prompt lengths round(N(2600,
-    780^2)), output lengths round(N(60, 18^2)), at least 1), composed into
-    512-token passes until every request has finished.  Each pass runs
-    kv_append and ragged attention for every layer (Llama-2-7B attention
-    shape, one K/V cache per layer, one block table shared by all layers).
-    Reports pass tokens per second over the whole trace and the distribution
-    of per-pass latency (all layers of a pass, CUDA events)."""
+class DenseStack:
+    """Random-weight Llama-2-7B-shaped decoder layers around the library's
+    attention: RMSNorm, a fused Q/K/V projection, the KV append and ragged
+    attention, the output projection, RMSNorm and a SwiGLU MLP (hidden 4096,
+    intermediate 11008), with residual adds.  The projections are plain cuBLAS
+    GEMMs (torch.matmul); rotary embeddings are left out (elementwise work that
+    does not change the shape of the pass).  It exists to measure pass latency
+    against token count (paper summary page, ideas I1/I2)."""
+
+    HIDDEN, INTER = 4096, 11008
+
+    def __init__(self, torch, rbkv, cfg, layers, max_tokens, device, seed):
+        H, I = self.HIDDEN, self.INTER
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+
+        def w(*shape, fan_in):
+            return (torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+                    * fan_in ** -0.5).to(torch.bfloat16)
+        self.layers = []
+        for _ in range(layers):
+            self.layers.append({"qkv": w(3, H, H, fan_in=H), "o": w(H, H, fan_in=H),
+                                "gu": w(2, H, I, fan_in=H), "down": w(I, H, fan_in=I),
+                                "n1": torch.ones(H, device=device, dtype=torch.bfloat16),
+                                "n2": torch.ones(H, device=device, dtype=torch.bfloat16)})
+        self.x0 = torch.randn(max_tokens, H, generator=g, device=device,
+                              dtype=torch.float32).to(torch.bfloat16)
+        self.o = torch.empty(max_tokens, cfg.num_heads_q, cfg.head_dim, device=device,
+                             dtype=torch.bfloat16)
+        self.torch, self.rbkv, self.cfg = torch, rbkv, cfg
+
+    def weight_bytes(self):
+        return sum(t.numel() * t.element_size() for l in self.layers for t in l.values())
+
+    def forward(self, p, caches, ws, hs):
+        torch, rbkv = self.torch, self.rbkv
+        F = torch.nn.functional
+        T = p.num_tokens
+        hq, d = self.cfg.num_heads_q, self.cfg.head_dim
+        x = self.x0[:T]
+        o = self.o[:T]
+        for l, W in enumerate(self.layers):
+            kc, vc = caches[l]
+            h = F.rms_norm(x, (self.HIDDEN,), W["n1"], 1e-5)
+            qkv = torch.matmul(h, W["qkv"])                 # [3][T][hidden], each contiguous
+            q, k, v = (qkv[i].view(T, hq, d) for i in range(3))
+            rbkv.kv_append(p, k, v, kc, vc, stream=hs)
+            rbkv.ragged_attention(p, q, kc, vc, o=o, workspace=ws, stream=hs)
+            x = x + torch.matmul(o.view(T, self.HIDDEN), W["o"])
+            h = F.rms_norm(x, (self.HIDDEN,), W["n2"], 1e-5)
+            gu = torch.matmul(h, W["gu"])
+            x = x + torch.matmul(F.silu(gu[0]) * gu[1], W["down"])
+        return x
+
+
+def _trace_setup(args, rank, world, local_rank, max_tokens):
     import torch
     import workloads
     from ragged_blocked_kv_gb300 import build as _build
@@ -520,43 +581,174 @@ def run_trace_bench(args, rank, world, local_rank):
     device = f"cuda:{local_rank}"
     torch.cuda.set_device(local_rank)
     L = args.layers
-    shape = workloads.Shape(32, 32, 128, 64, "bf16", 1.0 / math.sqrt(128.0))
     reqs = workloads.trace_requests(seed=args.seed)
-    nb = workloads.trace_block_pool(reqs, 32, shape.block_size)
+    nb = workloads.trace_block_pool(reqs, 32, 64)
     cfg = rbkv.Config(32, 32, 128, 64, "bf16", nb)
     caches = [(torch.zeros(cfg.cache_shape(), dtype=torch.bfloat16, device=device),
                torch.zeros(cfg.cache_shape(), dtype=torch.bfloat16, device=device))
               for _ in range(L)]
-    budget = 512
-    inputs = [workloads.make_qkv(shape, budget, args.seed, 1000 + l, device=device)
-              for l in range(L)]
-    o = torch.empty((budget, 32, 128), dtype=torch.bfloat16, device=device)
     ws = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    if args.layer == "full":
+        stack = DenseStack(torch, rbkv, cfg, L, max_tokens, device, args.seed)
+    else:
+        stack = AttentionStack(torch, rbkv, cfg, L, max_tokens, device, args.seed)
     stream = torch.cuda.current_stream()
     hs = rbkv._P(stream.cuda_stream)
     torch.cuda.synchronize()
+    return torch, rbkv, workloads, reqs, cfg, caches, ws, stack, stream, hs
 
-    def drive(trace_reqs, comp, record):
+
+class AttentionStack:
+    """Per layer only the library's part of the pass: the KV append and ragged
+    attention (Llama-2-7B attention shape, one K/V cache per layer, one block
+    table shared by all layers), on seeded Q/K/V."""
+
+    def __init__(self, torch, rbkv, cfg, layers, max_tokens, device, seed):
+        import workloads
+        import math as _m
+        shape = workloads.Shape(32, 32, 128, 64, "bf16", 1.0 / _m.sqrt(128.0))
+        self.inputs = [workloads.make_qkv(shape, max_tokens, seed, 1000 + l, device=device)
+                       for l in range(layers)]
+        self.o = torch.empty((max_tokens, 32, 128), dtype=torch.bfloat16, device=device)
+        self.rbkv = rbkv
+
+    def weight_bytes(self):
+        return 0
+
+    def forward(self, p, caches, ws, hs):
+        T = p.num_tokens
+        for l, (q, k, v) in enumerate(self.inputs):
+            kc, vc = caches[l]
+            self.rbkv.kv_append(p, k[:T], v[:T], kc, vc, stream=hs)
+            self.rbkv.ragged_attention(p, q[:T], kc, vc, o=self.o[:T], workspace=ws, stream=hs)
+
+
+PROFILE_TOKENS = (16, 32, 64, 128, 256, 384, 512, 768, 1024, 1536, 2048, 3072, 4096)
+
+
+def measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs, tokens=PROFILE_TOKENS,
+                    reps=10, warm=3):
+    """Pass latency (median of ``reps`` CUDA-event timings) against the pass's
+    token count, for two compositions of the same count: one fresh prompt of T
+    tokens, and min(T, 32) fresh prompts sharing T tokens.  Each pass is
+    composed, run ``warm + reps`` times and rolled back."""
+    out = []
+    for T in tokens:
+        row = {"tokens": int(T)}
+        for kind in ("one_prompt", "many_prompts"):
+            n = 1 if kind == "one_prompt" else min(T, 32)
+            states = [(90_000 + i, T // n + (1 if i < T % n else 0), 0) for i in range(n)]
+            comp = rbkv.Composer(cfg)
+            p = comp.compose(T, T, states)
+            assert p.num_tokens == T
+            for _ in range(warm):
+                stack.forward(p, caches, ws, hs)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for a, b in ev:
+                a.record(stream)
+                stack.forward(p, caches, ws, hs)
+                b.record(stream)
+            torch.cuda.synchronize()
+            row[f"latency_ms_{kind}"] = statistics.median(a.elapsed_time(b) for a, b in ev)
+            comp.rollback(p)
+        row["tokens_per_s"] = T / (row["latency_ms_one_prompt"] / 1e3)
+        out.append(row)
+    return out
+
+
+def run_profile_bench(args, rank, world, local_rank):
+    """Pass latency against token count (paper summary page, idea I1: latency
+    follows the token count, not the number of sequences; idea I2: throughput
+    saturates and is concave), and the largest budget whose interpolated
+    latency stays within ``--latency-bound`` (FastGen guide, "Prompt-Decode
+    Decoupling")."""
+    torch, rbkv, workloads, reqs, cfg, caches, ws, stack, stream, hs = _trace_setup(
+        args, rank, world, local_rank, max(PROFILE_TOKENS))
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    w0 = time.time()
+    prof = measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs)
+    w1 = time.time()
+    clk = clocks.stop(w0, w1)
+    toks = [r["tokens"] for r in prof]
+    lat = [r["latency_ms_one_prompt"] for r in prof]
+    budget = rbkv.budget_for_latency(toks, lat, args.latency_bound)
+    if rank != 0:
+        return
+    best = max(prof, key=lambda r: r["tokens_per_s"])
+    line = {
+        "metric": "pass latency vs tokens",
+        "value": best["tokens_per_s"],
+        "unit": "tokens/s (best over the sweep)",
+        "n_gpus": world,
+        "higher_is_better": True,
+        "dtype": "bf16",
+        "data": "synthetic, random weights",
+        "config": {
+            "workload": f"profile: {args.layers} layers, "
+                        + ("Llama-2-7B-shaped decoder layers (cuBLAS projections, library "
+                           "attention)" if args.layer == "full" else
+                           "library KV append + attention only") + ", fresh prompts",
+            "weights_gb": stack.weight_bytes() / 1e9,
+            "latency_bound_ms": args.latency_bound,
+            "budget_for_bound": budget,
+        },
+        "profile": prof,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_trace_bench(args, rank, world, local_rank):
+    """512 requests from 32 closed-loop clients (prompt lengths round(N(2600,
+    780^2)), output lengths round(N(60, 18^2)), at least 1), composed into
+    passes of ``--budget`` tokens (chunk cap the same, ``--policy`` greedy or
+    equal chunks) until every request has finished.  Each pass runs every
+    layer: the library's KV append and attention alone (``--layer attention``),
+    or whole random-weight decoder layers (``--layer full``).  ``--budget 0``
+    measures the latency profile first and takes the largest budget whose
+    interpolated pass latency is within ``--latency-bound``.  Reports pass
+    tokens per second over the whole trace, the per-pass latency distribution,
+    and the serving metrics of the trace on the GPU timeline (pass end times
+    from CUDA events; the host composes ahead of the GPU): TTFT, pace, token
+    intervals and effective throughput under ``--ttft-sla``/``--pace-sla``."""
+    from ragged_blocked_kv_gb300.serving import TraceRecorder, serving_metrics
+    max_tok = max(max(PROFILE_TOKENS), args.budget)
+    torch, rbkv, workloads, reqs, cfg, caches, ws, stack, stream, hs = _trace_setup(
+        args, rank, world, local_rank, max_tok)
+    L = args.layers
+    budget = args.budget
+    prof = None
+    if budget <= 0:
+        prof = measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs)
+        budget = rbkv.budget_for_latency([r["tokens"] for r in prof],
+                                         [r["latency_ms_one_prompt"] for r in prof],
+                                         args.latency_bound)
+        if budget <= 0:
+            raise SystemExit(f"no budget meets a {args.latency_bound} ms pass latency")
+
+    def drive(trace_reqs, comp, record, rec=None):
         events, tokens = [], []
 
         def compose(b, M, states):
-            p = comp.compose(b, M, states)
-            T = p.num_tokens
-            if T:
+            p = comp.compose(b, M, states, policy=args.policy)
+            if p.num_tokens:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                for l in range(L):
-                    q, k, v = inputs[l]
-                    kc, vc = caches[l]
-                    rbkv.kv_append(p, k[:T], v[:T], kc, vc, stream=hs)
-                    rbkv.ragged_attention(p, q[:T], kc, vc, o=o[:T], workspace=ws, stream=hs)
+                stack.forward(p, caches, ws, hs)
                 e1.record(stream)
                 if record:
                     events.append((e0, e1))
-                    tokens.append(T)
+                    tokens.append(p.num_tokens)
+            elif record:
+                events.append(None)
+                tokens.append(0)
             return p.meta
-        n = workloads.run_trace(trace_reqs, 32, budget, budget, compose, comp.release)
+        n = workloads.run_trace(trace_reqs, 32, budget, budget, compose, comp.release,
+                                on_pass=rec.on_pass if rec else None)
         return n, events, tokens
 
     # warm-up: a short trace of the same shape on its own composer
@@ -568,28 +760,38 @@ def run_trace_bench(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.5)
     comp = rbkv.Composer(cfg)
+    rec = TraceRecorder()
     launches0 = rbkv.kernel_launches()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     wall_t0 = time.time()
     t0.record(stream)
-    npass, events, tokens = drive(reqs, comp, True)
+    npass, events, tokens = drive(reqs, comp, True, rec)
     t1.record(stream)
     torch.cuda.synchronize()
     wall_t1 = time.time()
     clk = clocks.stop(wall_t0, wall_t1)
     launches = rbkv.kernel_launches() - launches0
     total_ms = t0.elapsed_time(t1)
-    lat = sorted(a.elapsed_time(b) for a, b in events)
+    lat = sorted(e[0].elapsed_time(e[1]) for e in events if e is not None)
+    ends, last = [], 0.0
+    for e in events:
+        last = t0.elapsed_time(e[1]) if e is not None else last
+        ends.append(last)
+    serving = serving_metrics(rec, ends, args.ttft_sla, args.pace_sla)
 
     def pct(x):
         return lat[min(len(lat) - 1, int(round(x / 100.0 * (len(lat) - 1))))]
 
-    (total_ms,), (ntok,) = over_ranks([total_ms], [sum(tokens)], world, device)
+    (total_ms,), (ntok,) = over_ranks([total_ms], [sum(tokens)], world, device=f"cuda:{local_rank}")
     if rank != 0:
         return
+    what = ("Llama-2-7B-shaped decoder layers (random weights, cuBLAS projections, library "
+            "KV append + attention)" if args.layer == "full" else
+            "library KV append + attention of 32q/32kv heads, head_dim 128, block 64")
     line = {
-        "metric": "ragged SplitFuse attention pass tokens/s",
+        "metric": ("SplitFuse forward pass tokens/s" if args.layer == "full"
+                   else "ragged SplitFuse attention pass tokens/s"),
         "value": ntok / (total_ms / 1e3),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -600,22 +802,28 @@ def run_trace_bench(args, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic",
+        "data": "synthetic" + (", random weights" if args.layer == "full" else ""),
         "config": {
-            "workload": f"trace: {len(reqs)} requests, 32 closed-loop clients, budget 512, "
-                        f"chunk cap 512, {L} layers of 32q/32kv heads, head_dim 128, block 64",
+            "workload": f"trace: {len(reqs)} requests, 32 closed-loop clients, budget {budget}, "
+                        f"chunk cap {budget}, {args.policy} chunks, {L} layers of {what}",
             "passes": npass,
             "pass_tokens": int(ntok),
             "expected_tokens": sum(r.prompt_len + r.output_len - 1 for r in reqs),
             "latency_ms": {"p50": pct(50), "p90": pct(90), "p99": pct(99), "max": lat[-1],
                            "mean": sum(lat) / len(lat)},
             "kv_cache_gb": 2 * L * caches[0][0].numel() * 2 / 1e9,
+            "weights_gb": stack.weight_bytes() / 1e9,
             "l2": "KV of every layer exceeds L2; no flush",
             "warmup": "a separate 64-request trace on its own composer",
+            "budget_from": (f"latency profile, bound {args.latency_bound} ms" if prof
+                            else "--budget"),
         },
+        "serving": serving,
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if prof:
+        line["profile"] = prof
     print(json.dumps(line), flush=True)
 
 
@@ -799,6 +1007,11 @@ def run_reference(args, rank):
     if rank != 0:
         return
     import workloads
+    if args.workload == "profile" or args.layer == "full":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle covers the "
+                          "attention pass only, not the dense layers or a latency profile"}),
+              flush=True)
+        return
     res = oracle_measure(args.workload, args.seed, args.steps, args.warmup)
     if args.workload == "trace":
         scn = workloads.Scenario("trace", workloads.Shape(32, 32, 128, 64, "bf16", 1.0), 512,
@@ -856,6 +1069,8 @@ def main():
     try:
         if args.workload == "trace":
             run_trace_bench(args, rank, world, local_rank)
+        elif args.workload == "profile":
+            run_profile_bench(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -284,6 +284,84 @@ rbkv_status rbkv_ragged_attention_noalloc(rbkv_pass* p, const void* q, const voi
  * skipped that access) or RBKV_ERR_TIMEOUT (a bounded wait gave up). */
 rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream);
 
+/* ---- frames: one fixed launch sequence for every pass (CUDA graphs) ---------
+ *
+ * Dynamic SplitFuse keeps every forward pass at about the same size (paper
+ * summary page, Summary and idea I3; InfoQ note: "a consistent forward
+ * size"), so a serving loop can record the launches of one pass once, as a
+ * CUDA graph, and replay them for every later pass.  A frame makes that
+ * possible: it holds a pass's metadata at fixed device addresses, inside
+ * capacities fixed when it is created, and its kernel launches are sized by
+ * those capacities (the loaded pass's own counts are read on the device).
+ * The launches of rbkv_frame_kv_append and rbkv_frame_attention therefore have
+ * the same arguments for every pass loaded into the frame; they allocate
+ * nothing, wait on no event and never synchronise, so they may be captured.
+ * Results are identical to rbkv_kv_append + rbkv_ragged_attention on the same
+ * pass (same plan, same kernels).
+ *
+ * Protocol (all on one stream): rbkv_frame_load(pass) writes the pass's
+ * metadata into the frame (host-to-device copies on the stream); then the
+ * frame's append and attention launches, directly or replayed from a graph;
+ * then the next rbkv_frame_load.  Only bf16 shapes whose decode and chunk rows
+ * both take the fast kernels are supported (RBKV_ERR_UNSUPPORTED otherwise). */
+
+typedef struct rbkv_frame rbkv_frame;
+
+/* Capacities of a frame.  0 in any field but max_tokens takes the default:
+ *   max_seqs          max_tokens
+ *   max_blocks        the pool's num_blocks
+ *   max_decode_items  4 x SMs + max_seqs x num_heads_kv (the automatic split
+ *                     plan never needs more)
+ *   max_chunk_tiles   ceil(max_tokens / 128) + 8, at least ceil(SMs / num_heads_q)
+ *   max_combine_rows  max_tokens x num_heads_kv
+ *   max_parts         max_decode_items + max_tokens x num_heads_kv x
+ *                     max(1, SMs / num_heads_q) */
+typedef struct {
+  int32_t max_tokens;       /* rows of Q/K/V/O the frame's launches address */
+  int32_t max_seqs;
+  int32_t max_blocks;       /* block-table entries of one pass */
+  int32_t max_decode_items;
+  int32_t max_chunk_tiles;
+  int32_t max_combine_rows;
+  int32_t max_parts;        /* partial-output slots of the workspace */
+} rbkv_frame_caps;
+
+/* Create a frame on the current device for passes of `cfg` (device memory for
+ * the metadata and pinned host staging; the filled-in capacities are returned
+ * in *caps_out when it is not NULL).  Errors: RBKV_ERR_INVALID (bad config or
+ * max_tokens < 1), RBKV_ERR_UNSUPPORTED (shape off the fast kernels),
+ * RBKV_ERR_CUDA. */
+rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* caps,
+                              rbkv_frame** out, rbkv_frame_caps* caps_out);
+void rbkv_frame_destroy(rbkv_frame* f);
+
+/* Plan the pass for the frame's device and copy its metadata into the frame
+ * on `stream` (from pinned staging; the host waits only when every staging
+ * buffer is still in flight).  The pass must have the frame's config and fit
+ * its capacities: RBKV_ERR_WORKSPACE names the capacity it exceeds (nothing is
+ * changed; the plain entry points still serve that pass).  An empty pass is
+ * loaded as zero counts. */
+rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream);
+
+/* rbkv_kv_append for the pass loaded last: k_new/v_new are [max_tokens][H_kv][D]
+ * (rows past the pass's token count are not read). */
+rbkv_status rbkv_frame_kv_append(rbkv_frame* f, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, rbkv_stream stream);
+
+/* Workspace bytes rbkv_frame_attention needs (for max_parts partial slots). */
+size_t rbkv_frame_workspace_bytes(const rbkv_frame* f);
+
+/* rbkv_ragged_attention for the pass loaded last: q and o are [max_tokens][H_q][D]
+ * (rows past the pass's token count are neither read as queries nor written);
+ * workspace as rbkv_frame_workspace_bytes, 256-byte aligned. */
+rbkv_status rbkv_frame_attention(rbkv_frame* f, const void* q, const void* k_cache,
+                                 const void* v_cache, void* o, void* workspace,
+                                 size_t workspace_bytes, rbkv_stream stream);
+
+/* As rbkv_pass_device_status, for the frame's status word (sticky across the
+ * passes loaded since it was last read). */
+rbkv_status rbkv_frame_device_status(rbkv_frame* f, rbkv_stream stream);
+
 /* ---- measurement ----------------------------------------------------------- */
 
 /* Kernel kinds for rbkv_profile_read. */

@@ -63,6 +63,12 @@ class _PlanInfo(C.Structure):
         "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk")]
 
 
+class _FrameCaps(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "max_tokens", "max_seqs", "max_blocks", "max_decode_items", "max_chunk_tiles",
+        "max_combine_rows", "max_parts")]
+
+
 # Every symbol include/rbkv.h declares, with (restype, argtypes).
 _P = C.c_void_p
 SIGNATURES = {
@@ -91,6 +97,14 @@ SIGNATURES = {
     "rbkv_ragged_attention": (C.c_int, [_P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "rbkv_pass_device_status": (C.c_int, [_P, _P]),
     "rbkv_ragged_attention_noalloc": (C.c_int, [_P, _P, _P, _P, _P, _P]),
+    "rbkv_frame_create": (C.c_int, [C.POINTER(_Config), C.POINTER(_FrameCaps), C.POINTER(_P),
+                                    C.POINTER(_FrameCaps)]),
+    "rbkv_frame_destroy": (None, [_P]),
+    "rbkv_frame_load": (C.c_int, [_P, _P, _P]),
+    "rbkv_frame_kv_append": (C.c_int, [_P, _P, _P, _P, _P, _P]),
+    "rbkv_frame_workspace_bytes": (C.c_size_t, [_P]),
+    "rbkv_frame_attention": (C.c_int, [_P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "rbkv_frame_device_status": (C.c_int, [_P, _P]),
     "rbkv_kernel_launches": (C.c_int64, []),
     "rbkv_profile_enable": (None, [C.c_int32]),
     "rbkv_profile_read": (C.c_int, [C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
@@ -372,6 +386,66 @@ def ragged_attention_noalloc(p: Pass, q, k_cache, v_cache, o, stream=None):
     return o
 
 
+class Frame:
+    """Fixed device home for one pass at a time, so that the append and
+    attention launches are identical for every pass (capturable once as a CUDA
+    graph and replayed).  ``load(pass)`` before each replay, on the same
+    stream.  Q/K/V/O buffers have ``max_tokens`` rows; rows past the loaded
+    pass's tokens are ignored."""
+
+    def __init__(self, config: Config, max_tokens: int, **caps):
+        want = _FrameCaps(max_tokens=int(max_tokens), **{k: int(v) for k, v in caps.items()})
+        got = _FrameCaps()
+        h = _P()
+        _check(lib().rbkv_frame_create(C.byref(config._c()), C.byref(want), C.byref(h),
+                                       C.byref(got)))
+        self._h = h
+        self.config = config
+        self.caps = {n: getattr(got, n) for n, _ in _FrameCaps._fields_}
+        self.max_tokens = self.caps["max_tokens"]
+
+    def workspace_bytes(self) -> int:
+        return int(lib().rbkv_frame_workspace_bytes(self._h))
+
+    def load(self, p: "Pass", stream=None) -> None:
+        _check(lib().rbkv_frame_load(self._h, p._h, _stream(stream)))
+
+    def kv_append(self, k_new, v_new, k_cache, v_cache, stream=None) -> None:
+        c = self.config
+        dt = c.torch_dtype
+        row = (self.max_tokens, c.num_heads_kv, c.head_dim)
+        _check(lib().rbkv_frame_kv_append(self._h, _dev_ptr(k_new, "k_new", dt, row),
+                                          _dev_ptr(v_new, "v_new", dt, row),
+                                          _dev_ptr(k_cache, "k_cache", dt, c.cache_shape()),
+                                          _dev_ptr(v_cache, "v_cache", dt, c.cache_shape()),
+                                          _stream(stream)))
+
+    def attention(self, q, k_cache, v_cache, o, workspace, stream=None) -> None:
+        c = self.config
+        dt = c.torch_dtype
+        qshape = (self.max_tokens, c.num_heads_q, c.head_dim)
+        _check(lib().rbkv_frame_attention(
+            self._h, _dev_ptr(q, "q", dt, qshape),
+            _dev_ptr(k_cache, "k_cache", dt, c.cache_shape()),
+            _dev_ptr(v_cache, "v_cache", dt, c.cache_shape()), _dev_ptr(o, "o", dt, qshape),
+            _P(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+            _stream(stream)))
+
+    def device_status(self, stream=None) -> None:
+        _check(lib().rbkv_frame_device_status(self._h, _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().rbkv_frame_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def budget_for_latency(tokens, latency, bound: float) -> int:
     """Largest token count whose latency, interpolated from a measured
     (tokens, latency) profile, stays within ``bound`` (0 if none)."""
@@ -407,5 +481,5 @@ def profile_read() -> dict:
     return out
 
 
-__all__ = ["budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+__all__ = ["Frame", "budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
            "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

@@ -176,6 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int)blockIdx.x >= pass_count(dp, kCountChunk, dp.n_chunk)) {
+    // a frame's capacity-sized grid: no tile here.  Still wait for the
+    // predecessor, so that this grid's completion covers the cache append
+    ptx::pdl_wait_previous();
+    return;
+  }
   const ChunkTile tile = dp.chunk_tiles[blockIdx.x];
   const int h = blockIdx.y;
   const int kvh = h / shp.g;

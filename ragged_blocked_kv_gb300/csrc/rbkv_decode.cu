@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::pdl_launch_dependents();
   Shared sm = carve(smem_raw);
   volatile int& abort_flag = *sm.abort_flag;
+  const int n_decode = pass_count(dp, kCountDecode, dp.n_decode);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = shp.g, B = shp.B, H_kv = shp.H_kv;
   if (ptx::smem_u32(smem_raw) & 1023) {
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tmap_v);
       uint32_t idx = 0;
       const int box_rows = B < kKeys ? B : kKeys;
-      for (int item = blockIdx.x; item < dp.n_decode && !abort_flag; item += gridDim.x) {
+      for (int item = blockIdx.x; item < n_decode && !abort_flag; item += gridDim.x) {
         const WorkItem it = dp.decode_items[item];
         const int32_t* table = dp.block_ids + it.table_off;
         const int nt = tiles_of(it);
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t tile_base = 0;
   const uint32_t stages_u32 = ptx::smem_u32(sm.stages);
 
-  for (int item = blockIdx.x; item < dp.n_decode; item += gridDim.x) {
+  for (int item = blockIdx.x; item < n_decode; item += gridDim.x) {
     const WorkItem it = dp.decode_items[item];
     const int nt = tiles_of(it);
 

@@ -838,14 +838,16 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
   return RBKV_OK;
 }
 
-rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream) {
-  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
-  if (!p->dev) return RBKV_OK;
-  cudaStream_t st = (cudaStream_t)stream;
+}  // extern "C"
+
+namespace {
+
+// Wait for `st`, then read and clear the four device status words at `dev`.
+rbkv_status read_device_status(void* dev, cudaStream_t st) {
   int32_t words[4] = {0, 0, 0, 0};
   cudaError_t e = cudaStreamSynchronize(st);
-  if (e == cudaSuccess) e = cudaMemcpy(words, p->dev, sizeof(words), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(p->dev, 0, sizeof(words));
+  if (e == cudaSuccess) e = cudaMemcpy(words, dev, sizeof(words), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(dev, 0, sizeof(words));
   if (e != cudaSuccess) return cuda_fail(e, "device status read");
   const int32_t word = words[0];
   if (word == kDevBounds) return fail(RBKV_ERR_DEVICE_BOUNDS, "a kernel met an out-of-range block id");
@@ -856,6 +858,257 @@ rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream) {
                                       std::to_string(words[3] >> 16) + ")");
   if (word != 0) return fail(RBKV_ERR_CUDA, "unknown device status " + std::to_string(word));
   return RBKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (!p->dev) return RBKV_OK;
+  return read_device_status(p->dev, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------
+// frames
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+struct rbkv_frame {
+  rbkv_config cfg{};
+  rbkv_frame_caps caps{};
+  int device = -1;
+  int sms = 0;
+  int32_t* dev = nullptr;   // device words: status[4] | counts[8] | sections
+  size_t words = 0;
+  size_t o_slot = 0, o_blocks = 0, o_dec = 0, o_chunk = 0, o_comb = 0;
+  static constexpr int kStages = 4;
+  int32_t* host[kStages] = {};   // pinned staging, same layout
+  cudaEvent_t ev[kStages] = {};
+  int next = 0;
+  DevPass dp{};
+  ~rbkv_frame() {
+    for (int i = 0; i < kStages; ++i) {
+      if (ev[i]) { cudaEventSynchronize(ev[i]); cudaEventDestroy(ev[i]); }
+      if (host[i]) cudaFreeHost(host[i]);
+    }
+    if (dev) cudaFree(dev);
+  }
+};
+
+namespace {
+
+bool same_config(const rbkv_config& a, const rbkv_config& b) {
+  return a.num_heads_q == b.num_heads_q && a.num_heads_kv == b.num_heads_kv &&
+         a.head_dim == b.head_dim && a.block_size == b.block_size && a.dtype == b.dtype &&
+         a.num_blocks == b.num_blocks;
+}
+
+size_t align4(size_t w) { return (w + 3) / 4 * 4; }
+
+}  // namespace
+
+extern "C" {
+
+rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* caps,
+                              rbkv_frame** out, rbkv_frame_caps* caps_out) {
+  if (!out || !caps) return fail(RBKV_ERR_INVALID, "caps or out is NULL");
+  *out = nullptr;
+  rbkv_status rs = check_config(cfg);
+  if (rs != RBKV_OK) return rs;
+  const ShapeInfo s = shape_of(*cfg);
+  if (cfg->dtype != RBKV_BF16 || !decode_fast_supported(s) || !chunk_fast_supported(s))
+    return fail(RBKV_ERR_UNSUPPORTED, "frames need a shape served by the tensor-core kernels");
+  rbkv_frame_caps c = *caps;
+  if (c.max_tokens < 1) return fail(RBKV_ERR_INVALID, "max_tokens must be >= 1");
+  if (c.max_seqs < 0 || c.max_blocks < 0 || c.max_decode_items < 0 || c.max_chunk_tiles < 0 ||
+      c.max_combine_rows < 0 || c.max_parts < 0)
+    return fail(RBKV_ERR_INVALID, "capacities must be >= 0");
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  const int64_t slots = (int64_t)sms * kDecodeCtasPerSm;
+  auto clamp = [](int64_t v) { return (int32_t)std::min<int64_t>(v, 1 << 28); };
+  if (!c.max_seqs) c.max_seqs = c.max_tokens;
+  if (!c.max_blocks) c.max_blocks = std::max(1, cfg->num_blocks);
+  if (!c.max_decode_items)
+    c.max_decode_items = clamp(4 * slots + (int64_t)c.max_seqs * s.H_kv);
+  if (!c.max_chunk_tiles)
+    c.max_chunk_tiles = clamp(std::max<int64_t>(ceil_div(c.max_tokens, kChunkTileRows) + 8,
+                                                ceil_div(sms, s.H_q)));
+  if (!c.max_combine_rows) c.max_combine_rows = clamp((int64_t)c.max_tokens * s.H_kv);
+  if (!c.max_parts)
+    c.max_parts = clamp((int64_t)c.max_decode_items +
+                        (int64_t)c.max_tokens * s.H_kv * std::max(1, sms / s.H_q));
+  std::unique_ptr<rbkv_frame> f(new rbkv_frame);
+  f->cfg = *cfg;
+  f->caps = c;
+  f->device = dev;
+  f->sms = sms;
+  size_t w = 12;  // status words, counts
+  f->o_slot = w;   w = align4(w + (size_t)c.max_tokens);
+  f->o_blocks = w; w = align4(w + (size_t)c.max_blocks);
+  f->o_dec = w;    w = align4(w + (size_t)c.max_decode_items * (sizeof(WorkItem) / 4));
+  f->o_chunk = w;  w = align4(w + (size_t)c.max_chunk_tiles * (sizeof(ChunkTile) / 4));
+  f->o_comb = w;   w = align4(w + (size_t)c.max_combine_rows * (sizeof(CombineRow) / 4));
+  f->words = w;
+  e = cudaMalloc((void**)&f->dev, w * 4);
+  if (e == cudaSuccess) e = cudaMemset(f->dev, 0, w * 4);
+  for (int i = 0; e == cudaSuccess && i < rbkv_frame::kStages; ++i) {
+    e = cudaHostAlloc((void**)&f->host[i], w * 4, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f->ev[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "frame allocation");
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "frame allocation");
+  DevPass& dp = f->dp;
+  int32_t* base = f->dev;
+  dp.status = base;
+  dp.counts = base + 4;
+  dp.slot = base + f->o_slot;
+  dp.block_ids = base + f->o_blocks;
+  dp.decode_items = (const WorkItem*)(base + f->o_dec);
+  dp.generic_items = nullptr;
+  dp.chunk_tiles = (const ChunkTile*)(base + f->o_chunk);
+  dp.combine_rows = (const CombineRow*)(base + f->o_comb);
+  dp.num_tokens = c.max_tokens;
+  dp.n_decode = c.max_decode_items;
+  dp.n_generic = 0;
+  dp.n_chunk = c.max_chunk_tiles;
+  dp.n_combine = c.max_combine_rows;
+  dp.n_parts = c.max_parts;
+  dp.num_blocks = cfg->num_blocks;
+  dp.decode_grid = (int32_t)std::min<int64_t>(slots, c.max_decode_items);
+  if (caps_out) *caps_out = c;
+  *out = f.release();
+  return RBKV_OK;
+}
+
+void rbkv_frame_destroy(rbkv_frame* f) { delete f; }
+
+rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
+  if (!f || !p) return fail(RBKV_ERR_INVALID, "frame or pass is NULL");
+  if (!same_config(f->cfg, p->cfg)) return fail(RBKV_ERR_INVALID, "pass and frame configs differ");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != f->device) return fail(RBKV_ERR_INVALID, "frame belongs to another device");
+  const rbkv_frame_caps& c = f->caps;
+  int32_t counts[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const Plan* pl = nullptr;
+  if (!p->slot.empty()) {
+    rbkv_status rs = ensure_plan(p);
+    if (rs != RBKV_OK) return rs;
+    pl = &p->plan;
+    auto over = [](const char* what, size_t n, int32_t cap) {
+      return fail(RBKV_ERR_WORKSPACE, std::string("pass exceeds the frame's ") + what + " (" +
+                                          std::to_string(n) + " > " + std::to_string(cap) + ")");
+    };
+    if (p->slot.size() > (size_t)c.max_tokens) return over("max_tokens", p->slot.size(), c.max_tokens);
+    if (p->seq_ids.size() > (size_t)c.max_seqs) return over("max_seqs", p->seq_ids.size(), c.max_seqs);
+    if (p->block_ids.size() > (size_t)c.max_blocks)
+      return over("max_blocks", p->block_ids.size(), c.max_blocks);
+    if (pl->decode.size() > (size_t)c.max_decode_items)
+      return over("max_decode_items", pl->decode.size(), c.max_decode_items);
+    if (pl->chunk.size() > (size_t)c.max_chunk_tiles)
+      return over("max_chunk_tiles", pl->chunk.size(), c.max_chunk_tiles);
+    if (pl->combine.size() > (size_t)c.max_combine_rows)
+      return over("max_combine_rows", pl->combine.size(), c.max_combine_rows);
+    if (pl->n_parts > c.max_parts) return over("max_parts", (size_t)pl->n_parts, c.max_parts);
+    if (!pl->generic.empty()) return fail(RBKV_ERR_UNSUPPORTED, "pass has CUDA-core work items");
+    counts[kCountTokens] = (int32_t)p->slot.size();
+    counts[kCountDecode] = (int32_t)pl->decode.size();
+    counts[kCountChunk] = (int32_t)pl->chunk.size();
+    counts[kCountCombine] = (int32_t)pl->combine.size();
+  }
+  const int k = f->next;
+  f->next = (f->next + 1) % rbkv_frame::kStages;
+  e = cudaEventSynchronize(f->ev[k]);  // the last copy out of this staging buffer
+  if (e != cudaSuccess) return cuda_fail(e, "frame staging");
+  int32_t* h = f->host[k];
+  cudaStream_t st = (cudaStream_t)stream;
+  std::memcpy(h + 4, counts, sizeof(counts));
+  size_t head_end = 12;
+  if (pl) {
+    std::memcpy(h + f->o_slot, p->slot.data(), p->slot.size() * 4);
+    std::memcpy(h + f->o_blocks, p->block_ids.data(), p->block_ids.size() * 4);
+    head_end = f->o_blocks + p->block_ids.size();
+  }
+  // counts, slots and block tables in one copy (not the status words), then
+  // the used part of each work list
+  e = cudaMemcpyAsync(f->dev + 4, h + 4, (head_end - 4) * 4, cudaMemcpyHostToDevice, st);
+  auto section = [&](size_t off, const void* src, size_t bytes) {
+    if (e != cudaSuccess || bytes == 0) return;
+    std::memcpy(h + off, src, bytes);
+    e = cudaMemcpyAsync(f->dev + off, h + off, bytes, cudaMemcpyHostToDevice, st);
+  };
+  if (pl) {
+    section(f->o_dec, pl->decode.data(), pl->decode.size() * sizeof(WorkItem));
+    section(f->o_chunk, pl->chunk.data(), pl->chunk.size() * sizeof(ChunkTile));
+    section(f->o_comb, pl->combine.data(), pl->combine.size() * sizeof(CombineRow));
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(f->ev[k], st);
+  if (e != cudaSuccess) return cuda_fail(e, "frame upload");
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_frame_kv_append(rbkv_frame* f, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, rbkv_stream stream) {
+  if (!f) return fail(RBKV_ERR_INVALID, "frame is NULL");
+  if (!k_new || !v_new || !k_cache || !v_cache) return fail(RBKV_ERR_INVALID, "NULL tensor");
+  cudaStream_t st = (cudaStream_t)stream;
+  const ShapeInfo s = shape_of(f->cfg);
+  cudaError_t e = launch_counted(RBKV_KERNEL_KV_APPEND, st, [&] {
+    return launch_kv_append(f->dp, s, k_new, v_new, k_cache, v_cache, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return RBKV_OK;
+}
+
+size_t rbkv_frame_workspace_bytes(const rbkv_frame* f) {
+  if (!f) return 0;
+  const ShapeInfo s = shape_of(f->cfg);
+  return partial_o_bytes(f->caps.max_parts, s) + partial_lse_bytes(f->caps.max_parts, s);
+}
+
+rbkv_status rbkv_frame_attention(rbkv_frame* f, const void* q, const void* k_cache,
+                                 const void* v_cache, void* o, void* workspace,
+                                 size_t workspace_bytes, rbkv_stream stream) {
+  if (!f) return fail(RBKV_ERR_INVALID, "frame is NULL");
+  if (!q || !k_cache || !v_cache || !o) return fail(RBKV_ERR_INVALID, "NULL tensor");
+  const size_t need = rbkv_frame_workspace_bytes(f);
+  if (!workspace || workspace_bytes < need)
+    return fail(RBKV_ERR_WORKSPACE, "frame workspace needs " + std::to_string(need) + " bytes");
+  if ((uintptr_t)workspace % 256) return fail(RBKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const ShapeInfo s = shape_of(f->cfg);
+  float* part_o = (float*)workspace;
+  float* part_lse = (float*)((char*)workspace + partial_o_bytes(f->caps.max_parts, s));
+  const DevPass& dp = f->dp;
+  // the same launch sequence as rbkv_ragged_attention with every kernel
+  // present: the chunk grid always precedes the decode grid (its CTAs without
+  // a tile wait for the append and leave)
+  const bool overlap = !g_prof.on;
+  cudaError_t e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
+    return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap);
+  });
+  if (e == cudaSuccess)
+    e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
+      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
+                                false);
+    });
+  if (e == cudaSuccess)
+    e = launch_counted(RBKV_KERNEL_COMBINE, st,
+                       [&] { return launch_combine(dp, s, part_o, part_lse, o, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_frame_device_status(rbkv_frame* f, rbkv_stream stream) {
+  if (!f) return fail(RBKV_ERR_INVALID, "frame is NULL");
+  return read_device_status(f->dev, (cudaStream_t)stream);
 }
 
 int64_t rbkv_kernel_launches(void) { return g_launches.load(); }

@@ -72,7 +72,21 @@ struct DevPass {
   int32_t n_parts;
   int32_t num_blocks;
   int32_t decode_grid;             // CTAs of the persistent decode launch
+  // A frame (rbkv_frame_*): the launches are sized by the frame's capacities
+  // (the counts above), and the loaded pass's own counts are read from this
+  // device array {num_tokens, n_decode, n_generic, n_chunk, n_combine}.
+  // Null for a plain pass.
+  const int32_t* counts;
 };
+
+enum { kCountTokens = 0, kCountDecode = 1, kCountGeneric = 2, kCountChunk = 3, kCountCombine = 4 };
+
+#ifdef __CUDACC__
+// The live count `i` of the pass a kernel serves.
+__device__ __forceinline__ int32_t pass_count(const DevPass& dp, int i, int32_t fixed) {
+  return dp.counts ? dp.counts[i] : fixed;
+}
+#endif
 
 struct ShapeInfo {
   int32_t H_q, H_kv, D, B, g;

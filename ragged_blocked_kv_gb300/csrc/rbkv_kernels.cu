@@ -12,6 +12,8 @@
 //   path - partial outputs O_i with log-sum-exps L_i merge as
 //   O = sum_i 2^(L_i - M) O_i / sum_i 2^(L_i - M), M = max_i L_i
 //   (log-sum-exps are kept in base 2 inside the library).
+#include <algorithm>
+
 #include "rbkv_internal.h"
 
 #include <cuda_bf16.h>
@@ -56,7 +58,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
   const int half = lane >> 4, hl = lane & 15;
   const uint4* __restrict__ src = half ? v_new : k_new;
   uint4* __restrict__ dst = half ? v_cache : k_cache;
-  const uint32_t rows = (uint32_t)dp.num_tokens * (uint32_t)H_kv;
+  const uint32_t rows = (uint32_t)pass_count(dp, kCountTokens, dp.num_tokens) * (uint32_t)H_kv;
   for (uint32_t r = blockIdx.x * kAppendWarps + warp; r < rows; r += gridDim.x * kAppendWarps) {
     const uint32_t t = r / (uint32_t)H_kv;
     const uint32_t h = r - t * (uint32_t)H_kv;
@@ -170,9 +172,10 @@ __global__ void __launch_bounds__(128)
   // launched to overlap the attention kernels' tail: the partials are only
   // complete once they have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  if (w >= (int64_t)dp.n_combine * s.g) return;
+  const int64_t n_warps = (int64_t)pass_count(dp, kCountCombine, dp.n_combine) * s.g;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < n_warps;
+       w += (int64_t)gridDim.x * blockDim.x / 32) {
   const CombineRow cr = dp.combine_rows[w / s.g];
   const int gi = (int)(w % s.g);
   const int D = s.D, dpl = D / 32;
@@ -197,6 +200,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int k = 0; k < kMaxDPerLane; ++k)
     if (k < dpl) orow[lane + 32 * k] = from_f<T>(acc[k] * inv);
+  }
 }
 
 int num_sms_current() {
@@ -245,7 +249,10 @@ cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* p
   if (s.D % 32) return cudaErrorNotSupported;
   const int64_t warps = (int64_t)dp.n_combine * s.g;
   if (warps == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((warps * 32 + 127) / 128);
+  // one warp per (row, query head); a frame's capacity-sized launch strides
+  int64_t nb = (warps * 32 + 127) / 128;
+  if (dp.counts) nb = std::min<int64_t>(nb, (int64_t)num_sms_current() * 8);
+  const unsigned blocks = (unsigned)nb;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
   cfg.blockDim = dim3(128);
