@@ -66,6 +66,9 @@ def parse_args():
                     help="tokens per pass (trace workload); 0 = from the latency profile")
     ap.add_argument("--latency-bound", type=float, default=30.0,
                     help="pass latency bound in ms for --budget 0 and the profile workload")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="launch every pass eagerly instead of replaying a CUDA graph "
+                         "(trace and profile workloads)")
     ap.add_argument("--ttft-sla", type=float, default=1000.0, help="TTFT bound, ms")
     ap.add_argument("--pace-sla", type=float, default=25.0,
                     help="bound on a request's mean interval between tokens, ms")
@@ -547,25 +550,40 @@ class DenseStack:
     def weight_bytes(self):
         return sum(t.numel() * t.element_size() for l in self.layers for t in l.values())
 
-    def forward(self, p, caches, ws, hs):
-        torch, rbkv = self.torch, self.rbkv
+    def _layers(self, T, caches, attend):
+        torch = self.torch
         F = torch.nn.functional
-        T = p.num_tokens
         hq, d = self.cfg.num_heads_q, self.cfg.head_dim
         x = self.x0[:T]
         o = self.o[:T]
         for l, W in enumerate(self.layers):
-            kc, vc = caches[l]
             h = F.rms_norm(x, (self.HIDDEN,), W["n1"], 1e-5)
             qkv = torch.matmul(h, W["qkv"])                 # [3][T][hidden], each contiguous
             q, k, v = (qkv[i].view(T, hq, d) for i in range(3))
-            rbkv.kv_append(p, k, v, kc, vc, stream=hs)
-            rbkv.ragged_attention(p, q, kc, vc, o=o, workspace=ws, stream=hs)
+            attend(l, q, k, v, o)
             x = x + torch.matmul(o.view(T, self.HIDDEN), W["o"])
             h = F.rms_norm(x, (self.HIDDEN,), W["n2"], 1e-5)
             gu = torch.matmul(h, W["gu"])
             x = x + torch.matmul(F.silu(gu[0]) * gu[1], W["down"])
         return x
+
+    def forward(self, p, caches, ws, hs):
+        rbkv = self.rbkv
+
+        def attend(l, q, k, v, o):
+            kc, vc = caches[l]
+            rbkv.kv_append(p, k, v, kc, vc, stream=hs)
+            rbkv.ragged_attention(p, q, kc, vc, o=o, workspace=ws, stream=hs)
+        return self._layers(p.num_tokens, caches, attend)
+
+    def forward_frame(self, frame, caches, ws):
+        """The pass loaded in ``frame``, on frame-sized buffers and the current
+        stream (capturable)."""
+        def attend(l, q, k, v, o):
+            kc, vc = caches[l]
+            frame.kv_append(k, v, kc, vc)
+            frame.attention(q, kc, vc, o, ws)
+        return self._layers(frame.max_tokens, caches, attend)
 
 
 def _trace_setup(args, rank, world, local_rank, max_tokens):
@@ -622,16 +640,67 @@ class AttentionStack:
             self.rbkv.kv_append(p, k[:T], v[:T], kc, vc, stream=hs)
             self.rbkv.ragged_attention(p, q[:T], kc, vc, o=self.o[:T], workspace=ws, stream=hs)
 
+    def forward_frame(self, frame, caches, ws):
+        T = frame.max_tokens
+        for l, (q, k, v) in enumerate(self.inputs):
+            kc, vc = caches[l]
+            frame.kv_append(k[:T], v[:T], kc, vc)
+            frame.attention(q[:T], kc, vc, self.o[:T], ws)
+
+
+class GraphRunner:
+    """Runs passes of a stack through a frame and one CUDA graph: the first
+    pass runs eagerly (warming cuBLAS and the library), then the stack's
+    launches are captured once; every later pass is a metadata load plus a
+    replay.  A pass the frame cannot hold runs eagerly through the plain entry
+    points."""
+
+    def __init__(self, torch, rbkv, cfg, stack, caches, ws, hs, max_tokens, **caps):
+        self.torch, self.rbkv, self.stack, self.caches, self.ws, self.hs = (
+            torch, rbkv, stack, caches, ws, hs)
+        self.frame = rbkv.Frame(cfg, max_tokens, **caps)
+        self.fws = torch.empty(max(256, self.frame.workspace_bytes()), dtype=torch.uint8,
+                               device=ws.device)
+        self.graph = None
+        self.per_replay = 0
+        self.replays = 0
+        self.eager = 0
+
+    def run(self, p):
+        torch, rbkv = self.torch, self.rbkv
+        try:
+            self.frame.load(p)
+        except rbkv.RbkvError:
+            self.eager += 1
+            self.stack.forward(p, self.caches, self.ws, self.hs)
+            return
+        if self.graph is None:
+            self.stack.forward_frame(self.frame, self.caches, self.fws)
+            torch.cuda.synchronize()
+            n0 = rbkv.kernel_launches()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                self.stack.forward_frame(self.frame, self.caches, self.fws)
+            self.per_replay = rbkv.kernel_launches() - n0
+            return
+        self.graph.replay()
+        self.replays += 1
+
+    def close(self):
+        self.graph = None
+        self.frame.close()
+
 
 PROFILE_TOKENS = (16, 32, 64, 128, 256, 384, 512, 768, 1024, 1536, 2048, 3072, 4096)
 
 
 def measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs, tokens=PROFILE_TOKENS,
-                    reps=10, warm=3):
+                    reps=10, warm=3, graph=True):
     """Pass latency (median of ``reps`` CUDA-event timings) against the pass's
     token count, for two compositions of the same count: one fresh prompt of T
     tokens, and min(T, 32) fresh prompts sharing T tokens.  Each pass is
-    composed, run ``warm + reps`` times and rolled back."""
+    composed, run ``warm + reps`` times (replays of one captured graph when
+    ``graph``) and rolled back."""
     out = []
     for T in tokens:
         row = {"tokens": int(T)}
@@ -641,16 +710,27 @@ def measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs, tokens=PROF
             comp = rbkv.Composer(cfg)
             p = comp.compose(T, T, states)
             assert p.num_tokens == T
+            if graph:
+                # room for one tensor-core tile per prompt, whatever the mix
+                runner = GraphRunner(torch, rbkv, cfg, stack, caches, ws, hs, T,
+                                     max_chunk_tiles=-(-T // 128) + n + 8)
+                run = runner.run
+            else:
+                def run(p):
+                    stack.forward(p, caches, ws, hs)
             for _ in range(warm):
-                stack.forward(p, caches, ws, hs)
+                run(p)
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(reps)]
             for a, b in ev:
                 a.record(stream)
-                stack.forward(p, caches, ws, hs)
+                run(p)
                 b.record(stream)
             torch.cuda.synchronize()
             row[f"latency_ms_{kind}"] = statistics.median(a.elapsed_time(b) for a, b in ev)
+            if graph:
+                assert runner.eager == 0
+                runner.close()
             comp.rollback(p)
         row["tokens_per_s"] = T / (row["latency_ms_one_prompt"] / 1e3)
         out.append(row)
@@ -669,7 +749,7 @@ def run_profile_bench(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     w0 = time.time()
-    prof = measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs)
+    prof = measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs, graph=args.graph)
     w1 = time.time()
     clk = clocks.stop(w0, w1)
     toks = [r["tokens"] for r in prof]
@@ -690,7 +770,8 @@ def run_profile_bench(args, rank, world, local_rank):
             "workload": f"profile: {args.layers} layers, "
                         + ("Llama-2-7B-shaped decoder layers (cuBLAS projections, library "
                            "attention)" if args.layer == "full" else
-                           "library KV append + attention only") + ", fresh prompts",
+                           "library KV append + attention only") + ", fresh prompts, "
+                        + ("one CUDA graph per pass" if args.graph else "eager launches"),
             "weights_gb": stack.weight_bytes() / 1e9,
             "latency_bound_ms": args.latency_bound,
             "budget_for_bound": budget,
@@ -722,12 +803,15 @@ def run_trace_bench(args, rank, world, local_rank):
     budget = args.budget
     prof = None
     if budget <= 0:
-        prof = measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs)
+        prof = measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs,
+                               graph=args.graph)
         budget = rbkv.budget_for_latency([r["tokens"] for r in prof],
                                          [r["latency_ms_one_prompt"] for r in prof],
                                          args.latency_bound)
         if budget <= 0:
             raise SystemExit(f"no budget meets a {args.latency_bound} ms pass latency")
+
+    runner = GraphRunner(torch, rbkv, cfg, stack, caches, ws, hs, budget) if args.graph else None
 
     def drive(trace_reqs, comp, record, rec=None):
         events, tokens = [], []
@@ -738,7 +822,10 @@ def run_trace_bench(args, rank, world, local_rank):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                stack.forward(p, caches, ws, hs)
+                if runner:
+                    runner.run(p)
+                else:
+                    stack.forward(p, caches, ws, hs)
                 e1.record(stream)
                 if record:
                     events.append((e0, e1))
@@ -762,6 +849,7 @@ def run_trace_bench(args, rank, world, local_rank):
     comp = rbkv.Composer(cfg)
     rec = TraceRecorder()
     launches0 = rbkv.kernel_launches()
+    replays0 = runner.replays if runner else 0
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     wall_t0 = time.time()
@@ -772,6 +860,8 @@ def run_trace_bench(args, rank, world, local_rank):
     wall_t1 = time.time()
     clk = clocks.stop(wall_t0, wall_t1)
     launches = rbkv.kernel_launches() - launches0
+    if runner:
+        launches += (runner.replays - replays0) * runner.per_replay
     total_ms = t0.elapsed_time(t1)
     lat = sorted(e[0].elapsed_time(e[1]) for e in events if e is not None)
     ends, last = [], 0.0
@@ -817,6 +907,9 @@ def run_trace_bench(args, rank, world, local_rank):
             "warmup": "a separate 64-request trace on its own composer",
             "budget_from": (f"latency profile, bound {args.latency_bound} ms" if prof
                             else "--budget"),
+            "launch": ("frame + one CUDA graph replayed per pass "
+                       f"({runner.per_replay} library kernels per replay, "
+                       f"{runner.eager} passes eager)" if runner else "eager launches"),
         },
         "serving": serving,
         "gpu_launches": int(launches),
