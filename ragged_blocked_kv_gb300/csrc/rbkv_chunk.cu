@@ -38,16 +38,18 @@ constexpr int kRows = kChunkTileRows;       // 128 query rows (MMA M)
 constexpr int kKeys = kChunkTileKeys;       // 64 keys per KV tile
 constexpr int kStages = 4;
 constexpr int kThreads = 6 * 32;
-constexpr int kQHalf = kRows * 128;         // 16 KB: 128 rows x 64 bf16
-constexpr int kQBytes = 2 * kQHalf;
 constexpr int kKVHalf = kKeys * 128;        // 8 KB
 constexpr int kKVTile = 2 * kKVHalf;        // 16 KB
 constexpr int kStage = 2 * kKVTile;         // K + V
-constexpr int kPBytes = kRows * 128;        // one P buffer: 128 rows x 64 keys bf16 (two of them)
-constexpr int kTmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
+// Tensor memory (fp32 columns x 128 lanes, lane = query row): S0 [0,64),
+// S1 [64,128), O [128,256); the MMA A operands as packed bf16 pairs: Q
+// [256,320) (128 head dims), P0 [320,352) and P1 [352,384) (64 keys each).
+constexpr int kTmemCols = 512;
 constexpr int kOCol = 128;
+constexpr int kQCol = 256;
+constexpr int kPCol = 320;
 // about 192 KB: one CTA per SM with a 4-deep K/V ring and two P buffers
-constexpr int kSmemBytes = kQBytes + kStages * kStage + 2 * kPBytes + 256;
+constexpr int kSmemBytes = kStages * kStage + 256;
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -77,14 +79,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                    ptx::smem_u32(bar))
                : "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 in, fp32 accumulate)
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, bool accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16 (bf16 in, fp32 accumulate).  A is
+// M rows = TMEM lanes, its K elements packed two per 32-bit column.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, bool accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
@@ -143,24 +146,24 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
 // two phases ahead of a waiter (the parity of a wait is then unambiguous): S,
 // P and PV completion each have one barrier per buffer.
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full;      // the softmax threads wrote Q into tensor memory
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];   // QK^T of tile j done: S buffer j & 1
-  uint64_t p_full[2];   // softmax of tile j done: P buffer j & 1 written
+  uint64_t p_full[2];   // softmax of tile j done: P buffer j & 1 written (tensor memory)
   uint64_t o_done[2];   // PV of tile j done (it read P buffer j & 1)
   uint32_t tmem_base;
   int abort_flag;
 };
-// shared memory: Q | K/V ring | two P buffers | barriers
-static_assert(kQBytes + kStages * kStage + 2 * kPBytes + (int)sizeof(Bars) <= kSmemBytes,
+// shared memory: K/V ring | barriers
+static_assert(kStages * kStage + (int)sizeof(Bars) <= kSmemBytes,
               "shared-memory layout overflows its allocation");
 
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                              const __grid_constant__ CUtensorMap tmap_k,
+    chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
-                              ShapeInfo shp, __nv_bfloat16* __restrict__ o,
+                              ShapeInfo shp, const __nv_bfloat16* __restrict__ q,
+                              __nv_bfloat16* __restrict__ o,
                               float* __restrict__ part_o, float* __restrict__ part_lse) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw;
@@ -169,10 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicCAS(dp.status, 0, kDevBounds);
     return;
   }
-  uint8_t* q_s = base;
-  uint8_t* kv_s = q_s + kQBytes;
-  uint8_t* p_s = kv_s + kStages * kStage;
-  Bars* bars = reinterpret_cast<Bars*>(p_s + 2 * kPBytes);
+  uint8_t* kv_s = base;
+  Bars* bars = reinterpret_cast<Bars*>(kv_s + kStages * kStage);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv = (ke - kb + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&bars->q_full, 1);
+    ptx::mbar_init(&bars->q_full, 4 * 32);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars->kv_full[s], 1);
       ptx::mbar_init(&bars->kv_empty[s], 1);
@@ -223,12 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      ptx::tma_prefetch_desc(&tmap_q);
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
-      ptx::mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-      ptx::tma_load_2d(q_s, &tmap_q, h * 128, tile.row_begin, &bars->q_full);
-      ptx::tma_load_2d(q_s + kQHalf, &tmap_q, h * 128 + 64, tile.row_begin, &bars->q_full);
       const int32_t* table = dp.block_ids + tile.table_off;
       const int box_rows = B < kKeys ? B : kKeys;
       int issued = 0;
@@ -268,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = j + 1;
       }
       // every copy must land before the CTA may exit
-      ptx::mbar_wait(&bars->q_full, 0, kWaitLimit);
       for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
         ptx::mbar_wait(&bars->kv_full[j % kStages], (j / kStages) & 1, kWaitLimit);
     }
@@ -277,10 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
       constexpr uint32_t idesc_o = instr_desc(kRows, 128, 1);
-      const uint32_t q_addr = ptx::smem_u32(q_s);
       const uint32_t kv_addr = ptx::smem_u32(kv_s);
-      const uint32_t p_addr = ptx::smem_u32(p_s);
       bool ok = ptx::mbar_wait(&bars->q_full, 0, kWaitLimit);
+      if (ok) tc_fence_after();
       int pv_issued = 0;
       int site = ok ? 0 : 22, at = 0;
       auto issue_qk = [&](int j) {
@@ -288,10 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + (j & 1) * kKeys;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+          // head dims 16kk .. 16kk+15: Q columns 8kk.., K's half kk/4, 32-byte step kk%4
           const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-          tc_mma(d, smem_desc(q_addr + qo, 16, 1024), smem_desc(kt + ko, 16, 1024), idesc_s,
-                 kk > 0);
+          tc_mma_ts(d, tmem + kQCol + kk * 8, smem_desc(kt + ko, 16, 1024), idesc_s, kk > 0);
         }
         tc_commit(&bars->s_full[j & 1]);
       };
@@ -323,11 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t vt = kv_addr + (j % kStages) * kStage + kKVTile;
-        const uint32_t pt = p_addr + (j & 1) * kPBytes;
+        const uint32_t pt = tmem + kPCol + (j & 1) * 32;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          tc_mma(tmem + kOCol, smem_desc(pt + kk * 32, 16, 1024),
-                 smem_desc(vt + kk * 2048, kKVHalf, 1024), idesc_o, j > 0 || kk > 0);
+          // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
+          tc_mma_ts(tmem + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kKVHalf, 1024), idesc_o,
+                    j > 0 || kk > 0);
         }
         tc_commit(&bars->o_done[j & 1]);
         tc_commit(&bars->kv_empty[j % kStages]);
@@ -347,6 +342,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = tile.pos_begin + row;             // position of this query row
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const float qk_scale = shp.scale * kLog2e;
+    {
+      // this thread's query row -> tensor memory (the QK^T A operand); rows
+      // past the tile's end are zero
+      float qv[64];
+      uint4* q4 = reinterpret_cast<uint4*>(qv);
+      if (row < tile.n_rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            q + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q4[i] = src[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q4[i] = make_uint4(0, 0, 0, 0);
+      }
+      tmem_st32(lane_base + kQCol, qv);
+      tmem_st32(lane_base + kQCol + 32, qv + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      ptx::mbar_arrive(&bars->q_full);
+    }
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     int site = 0, at = 0;
@@ -450,18 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(0, 0, 0, 0);
         }
       }
-      // P row -> shared memory, 128-byte swizzled K-major operand layout
-      uint8_t* prow = p_s + (j & 1) * kPBytes + row * 128;
+      // P row -> tensor memory as bf16 pairs (the PV A operand)
+      {
+        float pk[32];
+        uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 v;
-        v.x = ptx::pack_bf16x2(sc[c8 * 8 + 0], sc[c8 * 8 + 1]);
-        v.y = ptx::pack_bf16x2(sc[c8 * 8 + 2], sc[c8 * 8 + 3]);
-        v.z = ptx::pack_bf16x2(sc[c8 * 8 + 4], sc[c8 * 8 + 5]);
-        v.w = ptx::pack_bf16x2(sc[c8 * 8 + 6], sc[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) = v;
+        for (int c = 0; c < 32; ++c) pk32[c] = ptx::pack_bf16x2(sc[2 * c], sc[2 * c + 1]);
+        tmem_st32(lane_base + kPCol + (j & 1) * 32, pk);
+        tmem_wait_st();
       }
-      ptx::fence_proxy_async_smem();
       tc_fence_before();
       ptx::mbar_arrive(&bars->p_full[j & 1]);
     }
@@ -535,12 +547,9 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
     return cudaErrorMisalignedAddress;
   const int64_t rows = (int64_t)dp.num_blocks * s.H_kv * s.B;
   const int box_rows = s.B < kKeys ? s.B : kKeys;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tk, tv;
   cudaError_t e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
   if (e == cudaSuccess) e = make_cache_tmap(&tv, v_cache, rows, s.D, box_rows);
-  if (e != cudaSuccess) return e;
-  // Q as [T][H_q * 128] rows; boxes of 64 columns x 128 rows (rows past T read as zero)
-  e = make_tmap_2d(&tq, q, dp.num_tokens, (int64_t)s.H_q * s.D, kRows);
   if (e != cudaSuccess) return e;
   static bool attr_done = false;
   if (!attr_done) {
@@ -564,8 +573,8 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_tcgen05_kernel, tq, tk, tv, dp, s,
-                            (__nv_bfloat16*)o, part_o, part_lse);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tcgen05_kernel, tk, tv, dp, s,
+                            (const __nv_bfloat16*)q, (__nv_bfloat16*)o, part_o, part_lse);
 }
 
 }  // namespace rbkv
