@@ -35,20 +35,21 @@ namespace rbkv {
 namespace {
 
 constexpr int kRows = kChunkTileRows;       // 128 query rows (MMA M)
-constexpr int kKeys = kChunkTileKeys;       // 64 keys per KV tile
-constexpr int kStages = 4;
+constexpr int kKeys = kChunkTileKeys;       // 128 keys per KV tile (MMA N of QK^T)
+constexpr int kStages = 3;
 constexpr int kThreads = 6 * 32;
-constexpr int kKVHalf = kKeys * 128;        // 8 KB
-constexpr int kKVTile = 2 * kKVHalf;        // 16 KB
+constexpr int kKVHalf = kKeys * 128;        // 16 KB: 128 keys x 64 head dims
+constexpr int kKVTile = 2 * kKVHalf;        // 32 KB
 constexpr int kStage = 2 * kKVTile;         // K + V
-// Tensor memory (fp32 columns x 128 lanes, lane = query row): S0 [0,64),
-// S1 [64,128), O [128,256); the MMA A operands as packed bf16 pairs: Q
-// [256,320) (128 head dims), P0 [320,352) and P1 [352,384) (64 keys each).
+// Tensor memory (fp32 columns x 128 lanes, lane = query row): S0 [0,128) and
+// S1 [128,256) (scores of one KV tile each), O [256,384), Q [384,448) as
+// packed bf16 pairs (the QK^T A operand).  The probabilities P of a tile, as
+// bf16 pairs (the PV A operand), overwrite the first 64 columns of its S
+// buffer once they are read.
 constexpr int kTmemCols = 512;
-constexpr int kOCol = 128;
-constexpr int kQCol = 256;
-constexpr int kPCol = 320;
-// about 192 KB: one CTA per SM with a 4-deep K/V ring and two P buffers
+constexpr int kOCol = 256;
+constexpr int kQCol = 384;
+// 192 KB: one CTA per SM with a 3-deep ring of 128-key K/V tiles
 constexpr int kSmemBytes = kStages * kStage + 256;
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -150,8 +151,8 @@ struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];   // QK^T of tile j done: S buffer j & 1
-  uint64_t p_full[2];   // softmax of tile j done: P buffer j & 1 written (tensor memory)
-  uint64_t o_done[2];   // PV of tile j done (it read P buffer j & 1)
+  uint64_t p_full[2];   // softmax of tile j done: P written over S buffer j & 1
+  uint64_t o_done[2];   // PV of tile j done
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -228,19 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tmap_v);
       const int32_t* table = dp.block_ids + tile.table_off;
       const int box_rows = B < kKeys ? B : kKeys;
-      int issued = 0;
-      for (int j = 0; j < n_kv && !*abort_flag; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages &&
-            !ptx::mbar_wait(&bars->kv_empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
-          ptx::report_wait(dp.status, kDevTimeout, 21, j);
-          *abort_flag = 1;
-          break;
-        }
-        uint8_t* kdst = kv_s + s * kStage;
-        uint8_t* vdst = kdst + kKVTile;
-        int32_t rows[kKeys / 8];
-        int nsub = 0, loads = 0;
+      // cache rows of the boxes of tile j (-1: out-of-range block, skipped);
+      // looked up one tile ahead, so that the block-table loads overlap the
+      // wait for a free stage
+      int32_t rows[kKeys / 8];
+      int nsub = 0, loads = 0;
+      auto lookup = [&](int j) {
+        nsub = 0;
+        loads = 0;
         for (int r = 0; r < kKeys; r += box_rows) {
           const int key = kb + j * kKeys + r;
           if (key >= ke) break;
@@ -253,6 +249,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           rows[nsub++] = (blk * shp.H_kv + kvh) * B + (key % B);
           ++loads;
         }
+      };
+      if (n_kv > 0) lookup(0);
+      int issued = 0;
+      for (int j = 0; j < n_kv && !*abort_flag; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages &&
+            !ptx::mbar_wait(&bars->kv_empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
+          ptx::report_wait(dp.status, kDevTimeout, 21, j);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* kdst = kv_s + s * kStage;
+        uint8_t* vdst = kdst + kKVTile;
         ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 4));
         for (int i = 0; i < nsub; ++i) {
           if (rows[i] < 0) continue;
@@ -263,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_2d(vdst + kKVHalf + off, &tmap_v, 64, rows[i], &bars->kv_full[s]);
         }
         issued = j + 1;
+        if (j + 1 < n_kv) lookup(j + 1);
       }
       // every copy must land before the CTA may exit
       for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
@@ -283,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + (j & 1) * kKeys;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          // head dims 16kk .. 16kk+15: Q columns 8kk.., K's half kk/4, 32-byte step kk%4
+          // head dims 16kk .. 16kk+15: Q columns 8kk.., K's half kk/4, 32-byte step kk%4;
+          // N = all 128 keys of the tile
           const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
           tc_mma_ts(d, tmem + kQCol + kk * 8, smem_desc(kt + ko, 16, 1024), idesc_s, kk > 0);
         }
@@ -317,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t vt = kv_addr + (j % kStages) * kStage + kKVTile;
-        const uint32_t pt = tmem + kPCol + (j & 1) * 32;
+        const uint32_t pt = tmem + (j & 1) * kKeys;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
           // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
           tc_mma_ts(tmem + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kKVHalf, 1024), idesc_o,
                     j > 0 || kk > 0);
@@ -375,26 +386,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float sc[64];
-      tmem_ld32(lane_base + (j & 1) * kKeys, sc);
-      tmem_ld32(lane_base + (j & 1) * kKeys + 32, sc + 32);
-      tmem_wait_ld();
+      const uint32_t s_col = lane_base + (j & 1) * kKeys;  // S of tile j; then its P
       const int key0 = kb + j * kKeys;
       // this row sees the tile's first `lim` keys: those <= its position and
       // before the split's end (a prefix of the tile, possibly empty or all)
       const int lim = min(pos + 1, ke) - key0;
-      // row max over 8 independent partial maxima (no 64-long dependent chain)
+      const bool full = __all_sync(0xffffffffu, lim >= kKeys);
+      // row max over 8 independent partial maxima, in two 64-key halves (the
+      // second half first, so that the first stays in registers)
+      float sc[64];
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-      if (__all_sync(0xffffffffu, lim >= kKeys)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
-      } else {
+      for (int hf = 1; hf >= 0; --hf) {
+        tmem_ld32(s_col + hf * 64, sc);
+        tmem_ld32(s_col + hf * 64 + 32, sc + 32);
+        tmem_wait_ld();
+        const int lh = lim - hf * 64;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          sc[c] = c < lim ? sc[c] : -INFINITY;
-          mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+          for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], c < lh ? sc[c] : -INFINITY);
         }
       }
       const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -406,28 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (raise) {
         corr = ptx::ex2(m_ref - mt);
         m_ref = mt;
-      }
-      // a row with no key in this split so far keeps m_ref = -inf: its p are 0
-      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-      float ps8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        sc[c] = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
-        ps8[c & 7] += sc[c];
-      }
-      const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      l = l * corr + ps;
-      // P buffer j & 1 is free once the PV of tile j - 2 has run
-      if (j >= 2) {
-        const bool done = ptx::mbar_wait(&bars->o_done[j & 1], ((j - 2) >> 1) & 1, kWaitLimit);
-        if (!__all_sync(0xffffffffu, done)) {
-          ok = false;
-          site = 32;
-          at = j;
-          break;
-        }
       }
       // rescaling O needs every earlier PV finished (only when a row's max rose)
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
@@ -453,6 +446,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
       }
+      // a row with no key in this split so far keeps m_ref = -inf: its p are 0
+      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+      float ps8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        if (hf == 1) {
+          tmem_ld32(s_col + 64, sc);
+          tmem_ld32(s_col + 96, sc + 32);
+          tmem_wait_ld();
+        }
+        const int lh = lim - hf * 64;
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sc[c] = c < lh ? sc[c] : -INFINITY;
+        }
+        // P of these 64 keys as bf16 pairs over S columns already read
+        float pk[32];
+        uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
+          const float p1 = ptx::ex2(fmaf(sc[c + 1], qk_scale, nbase));
+          ps8[c & 7] += p0;
+          ps8[(c + 1) & 7] += p1;
+          pk32[c / 2] = ptx::pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_col + hf * 32, pk);
+      }
+      tmem_wait_st();
+      const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      l = l * corr + ps;
       if (j == n_kv - 1 && (ke % kKeys) != 0) {
         // keys past the split's end may be anything (unwritten slots): zero their V rows
         const int s = j % kStages;
@@ -464,15 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVHalf + key * 128 + ((c & 7) << 4)) =
               make_uint4(0, 0, 0, 0);
         }
-      }
-      // P row -> tensor memory as bf16 pairs (the PV A operand)
-      {
-        float pk[32];
-        uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pk32[c] = ptx::pack_bf16x2(sc[2 * c], sc[2 * c + 1]);
-        tmem_st32(lane_base + kPCol + (j & 1) * 32, pk);
-        tmem_wait_st();
+        // the PV MMA reads these rows through the async proxy
+        ptx::fence_proxy_async_smem();
       }
       tc_fence_before();
       ptx::mbar_arrive(&bars->p_full[j & 1]);

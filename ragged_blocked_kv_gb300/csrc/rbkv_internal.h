@@ -112,7 +112,7 @@ constexpr int32_t kDevTimeout = -7;
 constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decode kernel
 constexpr int kDecodeCtasPerSm = 1;
 constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
-constexpr int kChunkTileKeys = 64;       // keys per tensor-core KV tile
+constexpr int kChunkTileKeys = 128;      // keys per tensor-core KV tile
 constexpr int kChunkMinSplitKeys = 512;  // shortest automatic key split of prompt-chunk tiles
 
 bool decode_fast_supported(const ShapeInfo& s);
