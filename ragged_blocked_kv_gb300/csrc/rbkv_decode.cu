@@ -188,25 +188,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t tile_base = 0;
   const uint32_t stages_u32 = ptx::smem_u32(sm.stages);
 
+  // query rows of a unit's group as m16n8k16 A fragments (rows >= g are zero)
+  auto load_q = [&](int item, uint32_t(&dst)[8][4]) {
+    const WorkItem u = dp.decode_items[item];
+    const __nv_bfloat16* qbase = q + ((int64_t)u.row * shp.H_q + u.kv_head * g) * 128;
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qbase + r0 * 128);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qbase + r1 * 128);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int c = (kk * 16 + cq) >> 1;
+      dst[kk][0] = r0 < g ? __ldg(q0 + c) : 0u;
+      dst[kk][1] = r1 < g ? __ldg(q1 + c) : 0u;
+      dst[kk][2] = r0 < g ? __ldg(q0 + c + 4) : 0u;
+      dst[kk][3] = r1 < g ? __ldg(q1 + c + 4) : 0u;
+    }
+  };
+  uint32_t qa[8][4];
+  if ((int)blockIdx.x < n_decode) load_q(blockIdx.x, qa);
+
   for (int item = blockIdx.x; item < n_decode; item += gridDim.x) {
     const WorkItem it = dp.decode_items[item];
     const int nt = tiles_of(it);
-
-    // query rows of the group as m16n8k16 A fragments (rows >= g are zero)
-    uint32_t qa[8][4];
-    {
-      const __nv_bfloat16* qbase = q + ((int64_t)it.row * shp.H_q + it.kv_head * g) * 128;
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qbase + r0 * 128);
-      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qbase + r1 * 128);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int c = (kk * 16 + cq) >> 1;
-        qa[kk][0] = r0 < g ? __ldg(q0 + c) : 0u;
-        qa[kk][1] = r1 < g ? __ldg(q1 + c) : 0u;
-        qa[kk][2] = r0 < g ? __ldg(q0 + c + 4) : 0u;
-        qa[kk][3] = r1 < g ? __ldg(q1 + c + 4) : 0u;
-      }
-    }
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc_o[16][4];
 #pragma unroll
@@ -316,6 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tile_base += nt;
 
+    // the next unit's queries, loaded while this one is merged
+    uint32_t qn[8][4];
+    const int next = item + gridDim.x;
+    if (next < n_decode) load_q(next, qn);
+
     // ---- merge the four warps' states and write the unit's result -------
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -390,6 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // all consumer warps leave together if anyone gave up
     if (ptx::named_bar_or(1, kConsumers * 32, abort_flag != 0)) break;
+    if (next < n_decode) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
+    }
   }
   ptx::pdl_wait_previous();
 }
