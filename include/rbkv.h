@@ -284,6 +284,28 @@ rbkv_status rbkv_ragged_attention_noalloc(rbkv_pass* p, const void* q, const voi
  * skipped that access) or RBKV_ERR_TIMEOUT (a bounded wait gave up). */
 rbkv_status rbkv_pass_device_status(rbkv_pass* p, rbkv_stream stream);
 
+/* ---- diagnostics: failure detection without a GPU fault ----------------------
+ *
+ * The kernels never trap: a block id or slot outside the pool is reported in
+ * the pass's device status word (RBKV_ERR_DEVICE_BOUNDS) and the access is
+ * skipped; every wait on a barrier is bounded and a wait that gives up is
+ * reported (RBKV_ERR_TIMEOUT, with the wait site) before the kernel returns.
+ * These two calls let tests drive both paths on a real GPU. */
+
+/* Overwrite entry `index` of the pass's block tables (which = 0) or of its
+ * slot list (which = 1) with `value`, before the pass's first device call
+ * (the composer's own state is not touched; destroy the pass afterwards).
+ * Errors: RBKV_ERR_INVALID for a bad which/index, or a pass already on the
+ * device. */
+rbkv_status rbkv_debug_corrupt_pass(rbkv_pass* p, int32_t which, int32_t index, int32_t value);
+
+/* Launch one CTA on `stream` that waits on a barrier nothing will complete,
+ * giving up after `limit_cycles` SM clock cycles (at most 2^32), and reports
+ * the timeout (wait site 99) in the pass's status words, as a kernel's own
+ * bounded wait would.  The pass must be on the device (after rbkv_kv_append).
+ * Read the result with rbkv_pass_device_status. */
+rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_stream stream);
+
 /* ---- frames: one fixed launch sequence for every pass (CUDA graphs) ---------
  *
  * Dynamic SplitFuse keeps every forward pass at about the same size (paper

@@ -105,6 +105,8 @@ SIGNATURES = {
     "rbkv_frame_workspace_bytes": (C.c_size_t, [_P]),
     "rbkv_frame_attention": (C.c_int, [_P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "rbkv_frame_device_status": (C.c_int, [_P, _P]),
+    "rbkv_debug_corrupt_pass": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32]),
+    "rbkv_debug_wait_timeout": (C.c_int, [_P, C.c_int64, _P]),
     "rbkv_kernel_launches": (C.c_int64, []),
     "rbkv_profile_enable": (None, [C.c_int32]),
     "rbkv_profile_read": (C.c_int, [C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
@@ -235,6 +237,16 @@ class Pass:
 
     def device_status(self, stream=None) -> None:
         _check(lib().rbkv_pass_device_status(self._h, _stream(stream)))
+
+    def debug_corrupt(self, which: str, index: int, value: int) -> None:
+        """Fault injection for tests: overwrite a block-table ("block") or
+        slot ("slot") entry before the pass reaches the device."""
+        w = {"block": 0, "slot": 1}[which]
+        _check(lib().rbkv_debug_corrupt_pass(self._h, w, int(index), int(value)))
+
+    def debug_wait_timeout(self, limit_cycles: int, stream=None) -> None:
+        """Run a bounded wait that is bound to give up (reported in the status)."""
+        _check(lib().rbkv_debug_wait_timeout(self._h, int(limit_cycles), _stream(stream)))
 
     def destroy(self) -> None:
         if self._h:

@@ -762,6 +762,32 @@ rbkv_status rbkv_pass_plan_for_sms(const rbkv_pass* p, int32_t num_sms, rbkv_pla
   return RBKV_OK;
 }
 
+rbkv_status rbkv_debug_corrupt_pass(rbkv_pass* p, int32_t which, int32_t index, int32_t value) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (p->dev || p->planned) return fail(RBKV_ERR_INVALID, "the pass is already on the device");
+  std::vector<int32_t>* v = which == 0 ? &p->block_ids : which == 1 ? &p->slot : nullptr;
+  if (!v) return fail(RBKV_ERR_INVALID, "which must be 0 (block ids) or 1 (slots)");
+  if (index < 0 || (size_t)index >= v->size()) return fail(RBKV_ERR_INVALID, "index out of range");
+  (*v)[index] = value;
+  return RBKV_OK;
+}
+
+rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_stream stream) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (!p->dev) return fail(RBKV_ERR_INVALID, "the pass is not on the device");
+  if (limit_cycles < 0 || limit_cycles > ((int64_t)1 << 32))
+    return fail(RBKV_ERR_INVALID, "limit_cycles must be in [0, 2^32]");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (st != p->upload_stream) {
+    cudaError_t e = cudaStreamWaitEvent(st, p->upload_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  p->last_stream = st;
+  cudaError_t e = launch_wait_timeout((int32_t*)p->dev, (long long)limit_cycles, st);
+  if (e != cudaSuccess) return cuda_fail(e, "wait-timeout launch");
+  return RBKV_OK;
+}
+
 void rbkv_pass_destroy(rbkv_pass* p) {
   if (!p) return;
   if (p->dev) cudaFreeAsync(p->dev, p->last_stream);

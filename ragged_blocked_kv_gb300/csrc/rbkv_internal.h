@@ -145,6 +145,9 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
                               bool overlap_previous);
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
+// One CTA waiting `limit` cycles on a barrier nothing completes; reports the
+// timeout in `status` (diagnostics).
+cudaError_t launch_wait_timeout(int32_t* status, long long limit, cudaStream_t st);
 
 // Host helpers for the entry point that allocates nothing (rbkv_noalloc.cu).
 // attention_on_device: rbkv_ragged_attention for a pass whose metadata is

@@ -15,6 +15,7 @@
 #include <algorithm>
 
 #include "rbkv_internal.h"
+#include "rbkv_ptx.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -241,6 +242,22 @@ cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, cons
     generic_attention_kernel<float><<<dp.n_generic, kGenWarps * 32, 0, st>>>(
         dp, s, (const float*)q, (const float*)k_cache, (const float*)v_cache, (float*)o, part_o,
         part_lse);
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void wait_timeout_kernel(int32_t* status, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_barrier_init();
+    if (!ptx::mbar_wait(&bar, 0, limit)) ptx::report_wait(status, kDevTimeout, 99, 0);
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout(int32_t* status, long long limit, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit);
   return cudaGetLastError();
 }
 

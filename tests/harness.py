@@ -38,8 +38,9 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 class Pair:
     def __init__(self, rbkv, shape: workloads.Shape, num_blocks: int, seed: int = 0,
                  only_seqs: Optional[Set[int]] = None, input_device: str = "cpu",
-                 cache_fill: Optional[float] = None):
+                 cache_fill: Optional[float] = None, policy: str = "greedy"):
         self.rbkv = rbkv
+        self.policy = policy
         self.shape = shape
         self.seed = seed
         self.only = only_seqs
@@ -74,8 +75,8 @@ class Pair:
              tokens: Optional[Iterable[int]] = None) -> dict:
         """Compose, append and (optionally) attend one pass on both sides."""
         res: dict = {}
-        p = self.lib.compose(budget, max_chunk, states)
-        m = self.orc.compose(budget, max_chunk, states)
+        p = self.lib.compose(budget, max_chunk, states, policy=self.policy)
+        m = self.orc.compose(budget, max_chunk, states, policy=self.policy)
         res["meta_equal"] = all(
             np.array_equal(np.asarray(getattr(p.meta, f), np.int64), np.asarray(getattr(m, f), np.int64))
             for f in FIELDS)
@@ -167,10 +168,12 @@ class Pair:
 
 def run_scenario(rbkv, scn: workloads.Scenario, seed: int = 0, split_keys: Optional[int] = None,
                  passes: int = 1, only_seqs: Optional[Set[int]] = None,
-                 input_device: str = "cpu", cache_fill: Optional[float] = None) -> List[dict]:
+                 input_device: str = "cpu", cache_fill: Optional[float] = None,
+                 policy: str = "greedy") -> List[dict]:
     """Registration pass, then ``passes`` measured passes with states advanced
     between them.  Returns the measured passes' results."""
-    pair = Pair(rbkv, scn.shape, scn.num_blocks, seed, only_seqs, input_device, cache_fill)
+    pair = Pair(rbkv, scn.shape, scn.num_blocks, seed, only_seqs, input_device, cache_fill,
+                policy)
     b, st = scn.registration()
     if b > 0:
         r = pair.step(b, 0, st, attend=False)

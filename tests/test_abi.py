@@ -4,6 +4,8 @@ import re
 import subprocess
 from pathlib import Path
 
+import pytest
+
 HEADER = Path(__file__).resolve().parent.parent / "include" / "rbkv.h"
 
 
@@ -40,3 +42,16 @@ def test_bad_config_is_rejected_without_a_gpu(rbkv):
         rbkv.Composer(rbkv.Config(8, 2, 48, 16, "f32", 10))
     with pytest.raises(rbkv.RbkvError):
         rbkv.Composer(rbkv.Config(8, 2, 64, 0, "f32", 10))
+
+
+def test_debug_corrupt_validates_arguments(rbkv):
+    c = rbkv.Composer(rbkv.Config(8, 2, 64, 16, "f32", 10))
+    p = c.compose(20, 0, [(1, 20, 0)])
+    assert len(p.meta.block_ids) == 2 and p.num_tokens == 20
+    with pytest.raises(rbkv.RbkvError):
+        p.debug_corrupt("block", 2, 0)
+    with pytest.raises(rbkv.RbkvError):
+        p.debug_corrupt("slot", -1, 0)
+    p.debug_corrupt("block", 1, 9)
+    p.debug_corrupt("slot", 19, 3)
+    assert rbkv.lib().rbkv_debug_corrupt_pass(p._h, 2, 0, 0) == -1   # which: 0 or 1

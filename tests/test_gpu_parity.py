@@ -54,6 +54,18 @@ def test_chunked_prompt_over_passes(rbkv, split):
     assert res[-1]["pair"].cache_equal()
 
 
+def test_equal_chunk_policy_over_passes(rbkv):
+    """The equal-chunk policy's passes (near-equal chunks, passes under the
+    budget) through the kernels, every pass against the oracle."""
+    scn = workloads.scaled(workloads.llama2_7b(1), 4)
+    res = run_scenario(rbkv, scn, passes=9, policy="equal")
+    chunks = [max(r["meta"].n_new) for r in res if max(r["meta"].n_new) > 1]
+    assert chunks and max(chunks) - min(chunks) <= 1
+    for r in res:
+        _ok(r)
+    assert res[-1]["pair"].cache_equal()
+
+
 def test_garbage_in_unwritten_slots_does_not_leak(rbkv):
     """Slots past a sequence's context hold whatever the caller left there
     (here NaN); outputs must not see them."""
