@@ -4,11 +4,13 @@
 // log-sum-exp; Step 3's split path shows the per-split softmax).
 //
 // GB300 design (HBM-bound: every cached K/V byte is read once):
-//  - persistent grid, one CTA per SM, each CTA walks a host-ordered list of
-//    work units (longest first, dealt in snake order so CTAs finish together);
+//  - persistent grid, two CTAs per SM (one for groups above 8 query heads),
+//    each CTA walks a host-ordered list of work units (longest first, dealt in
+//    snake order so CTAs finish together);
 //  - a producer warp streams 64-key K and V tiles of the paged cache with TMA
 //    (2-D tiled loads through the block table, 128-byte swizzle) into a
-//    5-stage shared-memory ring guarded by mbarriers;
+//    3-stage shared-memory ring guarded by mbarriers (six tiles in flight per
+//    SM, and two CTAs' consumers to hide each other's latency);
 //  - four consumer warps share every tile, 16 keys each (so each warp consumes
 //    the ring strictly in order); each multiplies the group's query rows
 //    (padded to 16) by its keys with warp-level bf16 MMAs (fp32 accumulation),
@@ -32,7 +34,7 @@ namespace rbkv {
 
 namespace {
 
-constexpr int kStages = 5;
+constexpr int kStages = 3;
 constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kKeys = kDecodeTileKeys;        // 64 keys per tile
@@ -40,33 +42,33 @@ constexpr int kHalf = kKeys * 128;            // 64 rows x 128 B (64 bf16 of hea
 constexpr int kTile = 2 * kHalf;              // K or V tile, head_dim 128
 constexpr int kStage = 2 * kTile;             // K + V
 constexpr int kRowPad = 132;                  // fp32 row stride of the merge scratch
-constexpr int kScratchBytes = kConsumers * 16 * kRowPad * 4;   // [warp][16][kRowPad] fp32
-constexpr int kMlBytes = kConsumers * 16 * 2 * 4;
-// about 195 KB: a 5-deep ring of 32 KB K+V tiles and the merge buffers
-constexpr int kSmemBytes = kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 16;
+// a 3-deep ring of 32 KB K+V tiles, the merge scratch [warp][g][kRowPad] fp32,
+// (max, sum) per warp and row, barriers: 96.6 KB for g = 1, 112.8 KB for g = 8
+// (two CTAs per SM), 129.2 KB for g = 16 (one)
+__host__ __device__ constexpr int smem_bytes_for(int g) {
+  return kStages * kStage + kConsumers * g * (kRowPad + 2) * 4 + 2 * kStages * 8 + 16;
+}
+constexpr int kMaxSmemBytes = smem_bytes_for(16);
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shared {
   uint8_t* stages;     // kStages x kStage, 1024-aligned
-  float* scratch;      // [kConsumers][16][kRowPad]
-  float* ml;           // [kConsumers][16][2]
+  float* scratch;      // [kConsumers][g][kRowPad]
+  float* ml;           // [kConsumers][g][2]
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
   volatile int* abort_flag;
 };
 
 // shared memory: K/V ring | merge buffer | (max, sum) per warp and row |
-// full and empty barriers | abort flag
-static_assert(kStages * kStage + kScratchBytes + kMlBytes + 2 * kStages * 8 + 4 <= kSmemBytes,
-              "shared-memory layout overflows its allocation");
-
-__device__ __forceinline__ Shared carve(uint8_t* raw) {
+// full and empty barriers | abort flag (smem_bytes_for(g) bytes)
+__device__ __forceinline__ Shared carve(uint8_t* raw, int g) {
   Shared s;
   s.stages = raw;
   s.scratch = reinterpret_cast<float*>(s.stages + kStages * kStage);
-  s.ml = s.scratch + kConsumers * 16 * kRowPad;
-  s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * 16 * 2);
+  s.ml = s.scratch + kConsumers * g * kRowPad;
+  s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * g * 2);
   s.empty = s.full + kStages;
   s.abort_flag = reinterpret_cast<volatile int*>(s.empty + kStages);
   return s;
@@ -85,7 +87,7 @@ __device__ __forceinline__ uint32_t tile_off(int key, int d) {
   return half * kHalf + key * 128 + ((chunk ^ (key & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DevPass dp, ShapeInfo shp,
                           const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ o,
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // before ending, so that its completion covers both attention kernels.
   if (wait_first) ptx::pdl_wait_previous();
   ptx::pdl_launch_dependents();
-  Shared sm = carve(smem_raw);
+  Shared sm = carve(smem_raw, shp.g);
   volatile int& abort_flag = *sm.abort_flag;
   const int n_decode = pass_count(dp, kCountDecode, dp.n_decode);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -328,30 +330,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    // (rows >= g are padding: they take no part)
     if ((lane & 3) == 0) {
-      sm.ml[(warp * 16 + r0) * 2 + 0] = m0;
-      sm.ml[(warp * 16 + r0) * 2 + 1] = l0;
-      sm.ml[(warp * 16 + r1) * 2 + 0] = m1;
-      sm.ml[(warp * 16 + r1) * 2 + 1] = l1;
+      if (r0 < g) {
+        sm.ml[(warp * g + r0) * 2 + 0] = m0;
+        sm.ml[(warp * g + r0) * 2 + 1] = l0;
+      }
+      if (r1 < g) {
+        sm.ml[(warp * g + r1) * 2 + 0] = m1;
+        sm.ml[(warp * g + r1) * 2 + 1] = l1;
+      }
     }
     ptx::named_bar_sync(1, kConsumers * 32);
     float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-      M0 = fmaxf(M0, sm.ml[(w * 16 + r0) * 2]);
-      M1 = fmaxf(M1, sm.ml[(w * 16 + r1) * 2]);
-    }
     float L0 = 0.f, L1 = 0.f;
+    if (r0 < g) {
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-      const float mw0 = sm.ml[(w * 16 + r0) * 2], mw1 = sm.ml[(w * 16 + r1) * 2];
-      if (mw0 != -INFINITY) L0 += ptx::ex2(mw0 - M0) * sm.ml[(w * 16 + r0) * 2 + 1];
-      if (mw1 != -INFINITY) L1 += ptx::ex2(mw1 - M1) * sm.ml[(w * 16 + r1) * 2 + 1];
+      for (int w = 0; w < kConsumers; ++w) M0 = fmaxf(M0, sm.ml[(w * g + r0) * 2]);
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) {
+        const float mw0 = sm.ml[(w * g + r0) * 2];
+        if (mw0 != -INFINITY) L0 += ptx::ex2(mw0 - M0) * sm.ml[(w * g + r0) * 2 + 1];
+      }
+    }
+    if (r1 < g) {
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) M1 = fmaxf(M1, sm.ml[(w * g + r1) * 2]);
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) {
+        const float mw1 = sm.ml[(w * g + r1) * 2];
+        if (mw1 != -INFINITY) L1 += ptx::ex2(mw1 - M1) * sm.ml[(w * g + r1) * 2 + 1];
+      }
     }
     const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : ptx::ex2(m0 - M0) / L0;
     const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : ptx::ex2(m1 - M1) / L1;
     // each warp stores its rescaled O; then all four are summed per element
-    float* scr = sm.scratch + warp * 16 * kRowPad;
+    float* scr = sm.scratch + warp * g * kRowPad;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int d = i * 8 + cq;
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int w = 1; w < kConsumers; ++w) {
         const float4 b =
-            *reinterpret_cast<const float4*>(sm.scratch + (w * 16 + r) * kRowPad + c4);
+            *reinterpret_cast<const float4*>(sm.scratch + (w * g + r) * kRowPad + c4);
         a.x += b.x;
         a.y += b.y;
         a.z += b.z;
@@ -388,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (it.part >= 0 && t < g) {
       float M = -INFINITY, L = 0.f;
-      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, sm.ml[(w * 16 + t) * 2]);
+      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, sm.ml[(w * g + t) * 2]);
       for (int w = 0; w < kConsumers; ++w) {
-        const float mw = sm.ml[(w * 16 + t) * 2];
-        if (mw != -INFINITY) L += ptx::ex2(mw - M) * sm.ml[(w * 16 + t) * 2 + 1];
+        const float mw = sm.ml[(w * g + t) * 2];
+        if (mw != -INFINITY) L += ptx::ex2(mw - M) * sm.ml[(w * g + t) * 2 + 1];
       }
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
@@ -451,6 +465,12 @@ cudaError_t make_cache_tmap(CUtensorMap* m, const void* cache, int64_t rows, int
   return make_tmap_2d(m, cache, rows, head_dim, box_rows);
 }
 
+int decode_ctas_per_sm(const ShapeInfo& s) {
+  // two CTAs fit when each leaves room for the other (228 KB per SM, 1 KB
+  // reserved per CTA; 160 threads x at most 204 registers each)
+  return 2 * (smem_bytes_for(s.g) + 1024) <= 228 * 1024 ? 2 : 1;
+}
+
 bool decode_fast_supported(const ShapeInfo& s) {
   const bool block_ok = (s.B % kKeys == 0) || (kKeys % s.B == 0 && s.B % 8 == 0);
   return s.dtype == 0 && s.D == 128 && s.g >= 1 && s.g <= 16 && block_ok;
@@ -472,7 +492,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
   static bool attr_done = false;
   if (!attr_done) {
     e = cudaFuncSetAttribute(decode_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+                             kMaxSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_splitkv_kernel,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -483,7 +503,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dp.decode_grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes_for(s.g);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

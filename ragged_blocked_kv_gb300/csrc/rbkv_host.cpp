@@ -261,10 +261,10 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   if (p.split_keys > 0) {
     split = round_up(p.split_keys, gran);
   } else {
-    // about four waves of equal-size units over every CTA slot of the GPU,
-    // never shorter than 512 keys (shorter units cost more in partial-output
-    // traffic than they gain in balance)
-    int64_t slots = (int64_t)std::max(1, num_sms) * kDecodeCtasPerSm;
+    // about four units per SM of equal size, never shorter than 512 keys
+    // (every unit costs a start-up, a merge and, when split, a partial output
+    // and its combine: shorter units cost more than they gain in balance)
+    int64_t slots = (int64_t)std::max(1, num_sms);
     int64_t target = (decode_work + slots * 4 - 1) / (slots * 4);
     split = std::max<int32_t>(512, round_up(std::max<int64_t>(target, 1), gran));
   }
@@ -348,7 +348,7 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
     return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
   });
   int32_t grid = (int32_t)std::min<int64_t>((int64_t)decode.size(),
-                                            (int64_t)std::max(1, num_sms) * kDecodeCtasPerSm);
+                                            (int64_t)std::max(1, num_sms) * decode_ctas_per_sm(s));
   if (grid > 0) snake_order(decode, grid);
   pl.decode_grid = grid;
   pl.decode.swap(decode);
@@ -955,7 +955,7 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
-  const int64_t slots = (int64_t)sms * kDecodeCtasPerSm;
+  const int64_t slots = (int64_t)sms * decode_ctas_per_sm(s);
   auto clamp = [](int64_t v) { return (int32_t)std::min<int64_t>(v, 1 << 28); };
   if (!c.max_seqs) c.max_seqs = c.max_tokens;
   if (!c.max_blocks) c.max_blocks = std::max(1, cfg->num_blocks);

@@ -110,12 +110,14 @@ constexpr int32_t kDevTimeout = -7;
 
 // Fast-path envelopes.
 constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decode kernel
-constexpr int kDecodeCtasPerSm = 1;
+
 constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
 constexpr int kChunkTileKeys = 128;      // keys per tensor-core KV tile
 constexpr int kChunkMinSplitKeys = 512;  // shortest automatic key split of prompt-chunk tiles
 
 bool decode_fast_supported(const ShapeInfo& s);
+// Persistent decode CTAs resident per SM for this shape (1 or 2).
+int decode_ctas_per_sm(const ShapeInfo& s);
 // 2-D view of a bf16 [num_blocks][H_kv][B][head_dim] cache for TMA: `rows`
 // rows of head_dim elements, boxes of 64 columns x box_rows rows, 128 B swizzle.
 cudaError_t make_cache_tmap(::CUtensorMap_st* m, const void* cache, int64_t rows,
