@@ -165,12 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                               const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
                               ShapeInfo shp, const __nv_bfloat16* __restrict__ q,
                               __nv_bfloat16* __restrict__ o,
-                              float* __restrict__ part_o, float* __restrict__ part_lse) {
+                              float* __restrict__ part_o, float* __restrict__ part_lse,
+                              int wait_first) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw;
   if (ptx::smem_u32(smem_raw) & 1023) {
     // the swizzled operand layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) atomicCAS(dp.status, 0, kDevBounds);
+    ptx::pdl_wait_previous();   // the grid's completion still covers its predecessor
     return;
   }
   uint8_t* kv_s = base;
@@ -211,11 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // The grid may have been launched while the cache append before it still
-  // runs: wait for it here, after the set-up.  Only then let the decode
-  // kernel that follows start (on SMs this grid leaves free), so that it
-  // never sees a cache still being written.
-  ptx::pdl_wait_previous();
+  // The grid may have been launched while its predecessor still runs.  After
+  // the cache append (`wait_first`) it waits for it here, after the set-up.
+  // After this call's decode kernel it need not: that kernel let it start
+  // only once the append had finished; it then waits for the decode kernel
+  // before ending, so that its completion covers both attention kernels.
+  if (wait_first) ptx::pdl_wait_previous();
   if (threadIdx.x == 0) ptx::pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
@@ -548,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (!wait_first) ptx::pdl_wait_previous();
 }
 
 }  // namespace
@@ -559,7 +563,8 @@ bool chunk_fast_supported(const ShapeInfo& s) {
 
 cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                               const void* k_cache, const void* v_cache, void* o, float* part_o,
-                              float* part_lse, cudaStream_t st, bool overlap_previous) {
+                              float* part_lse, cudaStream_t st, bool overlap_previous,
+                              bool wait_first) {
   if (!chunk_fast_supported(s)) return cudaErrorNotSupported;
   if (dp.n_chunk == 0) return cudaSuccess;
   if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
@@ -593,7 +598,8 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, chunk_attn_tcgen05_kernel, tk, tv, dp, s,
-                            (const __nv_bfloat16*)q, (__nv_bfloat16*)o, part_o, part_lse);
+                            (const __nv_bfloat16*)q, (__nv_bfloat16*)o, part_o, part_lse,
+                            wait_first ? 1 : 0);
 }
 
 }  // namespace rbkv

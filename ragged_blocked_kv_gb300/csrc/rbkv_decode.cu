@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (ptx::smem_u32(smem_raw) & 1023) {
     // the swizzled tile layout needs a 1024-byte aligned base
     if (threadIdx.x == 0) atomicCAS(dp.status, 0, kDevBounds);
+    ptx::pdl_wait_previous();   // the grid's completion still covers its predecessor
     return;
   }
 

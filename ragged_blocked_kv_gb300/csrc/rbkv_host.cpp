@@ -518,13 +518,13 @@ rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache
   const DevPass& dp = p->dp;
   e = cudaSuccess;
   int launched = 0;
-  if (dp.n_chunk) {
-    e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, false);
+  if (dp.n_decode) {
+    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, false, true);
     ++launched;
   }
-  if (e == cudaSuccess && dp.n_decode) {
-    e = launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, dp.n_chunk > 0,
-                           false);
+  if (e == cudaSuccess && dp.n_chunk) {
+    e = launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, dp.n_decode > 0,
+                          dp.n_decode == 0);
     ++launched;
   }
   if (e == cudaSuccess && dp.n_generic) {
@@ -840,18 +840,20 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
   // Kernels overlap their predecessor in the stream through programmatic
   // dependent launch (not while per-launch events are recorded).  Each waits
   // for its predecessor before touching memory it might share with it: the
-  // chunk kernel before any global access; the decode kernel too, unless its
-  // predecessor is this call's chunk kernel (which lets it start only once
-  // everything before the chunk kernel has finished).
+  // decode kernel before any global access; the chunk kernel too, unless its
+  // predecessor is this call's decode kernel (which lets it start only once
+  // everything before the decode kernel has finished).  The decode grid goes
+  // first and fills every SM; chunk tiles take SMs as decode CTAs finish.
   const bool overlap = !g_prof.on;
-  if (dp.n_chunk)
-    e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
-      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap);
-    });
-  if (e == cudaSuccess && dp.n_decode)
+  if (dp.n_decode)
     e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
       return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
-                                dp.n_chunk == 0);
+                                true);
+    });
+  if (e == cudaSuccess && dp.n_chunk)
+    e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
+      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
+                               dp.n_decode == 0);
     });
   if (e == cudaSuccess && dp.n_generic)
     e = launch_counted(RBKV_KERNEL_GENERIC, st, [&] {
@@ -1114,16 +1116,17 @@ rbkv_status rbkv_frame_attention(rbkv_frame* f, const void* q, const void* k_cac
   float* part_lse = (float*)((char*)workspace + partial_o_bytes(f->caps.max_parts, s));
   const DevPass& dp = f->dp;
   // the same launch sequence as rbkv_ragged_attention with every kernel
-  // present: the chunk grid always precedes the decode grid (its CTAs without
-  // a tile wait for the append and leave)
+  // present: the decode grid always precedes the chunk grid (its CTAs without
+  // a unit leave; chunk CTAs without a tile wait for the decode grid and leave)
   const bool overlap = !g_prof.on;
-  cudaError_t e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
-    return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap);
+  cudaError_t e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
+    return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
+                              true);
   });
   if (e == cudaSuccess)
-    e = launch_counted(RBKV_KERNEL_DECODE, st, [&] {
-      return launch_decode_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
-                                false);
+    e = launch_counted(RBKV_KERNEL_CHUNK, st, [&] {
+      return launch_chunk_fast(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st, overlap,
+                               false);
     });
   if (e == cudaSuccess)
     e = launch_counted(RBKV_KERNEL_COMBINE, st,

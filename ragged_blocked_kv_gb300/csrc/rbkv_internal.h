@@ -144,7 +144,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
 cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void* q,
                               const void* k_cache, const void* v_cache, void* o,
                               float* part_o, float* part_lse, cudaStream_t st,
-                              bool overlap_previous);
+                              bool overlap_previous, bool wait_first);
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
 // One CTA waiting `limit` cycles on a barrier nothing completes; reports the
