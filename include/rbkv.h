@@ -334,7 +334,7 @@ typedef struct rbkv_frame rbkv_frame;
  *   max_blocks        the pool's num_blocks
  *   max_decode_items  4 x SMs + max_seqs x num_heads_kv (the automatic split
  *                     plan never needs more)
- *   max_chunk_tiles   ceil(max_tokens / 128) + 8, at least ceil(SMs / num_heads_q)
+ *   max_chunk_tiles   ceil(max_tokens / 128) + max_seqs, at least ceil(SMs / num_heads_q)
  *   max_combine_rows  max_tokens x num_heads_kv
  *   max_parts         max_decode_items + max_tokens x num_heads_kv x
  *                     max(1, SMs / num_heads_q) */

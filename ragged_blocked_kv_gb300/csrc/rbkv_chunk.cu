@@ -23,6 +23,8 @@
 // (about 192 KB of shared memory, 256 TMEM columns).
 // Every wait is bounded; on timeout the kernel records RBKV_ERR_TIMEOUT, lets
 // its copies and MMAs drain (bounded), frees its TMEM and returns.
+#include <algorithm>
+
 #include "rbkv_internal.h"
 #include "rbkv_ptx.cuh"
 
@@ -180,20 +182,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if ((int)blockIdx.x >= pass_count(dp, kCountChunk, dp.n_chunk)) {
-    // a frame's capacity-sized grid: no tile here.  Still wait for the
-    // predecessor, so that this grid's completion covers the cache append
+  // work items: (tile, query head) pairs, tiles sorted longest first, heads
+  // inner; this persistent CTA takes items in snake order over the grid
+  const int n_items = pass_count(dp, kCountChunk, dp.n_chunk) * shp.H_q;
+  if ((int)blockIdx.x >= n_items) {
+    // a grid sized for a frame's capacity: nothing here.  Still wait for the
+    // predecessor, so that this grid's completion covers it
     ptx::pdl_wait_previous();
     return;
   }
-  const ChunkTile tile = dp.chunk_tiles[blockIdx.x];
-  const int h = blockIdx.y;
-  const int kvh = h / shp.g;
+  const int G = gridDim.x;
+  auto item_of = [&](int k) -> int {
+    const int w = k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    return w < n_items ? w : -1;
+  };
   const int B = shp.B;
-  // keys of this split: [kb, ke); the last row of the tile sees keys < pos_begin + n_rows
-  const int kb = tile.key_begin;
-  const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
-  const int n_kv = (ke - kb + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 4 * 32);
@@ -225,61 +228,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Every role walks the same items and KV tiles in the same order; `gi`
+  // numbers this CTA's KV tiles across items, so the ring stage (gi % kStages),
+  // the S/P buffer (gi & 1) and every barrier phase continue from item to item.
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
-      const int32_t* table = dp.block_ids + tile.table_off;
       const int box_rows = B < kKeys ? B : kKeys;
-      // cache rows of the boxes of tile j (-1: out-of-range block, skipped);
-      // looked up one tile ahead, so that the block-table loads overlap the
-      // wait for a free stage
-      int32_t rows[kKeys / 8];
-      int nsub = 0, loads = 0;
-      auto lookup = [&](int j) {
-        nsub = 0;
-        loads = 0;
-        for (int r = 0; r < kKeys; r += box_rows) {
-          const int key = kb + j * kKeys + r;
-          if (key >= ke) break;
-          const int32_t blk = table[key / B];
-          if (blk < 0 || blk >= dp.num_blocks) {
-            atomicCAS(dp.status, 0, kDevBounds);
-            rows[nsub++] = -1;
-            continue;
+      uint32_t gi = 0;
+      bool stop = false;
+      for (int k = 0; !stop; ++k) {
+        const int w = item_of(k);
+        if (w < 0) break;
+        const ChunkTile tile = dp.chunk_tiles[w / shp.H_q];
+        const int kvh = (w % shp.H_q) / shp.g;
+        const int kb = tile.key_begin;
+        const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
+        const int n_kv = (ke - kb + kKeys - 1) / kKeys;
+        const int32_t* table = dp.block_ids + tile.table_off;
+        // cache rows of the boxes of KV tile j (-1: out-of-range block,
+        // skipped); looked up one tile ahead, so that the block-table loads
+        // overlap the wait for a free stage
+        int32_t rows[kKeys / 8];
+        int nsub = 0, loads = 0;
+        auto lookup = [&](int j) {
+          nsub = 0;
+          loads = 0;
+          for (int r = 0; r < kKeys; r += box_rows) {
+            const int key = kb + j * kKeys + r;
+            if (key >= ke) break;
+            const int32_t blk = table[key / B];
+            if (blk < 0 || blk >= dp.num_blocks) {
+              atomicCAS(dp.status, 0, kDevBounds);
+              rows[nsub++] = -1;
+              continue;
+            }
+            rows[nsub++] = (blk * shp.H_kv + kvh) * B + (key % B);
+            ++loads;
           }
-          rows[nsub++] = (blk * shp.H_kv + kvh) * B + (key % B);
-          ++loads;
+        };
+        if (n_kv > 0) lookup(0);
+        for (int j = 0; j < n_kv; ++j, ++gi) {
+          const int s = gi % kStages;
+          if (*abort_flag) {
+            stop = true;
+            break;
+          }
+          if (gi >= (uint32_t)kStages &&
+              !ptx::mbar_wait(&bars->kv_empty[s], ((gi / kStages) - 1) & 1, kWaitLimit)) {
+            ptx::report_wait(dp.status, kDevTimeout, 21, (int)gi);
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          uint8_t* kdst = kv_s + s * kStage;
+          uint8_t* vdst = kdst + kKVTile;
+          ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 4));
+          for (int i = 0; i < nsub; ++i) {
+            if (rows[i] < 0) continue;
+            const int off = i * box_rows * 128;
+            ptx::tma_load_2d(kdst + off, &tmap_k, 0, rows[i], &bars->kv_full[s]);
+            ptx::tma_load_2d(kdst + kKVHalf + off, &tmap_k, 64, rows[i], &bars->kv_full[s]);
+            ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &bars->kv_full[s]);
+            ptx::tma_load_2d(vdst + kKVHalf + off, &tmap_v, 64, rows[i], &bars->kv_full[s]);
+          }
+          if (j + 1 < n_kv) lookup(j + 1);
         }
-      };
-      if (n_kv > 0) lookup(0);
-      int issued = 0;
-      for (int j = 0; j < n_kv && !*abort_flag; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages &&
-            !ptx::mbar_wait(&bars->kv_empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
-          ptx::report_wait(dp.status, kDevTimeout, 21, j);
-          *abort_flag = 1;
-          break;
-        }
-        uint8_t* kdst = kv_s + s * kStage;
-        uint8_t* vdst = kdst + kKVTile;
-        ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 4));
-        for (int i = 0; i < nsub; ++i) {
-          if (rows[i] < 0) continue;
-          const int off = i * box_rows * 128;
-          ptx::tma_load_2d(kdst + off, &tmap_k, 0, rows[i], &bars->kv_full[s]);
-          ptx::tma_load_2d(kdst + kKVHalf + off, &tmap_k, 64, rows[i], &bars->kv_full[s]);
-          ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &bars->kv_full[s]);
-          ptx::tma_load_2d(vdst + kKVHalf + off, &tmap_v, 64, rows[i], &bars->kv_full[s]);
-        }
-        issued = j + 1;
-        if (j + 1 < n_kv) lookup(j + 1);
       }
       // every copy must land before the CTA may exit
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        ptx::mbar_wait(&bars->kv_full[j % kStages], (j / kStages) & 1, kWaitLimit);
+      for (uint32_t t = gi > (uint32_t)kStages ? gi - kStages : 0; t < gi; ++t)
+        ptx::mbar_wait(&bars->kv_full[t % kStages], (t / kStages) & 1, kWaitLimit);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -287,13 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
       constexpr uint32_t idesc_o = instr_desc(kRows, 128, 1);
       const uint32_t kv_addr = ptx::smem_u32(kv_s);
-      bool ok = ptx::mbar_wait(&bars->q_full, 0, kWaitLimit);
-      if (ok) tc_fence_after();
-      int pv_issued = 0;
-      int site = ok ? 0 : 22, at = 0;
-      auto issue_qk = [&](int j) {
-        const uint32_t kt = kv_addr + (j % kStages) * kStage;
-        const uint32_t d = tmem + (j & 1) * kKeys;
+      auto issue_qk = [&](uint32_t t) {
+        const uint32_t kt = kv_addr + (t % kStages) * kStage;
+        const uint32_t d = tmem + (t & 1) * kKeys;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // head dims 16kk .. 16kk+15: Q columns 8kk.., K's half kk/4, 32-byte step kk%4;
@@ -301,244 +317,299 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
           tc_mma_ts(d, tmem + kQCol + kk * 8, smem_desc(kt + ko, 16, 1024), idesc_s, kk > 0);
         }
-        tc_commit(&bars->s_full[j & 1]);
+        tc_commit(&bars->s_full[t & 1]);
       };
-      if (ok && n_kv > 0) {
-        ok = ptx::mbar_wait(&bars->kv_full[0], 0, kWaitLimit);
-        if (!ok) site = 23;
-        if (ok) {
-          tc_fence_after();
-          issue_qk(0);
-        }
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          if (!ptx::mbar_wait(&bars->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
-                              kWaitLimit)) {
-            ok = false;
-            site = 24;
-            at = j + 1;
-            break;
-          }
-          tc_fence_after();
-          issue_qk(j + 1);
-        }
-        if (!ptx::mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, kWaitLimit) || *abort_flag) {
+      bool ok = true;
+      int site = 0, at = 0;
+      uint32_t gi = 0;
+      long long pv_last = -1;   // the last PV issued (its tile number)
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k);
+        if (w < 0) break;
+        const ChunkTile tile = dp.chunk_tiles[w / shp.H_q];
+        const int kb = tile.key_begin;
+        const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
+        const int n_kv = (ke - kb + kKeys - 1) / kKeys;
+        // this item's Q rows are in tensor memory
+        if (!ptx::mbar_wait(&bars->q_full, k & 1, kWaitLimit) || *abort_flag) {
           ok = false;
-          site = 25;
-          at = j;
+          site = 22;
+          at = k;
           break;
         }
         tc_fence_after();
-        const uint32_t vt = kv_addr + (j % kStages) * kStage + kKVTile;
-        const uint32_t pt = tmem + (j & 1) * kKeys;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
-          tc_mma_ts(tmem + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kKVHalf, 1024), idesc_o,
-                    j > 0 || kk > 0);
+        if (n_kv > 0) {
+          if (!ptx::mbar_wait(&bars->kv_full[gi % kStages], (gi / kStages) & 1, kWaitLimit)) {
+            ok = false;
+            site = 23;
+            at = (int)gi;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(gi);
         }
-        tc_commit(&bars->o_done[j & 1]);
-        tc_commit(&bars->kv_empty[j % kStages]);
-        pv_issued = j + 1;
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const uint32_t t = gi + j;
+          if (j + 1 < n_kv) {
+            if (!ptx::mbar_wait(&bars->kv_full[(t + 1) % kStages], ((t + 1) / kStages) & 1,
+                                kWaitLimit)) {
+              ok = false;
+              site = 24;
+              at = (int)t + 1;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(t + 1);
+          }
+          if (!ptx::mbar_wait(&bars->p_full[t & 1], (t >> 1) & 1, kWaitLimit) || *abort_flag) {
+            ok = false;
+            site = 25;
+            at = (int)t;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vt = kv_addr + (t % kStages) * kStage + kKVTile;
+          const uint32_t pt = tmem + (t & 1) * kKeys;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
+            tc_mma_ts(tmem + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kKVHalf, 1024),
+                      idesc_o, j > 0 || kk > 0);
+          }
+          tc_commit(&bars->o_done[t & 1]);
+          tc_commit(&bars->kv_empty[t % kStages]);
+          pv_last = t;
+        }
+        gi += n_kv;
       }
       if (!ok) {
         ptx::report_wait(dp.status, kDevTimeout, site, at);
         *abort_flag = 1;
       }
       // the last PV (and so every earlier one) must finish before TMEM is released
-      if (pv_issued > 0)
-        ptx::mbar_wait(&bars->o_done[(pv_issued - 1) & 1], ((pv_issued - 1) >> 1) & 1, kWaitLimit);
+      if (pv_last >= 0)
+        ptx::mbar_wait(&bars->o_done[pv_last & 1], (pv_last >> 1) & 1, kWaitLimit);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int row = threadIdx.x;                      // 0..127 = TMEM lane
-    const int pos = tile.pos_begin + row;             // position of this query row
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const float qk_scale = shp.scale * kLog2e;
-    {
-      // this thread's query row -> tensor memory (the QK^T A operand); rows
-      // past the tile's end are zero
-      float qv[64];
-      uint4* q4 = reinterpret_cast<uint4*>(qv);
-      if (row < tile.n_rows) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            q + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q4[i] = src[i];
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q4[i] = make_uint4(0, 0, 0, 0);
-      }
-      tmem_st32(lane_base + kQCol, qv);
-      tmem_st32(lane_base + kQCol + 32, qv + 32);
-      tmem_wait_st();
-      tc_fence_before();
-      ptx::mbar_arrive(&bars->q_full);
-    }
-    float m_ref = -INFINITY, l = 0.f;
+    uint32_t gi = 0;
     bool ok = true;
     int site = 0, at = 0;
-    for (int j = 0; j < n_kv; ++j) {
-      // tcgen05.ld/st are warp-collective: every decision below is warp-uniform
-      const bool got = ptx::mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, kWaitLimit);
-      if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *abort_flag != 0)) {
-        ok = false;
-        site = 31;
-        at = j;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t s_col = lane_base + (j & 1) * kKeys;  // S of tile j; then its P
-      const int key0 = kb + j * kKeys;
-      // this row sees the tile's first `lim` keys: those <= its position and
-      // before the split's end (a prefix of the tile, possibly empty or all)
-      const int lim = min(pos + 1, ke) - key0;
-      const bool full = __all_sync(0xffffffffu, lim >= kKeys);
-      // row max over 8 independent partial maxima, in two 64-key halves (the
-      // second half first, so that the first stays in registers)
-      float sc[64];
-      float mx8[8];
+    for (int k = 0; ok; ++k) {
+      const int w = item_of(k);
+      if (w < 0) break;
+      const ChunkTile tile = dp.chunk_tiles[w / shp.H_q];
+      const int h = w % shp.H_q;
+      const int kvh = h / shp.g;
+      const int kb = tile.key_begin;
+      const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
+      const int n_kv = (ke - kb + kKeys - 1) / kKeys;
+      const int pos = tile.pos_begin + row;           // position of this query row
+      {
+        // this thread's query row -> tensor memory (the QK^T A operand); rows
+        // past the tile's end are zero.  The previous item's MMAs have all
+        // finished (its epilogue waited for its last PV).
+        float qv[64];
+        uint4* q4 = reinterpret_cast<uint4*>(qv);
+        if (row < tile.n_rows) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              q + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-#pragma unroll
-      for (int hf = 1; hf >= 0; --hf) {
-        tmem_ld32(s_col + hf * 64, sc);
-        tmem_ld32(s_col + hf * 64 + 32, sc + 32);
-        tmem_wait_ld();
-        const int lh = lim - hf * 64;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+          for (int i = 0; i < 16; ++i) q4[i] = src[i];
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], c < lh ? sc[c] : -INFINITY);
+          for (int i = 0; i < 16; ++i) q4[i] = make_uint4(0, 0, 0, 0);
         }
+        tmem_st32(lane_base + kQCol, qv);
+        tmem_st32(lane_base + kQCol + 32, qv + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        ptx::mbar_arrive(&bars->q_full);
       }
-      const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // the scale is positive, so the row max scales with it
-      const float mt = mraw * qk_scale;
-      float corr = 1.f;
-      const bool raise = mt > m_ref + kRescaleThreshold;
-      if (raise) {
-        corr = ptx::ex2(m_ref - mt);
-        m_ref = mt;
-      }
-      // rescaling O needs every earlier PV finished (only when a row's max rose)
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        const bool done =
-            ptx::mbar_wait(&bars->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitLimit);
-        if (!__all_sync(0xffffffffu, done)) {
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_kv; ++j) {
+        const uint32_t t = gi + j;
+        // tcgen05.ld/st are warp-collective: every decision below is warp-uniform
+        const bool got = ptx::mbar_wait(&bars->s_full[t & 1], (t >> 1) & 1, kWaitLimit);
+        if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *abort_flag != 0)) {
           ok = false;
-          site = 33;
-          at = j;
+          site = 31;
+          at = (int)t;
           break;
         }
         tc_fence_after();
-        {
+        const uint32_t s_col = lane_base + (t & 1) * kKeys;  // S of tile t; then its P
+        const int key0 = kb + j * kKeys;
+        // this row sees the tile's first `lim` keys: those <= its position and
+        // before the split's end (a prefix of the tile, possibly empty or all)
+        const int lim = min(pos + 1, ke) - key0;
+        const bool full = __all_sync(0xffffffffu, lim >= kKeys);
+        // row max over 8 independent partial maxima, in two 64-key halves (the
+        // second half first, so that the first stays in registers)
+        float sc[64];
+        float mx8[8];
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            float ov[32];
+        for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          tmem_ld32(s_col + hf * 64, sc);
+          tmem_ld32(s_col + hf * 64 + 32, sc + 32);
+          tmem_wait_ld();
+          const int lh = lim - hf * 64;
+          if (full) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              mx8[c & 7] = fmaxf(mx8[c & 7], c < lh ? sc[c] : -INFINITY);
+          }
+        }
+        const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // the scale is positive, so the row max scales with it
+        const float mt = mraw * qk_scale;
+        float corr = 1.f;
+        const bool raise = mt > m_ref + kRescaleThreshold;
+        if (raise) {
+          corr = ptx::ex2(m_ref - mt);
+          m_ref = mt;
+        }
+        // rescaling O needs every earlier PV of this item finished (only when
+        // a row's max rose)
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          const bool done =
+              ptx::mbar_wait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, kWaitLimit);
+          if (!__all_sync(0xffffffffu, done)) {
+            ok = false;
+            site = 33;
+            at = (int)t;
+            break;
+          }
+          tc_fence_after();
+          {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              float ov[32];
+              tmem_ld32(lane_base + kOCol + c4 * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] *= corr;
+              tmem_st32(lane_base + kOCol + c4 * 32, ov);
+            }
+            tmem_wait_st();
+          }
+        }
+        // a row with no key in this split so far keeps m_ref = -inf: its p are 0
+        const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+        float ps8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (hf == 1) {
+            tmem_ld32(s_col + 64, sc);
+            tmem_ld32(s_col + 96, sc + 32);
+            tmem_wait_ld();
+          }
+          const int lh = lim - hf * 64;
+          if (!full) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sc[c] = c < lh ? sc[c] : -INFINITY;
+          }
+          // P of these 64 keys as bf16 pairs over S columns already read
+          float pk[32];
+          uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
+            const float p1 = ptx::ex2(fmaf(sc[c + 1], qk_scale, nbase));
+            ps8[c & 7] += p0;
+            ps8[(c + 1) & 7] += p1;
+            pk32[c / 2] = ptx::pack_bf16x2(p0, p1);
+          }
+          tmem_st32(s_col + hf * 32, pk);
+        }
+        tmem_wait_st();
+        const float ps =
+            ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+        l = l * corr + ps;
+        if (j == n_kv - 1 && (ke % kKeys) != 0) {
+          // keys past the split's end may be anything (unwritten slots): zero their V rows
+          const int s = t % kStages;
+          ptx::mbar_wait(&bars->kv_full[s], (t / kStages) & 1, kWaitLimit);
+          uint8_t* vt = kv_s + s * kStage + kKVTile;
+          const int valid = ke - key0;
+          for (int e = row; e < (kKeys - valid) * 16; e += kRows) {
+            const int key = valid + e / 16, c = e % 16;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVHalf + key * 128 + ((c & 7) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+          // the PV MMA reads these rows through the async proxy
+          ptx::fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        ptx::mbar_arrive(&bars->p_full[t & 1]);
+      }
+      bool fin = ok;
+      if (fin && n_kv > 0) {
+        const uint32_t tl = gi + n_kv - 1;
+        fin = ptx::mbar_wait(&bars->o_done[tl & 1], (tl >> 1) & 1, kWaitLimit);
+      }
+      if (__all_sync(0xffffffffu, fin)) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool store = row < tile.n_rows;
+        const bool partial = tile.part_base >= 0;
+        __nv_bfloat16* orow = o + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128;
+        // partial slot of (row, KV head, split); query head h % g inside it
+        const int64_t slot =
+            ((int64_t)tile.part_base + ((int64_t)row * shp.H_kv + kvh) * tile.nsplit +
+             tile.split) * shp.g + (h % shp.g);
+        float* prow = part_o + slot * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float ov[32];
+          if (n_kv > 0) {
             tmem_ld32(lane_base + kOCol + c4 * 32, ov);
             tmem_wait_ld();
+          } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] *= corr;
-            tmem_st32(lane_base + kOCol + c4 * 32, ov);
+            for (int c = 0; c < 32; ++c) ov[c] = 0.f;   // an empty key range: no PV ran
           }
-          tmem_wait_st();
+          if (store && !partial) {
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              uint4 v;
+              v.x = ptx::pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
+              v.y = ptx::pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
+              v.z = ptx::pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
+              v.w = ptx::pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
+              *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = v;
+            }
+          } else if (store) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              *reinterpret_cast<float4*>(prow + c4 * 32 + c8 * 4) =
+                  make_float4(ov[c8 * 4 + 0] * inv, ov[c8 * 4 + 1] * inv, ov[c8 * 4 + 2] * inv,
+                              ov[c8 * 4 + 3] * inv);
+          }
+        }
+        if (store && partial) part_lse[slot] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+      } else {
+        if (ok) {
+          ok = false;
+          site = 34;
+          at = (int)(gi + n_kv);
         }
       }
-      // a row with no key in this split so far keeps m_ref = -inf: its p are 0
-      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-      float ps8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        if (hf == 1) {
-          tmem_ld32(s_col + 64, sc);
-          tmem_ld32(s_col + 96, sc + 32);
-          tmem_wait_ld();
-        }
-        const int lh = lim - hf * 64;
-        if (!full) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sc[c] = c < lh ? sc[c] : -INFINITY;
-        }
-        // P of these 64 keys as bf16 pairs over S columns already read
-        float pk[32];
-        uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
-          const float p1 = ptx::ex2(fmaf(sc[c + 1], qk_scale, nbase));
-          ps8[c & 7] += p0;
-          ps8[(c + 1) & 7] += p1;
-          pk32[c / 2] = ptx::pack_bf16x2(p0, p1);
-        }
-        tmem_st32(s_col + hf * 32, pk);
-      }
-      tmem_wait_st();
-      const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      l = l * corr + ps;
-      if (j == n_kv - 1 && (ke % kKeys) != 0) {
-        // keys past the split's end may be anything (unwritten slots): zero their V rows
-        const int s = j % kStages;
-        ptx::mbar_wait(&bars->kv_full[s], (j / kStages) & 1, kWaitLimit);
-        uint8_t* vt = kv_s + s * kStage + kKVTile;
-        const int valid = ke - key0;
-        for (int e = row; e < (kKeys - valid) * 16; e += kRows) {
-          const int key = valid + e / 16, c = e % 16;
-          *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVHalf + key * 128 + ((c & 7) << 4)) =
-              make_uint4(0, 0, 0, 0);
-        }
-        // the PV MMA reads these rows through the async proxy
-        ptx::fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      ptx::mbar_arrive(&bars->p_full[j & 1]);
+      gi += n_kv;
     }
-    bool fin = ok && n_kv > 0;
-    if (fin)
-      fin = ptx::mbar_wait(&bars->o_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, kWaitLimit);
-    if (__all_sync(0xffffffffu, fin)) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool store = row < tile.n_rows;
-      const bool partial = tile.part_base >= 0;
-      __nv_bfloat16* orow = o + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128;
-      // partial slot of (row, KV head, split); query head h % g inside it
-      const int64_t slot =
-          ((int64_t)tile.part_base + ((int64_t)row * shp.H_kv + kvh) * tile.nsplit + tile.split) *
-              shp.g + (h % shp.g);
-      float* prow = part_o + slot * 128;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float ov[32];
-        tmem_ld32(lane_base + kOCol + c4 * 32, ov);
-        tmem_wait_ld();
-        if (store && !partial) {
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint4 v;
-            v.x = ptx::pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
-            v.y = ptx::pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
-            v.z = ptx::pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
-            v.w = ptx::pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = v;
-          }
-        } else if (store) {
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<float4*>(prow + c4 * 32 + c8 * 4) =
-                make_float4(ov[c8 * 4 + 0] * inv, ov[c8 * 4 + 1] * inv, ov[c8 * 4 + 2] * inv,
-                            ov[c8 * 4 + 3] * inv);
-        }
-      }
-      if (store && partial) part_lse[slot] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-    } else if (!ok || n_kv > 0) {
-      ptx::report_wait(dp.status, kDevTimeout, ok ? 34 : site, ok ? n_kv : at);
+    if (!ok) {
+      ptx::report_wait(dp.status, kDevTimeout, site, at);
       *abort_flag = 1;
     }
   }
@@ -586,7 +657,19 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid(dp.n_chunk, s.H_q);
+  // persistent: at most one CTA per SM, each walking (tile, head) items
+  static int sms_of[64] = {0};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = dev < 64 ? sms_of[dev] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sms_of[dev] = sms;
+  }
+  const int64_t items = (int64_t)dp.n_chunk * s.H_q;
+  dim3 grid((unsigned)std::min<int64_t>(items, std::max(1, sms)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);

@@ -963,8 +963,9 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   if (!c.max_blocks) c.max_blocks = std::max(1, cfg->num_blocks);
   if (!c.max_decode_items)
     c.max_decode_items = clamp(4 * slots + (int64_t)c.max_seqs * s.H_kv);
-  if (!c.max_chunk_tiles)
-    c.max_chunk_tiles = clamp(std::max<int64_t>(ceil_div(c.max_tokens, kChunkTileRows) + 8,
+  if (!c.max_chunk_tiles)   // the chunk grid is persistent: capacity costs nothing at launch
+    c.max_chunk_tiles = clamp(std::max<int64_t>((int64_t)ceil_div(c.max_tokens, kChunkTileRows) +
+                                                    c.max_seqs,
                                                 ceil_div(sms, s.H_q)));
   if (!c.max_combine_rows) c.max_combine_rows = clamp((int64_t)c.max_tokens * s.H_kv);
   if (!c.max_parts)
