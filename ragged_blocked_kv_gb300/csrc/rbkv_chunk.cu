@@ -25,6 +25,8 @@
 // its copies and MMAs drain (bounded), frees its TMEM and returns.
 #include <algorithm>
 
+#include <atomic>
+
 #include "rbkv_internal.h"
 #include "rbkv_ptx.cuh"
 
@@ -646,8 +648,13 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   cudaError_t e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
   if (e == cudaSuccess) e = make_cache_tmap(&tv, v_cache, rows, s.D, box_rows);
   if (e != cudaSuccess) return e;
-  static bool attr_done = false;
-  if (!attr_done) {
+  // the shared-memory limit is raised once per device
+  static std::atomic<uint64_t> attr_done{0};
+  int attr_dev = 0;
+  e = cudaGetDevice(&attr_dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t attr_bit = 1ull << (attr_dev & 63);
+  if (!(attr_done.load() & attr_bit)) {
     e = cudaFuncSetAttribute(chunk_attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e == cudaSuccess)
@@ -655,7 +662,7 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done.fetch_or(attr_bit);
   }
   // persistent: at most one CTA per SM, each walking (tile, head) items
   static int sms_of[64] = {0};

@@ -21,6 +21,8 @@
 //    base-2 log-sum-exp for the combine kernel.
 // Every wait is bounded: on timeout the kernel records RBKV_ERR_TIMEOUT in the
 // pass's status word and stops.
+#include <atomic>
+
 #include "rbkv_internal.h"
 #include "rbkv_ptx.cuh"
 
@@ -490,8 +492,13 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
   cudaError_t e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
   if (e == cudaSuccess) e = make_cache_tmap(&tv, v_cache, rows, s.D, box_rows);
   if (e != cudaSuccess) return e;
-  static bool attr_done = false;
-  if (!attr_done) {
+  // the shared-memory limit is raised once per device
+  static std::atomic<uint64_t> attr_done{0};
+  int attr_dev = 0;
+  e = cudaGetDevice(&attr_dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t attr_bit = 1ull << (attr_dev & 63);
+  if (!(attr_done.load() & attr_bit)) {
     e = cudaFuncSetAttribute(decode_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxSmemBytes);
     if (e == cudaSuccess)
@@ -499,7 +506,7 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done.fetch_or(attr_bit);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dp.decode_grid);

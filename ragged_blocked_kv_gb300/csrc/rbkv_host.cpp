@@ -805,7 +805,7 @@ rbkv_status rbkv_kv_append(rbkv_pass* p, const void* k_new, const void* v_new, v
   if (rs != RBKV_OK) return rs;
   const ShapeInfo s = shape_of(p->cfg);
   cudaError_t e = launch_counted(RBKV_KERNEL_KV_APPEND, st, [&] {
-    return launch_kv_append(p->dp, s, k_new, v_new, k_cache, v_cache, st);
+    return launch_kv_append(p->dp, s, k_new, v_new, k_cache, v_cache, st, !g_prof.on);
   });
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return RBKV_OK;
@@ -1090,7 +1090,7 @@ rbkv_status rbkv_frame_kv_append(rbkv_frame* f, const void* k_new, const void* v
   cudaStream_t st = (cudaStream_t)stream;
   const ShapeInfo s = shape_of(f->cfg);
   cudaError_t e = launch_counted(RBKV_KERNEL_KV_APPEND, st, [&] {
-    return launch_kv_append(f->dp, s, k_new, v_new, k_cache, v_cache, st);
+    return launch_kv_append(f->dp, s, k_new, v_new, k_cache, v_cache, st, !g_prof.on);
   });
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return RBKV_OK;

@@ -129,7 +129,8 @@ bool chunk_fast_supported(const ShapeInfo& s);
 
 // Kernel launchers (return the launch's cudaError_t).
 cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* k_new,
-                             const void* v_new, void* k_cache, void* v_cache, cudaStream_t st);
+                             const void* v_new, void* k_cache, void* v_cache, cudaStream_t st,
+                             bool overlap_previous);
 cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
                                      const void* k_cache, const void* v_cache, void* o,
                                      float* part_o, float* part_lse, cudaStream_t st);

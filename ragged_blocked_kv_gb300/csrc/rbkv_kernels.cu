@@ -46,32 +46,60 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // ---------------------------------------------------------------------------
 // One warp per (token, KV head): the first half of the warp copies the K row,
 // the second half the V row, 16 bytes per lane per step (32-bit index math).
+// A warp takes two rows at a time, with every load of both issued before the
+// first store (rows are at most 64 x 16 bytes).
 constexpr int kAppendWarps = 8;
 
 __global__ void __launch_bounds__(kAppendWarps * 32)
     kv_append_kernel(DevPass dp, int32_t H_kv, int32_t B, int32_t vec_per_row,
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache, uint4* __restrict__ v_cache) {
-  // the attention kernels may launch now; they wait for this grid before
-  // reading the cache
+  // Launched to overlap its predecessor's tail: wait for it (it may have
+  // produced k_new / v_new, or still read cache blocks this pass reuses).
+  // The attention kernels may launch as soon as every CTA is here; they wait
+  // for this grid before reading the cache.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const uint4* __restrict__ src = half ? v_new : k_new;
   uint4* __restrict__ dst = half ? v_cache : k_cache;
   const uint32_t rows = (uint32_t)pass_count(dp, kCountTokens, dp.num_tokens) * (uint32_t)H_kv;
-  for (uint32_t r = blockIdx.x * kAppendWarps + warp; r < rows; r += gridDim.x * kAppendWarps) {
-    const uint32_t t = r / (uint32_t)H_kv;
-    const uint32_t h = r - t * (uint32_t)H_kv;
-    const int32_t slot = dp.slot[t];
-    const int32_t blk = slot / B, off = slot - blk * B;
-    if (slot < 0 || blk >= dp.num_blocks) {
-      if (lane == 0) report(dp.status, kDevBounds);
-      continue;
+  const uint32_t stride = gridDim.x * kAppendWarps;
+  for (uint32_t r0 = blockIdx.x * kAppendWarps + warp; r0 < rows; r0 += 2 * stride) {
+    const uint32_t r1 = r0 + stride;
+    const bool two = r1 < rows;
+    const uint32_t t0 = r0 / (uint32_t)H_kv;
+    const uint32_t t1 = two ? r1 / (uint32_t)H_kv : t0;
+    const int32_t slot0 = dp.slot[t0];
+    const int32_t slot1 = dp.slot[t1];
+    uint4 b0[4], b1[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v = hl + 16 * i;
+      if (v < vec_per_row) {
+        b0[i] = src[(size_t)r0 * vec_per_row + v];
+        if (two) b1[i] = src[(size_t)r1 * vec_per_row + v];
+      }
     }
-    const uint4* s_row = src + (size_t)r * vec_per_row;
-    uint4* d_row = dst + (((size_t)blk * H_kv + h) * B + off) * vec_per_row;
-    for (int v = hl; v < vec_per_row; v += 16) d_row[v] = s_row[v];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (k == 1 && !two) break;
+      const uint32_t r = k ? r1 : r0, t = k ? t1 : t0;
+      const int32_t slot = k ? slot1 : slot0;
+      const uint32_t h = r - t * (uint32_t)H_kv;
+      const int32_t blk = slot / B, off = slot - blk * B;
+      if (slot < 0 || blk >= dp.num_blocks) {
+        if (lane == 0) report(dp.status, kDevBounds);
+        continue;
+      }
+      uint4* d_row = dst + (((size_t)blk * H_kv + h) * B + off) * vec_per_row;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int v = hl + 16 * i;
+        if (v < vec_per_row) d_row[v] = k ? b1[i] : b0[i];
+      }
+    }
   }
 }
 
@@ -173,6 +201,8 @@ __global__ void __launch_bounds__(128)
   // launched to overlap the attention kernels' tail: the partials are only
   // complete once they have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next pass's cache append may launch now (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x % 32;
   const int64_t n_warps = (int64_t)pass_count(dp, kCountCombine, dp.n_combine) * s.g;
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < n_warps;
@@ -214,7 +244,8 @@ int num_sms_current() {
 }  // namespace
 
 cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* k_new,
-                             const void* v_new, void* k_cache, void* v_cache, cudaStream_t st) {
+                             const void* v_new, void* k_cache, void* v_cache, cudaStream_t st,
+                             bool overlap_previous) {
   const int esz = s.dtype == 0 ? 2 : 4;
   const int vec = s.D * esz / 16;
   const int64_t rows = (int64_t)dp.num_tokens * s.H_kv;
@@ -223,10 +254,17 @@ cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* 
   int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
   const int64_t cap = (int64_t)num_sms_current() * 8;
   if (blocks > cap) blocks = cap;
-  kv_append_kernel<<<(unsigned)blocks, kAppendWarps * 32, 0, st>>>(
-      dp, s.H_kv, s.B, vec, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
-      (uint4*)v_cache);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kAppendWarps * 32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kv_append_kernel, dp, s.H_kv, s.B, vec, (const uint4*)k_new,
+                            (const uint4*)v_new, (uint4*)k_cache, (uint4*)v_cache);
 }
 
 cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
