@@ -40,8 +40,8 @@ HBM_FALLBACK_GBS = 6800.0
 # summarised under profiles/, keyed by (workload, kernel) and valid only for
 # the kernel source they were taken on (sha256 prefix of its .cu file)
 TRAFFIC_BYTES = {
-    ("llama2_7b", "decode"): ("rbkv_decode.cu", "507444b07d41", 615_034_880),
-    ("mistral_7b", "decode"): ("rbkv_decode.cu", "507444b07d41", 9_181_227_264),
+    ("llama2_7b", "decode"): ("rbkv_decode.cu", "9aeb83c3161f", 614_349_056),
+    ("mistral_7b", "decode"): ("rbkv_decode.cu", "9aeb83c3161f", 9_181_267_776),
 }
 BF16_FALLBACK_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
