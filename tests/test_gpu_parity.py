@@ -66,6 +66,28 @@ def test_equal_chunk_policy_over_passes(rbkv):
     assert res[-1]["pair"].cache_equal()
 
 
+@pytest.mark.parametrize("hq,hkv", [(16, 4), (8, 8)])
+def test_many_prompt_chunks_persistent_grid(rbkv, hq, hkv):
+    """Hundreds of prompt chunks of mixed length (fresh prompts and chunks behind
+    cached prefixes) next to decodes: many more (tile, head) items than SMs, so
+    every chunk CTA walks several items in snake order, with items as short as
+    one key tile.  Every output against the oracle."""
+    rng = np.random.default_rng(hq * 7 + hkv)
+    shape = workloads.Shape(hq, hkv, 128, 64, "bf16", 1.0 / np.sqrt(128.0))
+    hist = [(1000 + i, int(rng.integers(1, 700))) for i in range(40)]
+    reqs = [(1000 + i, c + int(rng.integers(1, 90)), c) for i, (_, c) in enumerate(hist[:30])]
+    reqs += [(1000 + i, c, c) for i, (_, c) in enumerate(hist[30:], start=30)]      # decodes
+    reqs += [(5000 + i, int(rng.integers(1, 160)), 0) for i in range(160)]            # fresh prompts
+    budget = sum(p - s if p > s else 1 for _, p, s in reqs)
+    nb = sum(-(-(c + 300) // 64) for _, c in hist) + sum(-(-p // 64) for sid, p, s in reqs
+                                                           if sid >= 5000) + 64
+    scn = workloads.Scenario("many", shape, budget, 0, hist, reqs, nb)
+    (r,) = run_scenario(rbkv, scn)
+    assert r["plan"]["chunk_tiles"] * hq > 4 * 152
+    _ok(r)
+    assert r["pair"].cache_equal()
+
+
 def test_garbage_in_unwritten_slots_does_not_leak(rbkv):
     """Slots past a sequence's context hold whatever the caller left there
     (here NaN); outputs must not see them."""
