@@ -309,8 +309,8 @@ rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_str
 /* ---- frames: one fixed launch sequence for every pass (CUDA graphs) ---------
  *
  * Dynamic SplitFuse keeps every forward pass at about the same size (paper
- * summary page, Summary and idea I3; InfoQ note: "a consistent forward
- * size"), so a serving loop can record the launches of one pass once, as a
+ * summary page, Summary and idea I3; InfoQ release note: passes of a steady
+ * size), so a serving loop can record the launches of one pass once, as a
  * CUDA graph, and replay them for every later pass.  A frame makes that
  * possible: it holds a pass's metadata at fixed device addresses, inside
  * capacities fixed when it is created, and its kernel launches are sized by

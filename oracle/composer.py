@@ -1,10 +1,10 @@
 """Dynamic SplitFuse pass composition, written out step by step (oracle).
 
-Source: "DeepSpeed-FastGen" paper summary page, Summary and idea I3 - the
-scheduler keeps every forward pass at a fixed token budget, cuts long prompts
-into chunks spread over several passes, and packs generation tokens and short
-prompts to fill the budget; InfoQ release note - a consistent forward size
-built from partial prompt tokens composed with generation.  The FastGen guide's
+Source: "DeepSpeed-FastGen" paper summary page, Summary and idea I3 - each
+pass is held to one token budget: a long prompt is cut into pieces that go
+into successive passes, and generation tokens and short prompts take up the
+rest of the budget; InfoQ release note - passes of a steady size, made
+of pieces of prompts mixed with generation tokens.  The FastGen guide's
 "Prompt-Decode Decoupling" adds that chunks are bounded (e.g. 512 tokens) and
 interleaved with decode steps so generation never stalls.
 

@@ -2,9 +2,9 @@
 
 Source: DeepSpeed-FastGen paper summary page, Key points and idea I4 - judge a
 chat service by an "effective throughput" tied to time to first token (TTFT)
-and the steady pace of streamed tokens, and report token-level tail latency;
-the FastGen guide's benchmark table reports TTFT P90, per-token P99 latency and
-requests per second served within a per-token latency bound.
+and how regularly the following tokens arrive, and report token-level tail
+latency; the FastGen guide's benchmark table reports TTFT P90, per-token P99
+latency and requests per second served within a per-token latency bound.
 
 Readings (the pages define no formula):
 

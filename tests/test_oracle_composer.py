@@ -1,7 +1,8 @@
 """Pins for the oracle's Dynamic SplitFuse composer (CPU only).
 
 What the pages fix: every pass holds exactly the token budget when there is
-enough demand (paper summary page, Summary: "fill the budget exactly"); long
+enough demand (paper summary page, Summary: passes are topped up to the whole
+budget); long
 prompts are spread over passes in chunks; generation tokens ride along in every
 pass (FastGen guide, "Prompt-Decode Decoupling").  The tiny workload statement
 fixes its pass's token counts (40 + 3 + 21).

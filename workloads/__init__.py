@@ -8,8 +8,8 @@ lists them.  Composition, appending and attention are done by each side on its
 own.
 
 Workload shapes follow the pages' settings: Llama-2-7B, Llama-2-70B and
-Mistral-7B attention shapes; prompt and output lengths drawn from normal
-distributions with means 2600 and 60 and 30% standard deviation
+Mistral-7B attention shapes; normally distributed prompt and output lengths
+with means 2600 and 60 and 30% standard deviation
 ("DeepSpeed-FastGen" paper summary page, Key points, benchmark setup); a
 512-request closed-loop trace from up to 32 clients (same passage).
 """
