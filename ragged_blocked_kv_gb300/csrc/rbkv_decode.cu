@@ -44,20 +44,27 @@ constexpr int kHalf = kKeys * 128;            // 64 rows x 128 B (64 bf16 of hea
 constexpr int kTile = 2 * kHalf;              // K or V tile, head_dim 128
 constexpr int kStage = 2 * kTile;             // K + V
 constexpr int kRowPad = 132;                  // fp32 row stride of the merge scratch
-// a 3-deep ring of 32 KB K+V tiles, the merge scratch [warp][g][kRowPad] fp32,
-// (max, sum) per warp and row, barriers: 96.6 KB for g = 1, 112.8 KB for g = 8
-// (two CTAs per SM), 129.2 KB for g = 16 (one)
-__host__ __device__ constexpr int smem_bytes_for(int g) {
-  return kStages * kStage + kConsumers * g * (kRowPad + 2) * 4 + 2 * kStages * 8 + 16;
+// Rows of a unit's merge buffers: its query rows x heads - g for decode rows;
+// with packed prompt rows (`packed`), up to kDecodeRowsCap for groups of up
+// to kDecodeRowsCap heads, g above that.
+__host__ __device__ constexpr int rows_cap_for(int g, bool packed) {
+  return packed && g < kDecodeRowsCap ? kDecodeRowsCap : g;
 }
-constexpr int kMaxSmemBytes = smem_bytes_for(16);
+// a 3-deep ring of 32 KB K+V tiles, the merge scratch [warp][rows][kRowPad]
+// fp32, (max, sum) per warp and row, barriers: 96.6 KB (g = 1) to 112.8 KB
+// (g = 8, or packed rows) - two CTAs per SM - and 129.2 KB for g = 16 (one)
+__host__ __device__ constexpr int smem_bytes_for(int g, bool packed) {
+  return kStages * kStage + kConsumers * rows_cap_for(g, packed) * (kRowPad + 2) * 4 +
+         2 * kStages * 8 + 16;
+}
+constexpr int kMaxSmemBytes = smem_bytes_for(16, true);
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clock
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shared {
   uint8_t* stages;     // kStages x kStage, 1024-aligned
-  float* scratch;      // [kConsumers][g][kRowPad]
-  float* ml;           // [kConsumers][g][2]
+  float* scratch;      // [kConsumers][rows][kRowPad]
+  float* ml;           // [kConsumers][rows][2]
   uint64_t* full;      // [kStages]
   uint64_t* empty;     // [kStages]
   volatile int* abort_flag;
@@ -65,12 +72,12 @@ struct Shared {
 
 // shared memory: K/V ring | merge buffer | (max, sum) per warp and row |
 // full and empty barriers | abort flag (smem_bytes_for(g) bytes)
-__device__ __forceinline__ Shared carve(uint8_t* raw, int g) {
+__device__ __forceinline__ Shared carve(uint8_t* raw, int rows) {
   Shared s;
   s.stages = raw;
   s.scratch = reinterpret_cast<float*>(s.stages + kStages * kStage);
-  s.ml = s.scratch + kConsumers * g * kRowPad;
-  s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * g * 2);
+  s.ml = s.scratch + kConsumers * rows * kRowPad;
+  s.full = reinterpret_cast<uint64_t*>(s.ml + kConsumers * rows * 2);
   s.empty = s.full + kStages;
   s.abort_flag = reinterpret_cast<volatile int*>(s.empty + kStages);
   return s;
@@ -89,6 +96,7 @@ __device__ __forceinline__ uint32_t tile_off(int key, int d) {
   return half * kHalf + key * 128 + ((chunk ^ (key & 7)) << 4);
 }
 
+template <bool kPacked>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DevPass dp, ShapeInfo shp,
@@ -105,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   // before ending, so that its completion covers both attention kernels.
   if (wait_first) ptx::pdl_wait_previous();
   ptx::pdl_launch_dependents();
-  Shared sm = carve(smem_raw, shp.g);
+  const int rcap = rows_cap_for(shp.g, kPacked);
+  Shared sm = carve(smem_raw, rcap);
   volatile int& abort_flag = *sm.abort_flag;
   const int n_decode = pass_count(dp, kCountDecode, dp.n_decode);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -193,19 +202,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t tile_base = 0;
   const uint32_t stages_u32 = ptx::smem_u32(sm.stages);
 
-  // query rows of a unit's group as m16n8k16 A fragments (rows >= g are zero)
+  // the query rows of a unit as m16n8k16 A fragments: fragment row r is
+  // query head r % g of the unit's row r / g; rows past n_rows * g are zero
   auto load_q = [&](int item, uint32_t(&dst)[8][4]) {
     const WorkItem u = dp.decode_items[item];
-    const __nv_bfloat16* qbase = q + ((int64_t)u.row * shp.H_q + u.kv_head * g) * 128;
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qbase + r0 * 128);
-    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qbase + r1 * 128);
+    const int nrg = kPacked ? u.n_rows * g : g;
+    const __nv_bfloat16* qb0 =
+        q + ((int64_t)(u.row + r0 / g) * shp.H_q + u.kv_head * g + r0 % g) * 128;
+    const __nv_bfloat16* qb1 =
+        q + ((int64_t)(u.row + r1 / g) * shp.H_q + u.kv_head * g + r1 % g) * 128;
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb0);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb1);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int c = (kk * 16 + cq) >> 1;
-      dst[kk][0] = r0 < g ? __ldg(q0 + c) : 0u;
-      dst[kk][1] = r1 < g ? __ldg(q1 + c) : 0u;
-      dst[kk][2] = r0 < g ? __ldg(q0 + c + 4) : 0u;
-      dst[kk][3] = r1 < g ? __ldg(q1 + c + 4) : 0u;
+      dst[kk][0] = r0 < nrg ? __ldg(q0 + c) : 0u;
+      dst[kk][1] = r1 < nrg ? __ldg(q1 + c) : 0u;
+      dst[kk][2] = r0 < nrg ? __ldg(q0 + c + 4) : 0u;
+      dst[kk][3] = r1 < nrg ? __ldg(q1 + c + 4) : 0u;
     }
   };
   uint32_t qa[8][4];
@@ -214,6 +228,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int item = blockIdx.x; item < n_decode; item += gridDim.x) {
     const WorkItem it = dp.decode_items[item];
     const int nt = tiles_of(it);
+    const int nrg = kPacked ? it.n_rows * g : g;
+    // keys visible to fragment rows r0 and r1 (packed rows are causal)
+    const int lim0 = kPacked && r0 < nrg ? min(it.key_end, it.diag + r0 / g) : it.key_end;
+    const int lim1 = kPacked && r1 < nrg ? min(it.key_end, it.diag + r1 / g) : it.key_end;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc_o[16][4];
 #pragma unroll
@@ -266,15 +284,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           ptx::mma_bf16_16816(sc[0], qa[kk], b0, b1);
           ptx::mma_bf16_16816(sc[1], qa[kk], b2, b3);
         }
-        // scale, mask keys past the unit, online softmax (rows r0 and r1)
+        // scale, mask keys past each row's limit, online softmax (rows r0 and r1)
+        const int valid0 = min(kKeys, lim0 - k0) - wk, valid1 = min(kKeys, lim1 - k0) - wk;
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
           const int key = n * 8 + cq;
-          sc[n][0] = key < valid ? sc[n][0] * qk_scale : -INFINITY;
-          sc[n][1] = key + 1 < valid ? sc[n][1] * qk_scale : -INFINITY;
-          sc[n][2] = key < valid ? sc[n][2] * qk_scale : -INFINITY;
-          sc[n][3] = key + 1 < valid ? sc[n][3] * qk_scale : -INFINITY;
+          sc[n][0] = key < valid0 ? sc[n][0] * qk_scale : -INFINITY;
+          sc[n][1] = key + 1 < valid0 ? sc[n][1] * qk_scale : -INFINITY;
+          sc[n][2] = key < valid1 ? sc[n][2] * qk_scale : -INFINITY;
+          sc[n][3] = key + 1 < valid1 ? sc[n][3] * qk_scale : -INFINITY;
           mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
           mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
         }
@@ -283,13 +302,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float c0 = ptx::ex2(m0 - mn0), c1 = ptx::ex2(m1 - mn1);
+        // a row with no visible key so far keeps max -inf: its terms are 0
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float c0 = ptx::ex2(m0 - b0), c1 = ptx::ex2(m1 - b1);
         m0 = mn0;
         m1 = mn1;
-        const float p00 = ptx::ex2(sc[0][0] - mn0), p01 = ptx::ex2(sc[0][1] - mn0);
-        const float p02 = ptx::ex2(sc[0][2] - mn1), p03 = ptx::ex2(sc[0][3] - mn1);
-        const float p10 = ptx::ex2(sc[1][0] - mn0), p11 = ptx::ex2(sc[1][1] - mn0);
-        const float p12 = ptx::ex2(sc[1][2] - mn1), p13 = ptx::ex2(sc[1][3] - mn1);
+        const float p00 = ptx::ex2(sc[0][0] - b0), p01 = ptx::ex2(sc[0][1] - b0);
+        const float p02 = ptx::ex2(sc[0][2] - b1), p03 = ptx::ex2(sc[0][3] - b1);
+        const float p10 = ptx::ex2(sc[1][0] - b0), p11 = ptx::ex2(sc[1][1] - b0);
+        const float p12 = ptx::ex2(sc[1][2] - b1), p13 = ptx::ex2(sc[1][3] - b1);
         l0 = l0 * c0 + (p00 + p01 + p10 + p11);
         l1 = l1 * c1 + (p02 + p03 + p12 + p13);
         uint32_t pa[4];
@@ -333,68 +354,69 @@ __global__ void __launch_bounds__(kThreads, 2)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    // (rows >= g are padding: they take no part)
+    // (fragment rows >= n_rows * g are padding: they take no part)
     if ((lane & 3) == 0) {
-      if (r0 < g) {
-        sm.ml[(warp * g + r0) * 2 + 0] = m0;
-        sm.ml[(warp * g + r0) * 2 + 1] = l0;
+      if (r0 < nrg) {
+        sm.ml[(warp * rcap + r0) * 2 + 0] = m0;
+        sm.ml[(warp * rcap + r0) * 2 + 1] = l0;
       }
-      if (r1 < g) {
-        sm.ml[(warp * g + r1) * 2 + 0] = m1;
-        sm.ml[(warp * g + r1) * 2 + 1] = l1;
+      if (r1 < nrg) {
+        sm.ml[(warp * rcap + r1) * 2 + 0] = m1;
+        sm.ml[(warp * rcap + r1) * 2 + 1] = l1;
       }
     }
     ptx::named_bar_sync(1, kConsumers * 32);
     float M0 = -INFINITY, M1 = -INFINITY;
     float L0 = 0.f, L1 = 0.f;
-    if (r0 < g) {
+    if (r0 < nrg) {
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) M0 = fmaxf(M0, sm.ml[(w * g + r0) * 2]);
+      for (int w = 0; w < kConsumers; ++w) M0 = fmaxf(M0, sm.ml[(w * rcap + r0) * 2]);
 #pragma unroll
       for (int w = 0; w < kConsumers; ++w) {
-        const float mw0 = sm.ml[(w * g + r0) * 2];
-        if (mw0 != -INFINITY) L0 += ptx::ex2(mw0 - M0) * sm.ml[(w * g + r0) * 2 + 1];
+        const float mw0 = sm.ml[(w * rcap + r0) * 2];
+        if (mw0 != -INFINITY) L0 += ptx::ex2(mw0 - M0) * sm.ml[(w * rcap + r0) * 2 + 1];
       }
     }
-    if (r1 < g) {
+    if (r1 < nrg) {
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) M1 = fmaxf(M1, sm.ml[(w * g + r1) * 2]);
+      for (int w = 0; w < kConsumers; ++w) M1 = fmaxf(M1, sm.ml[(w * rcap + r1) * 2]);
 #pragma unroll
       for (int w = 0; w < kConsumers; ++w) {
-        const float mw1 = sm.ml[(w * g + r1) * 2];
-        if (mw1 != -INFINITY) L1 += ptx::ex2(mw1 - M1) * sm.ml[(w * g + r1) * 2 + 1];
+        const float mw1 = sm.ml[(w * rcap + r1) * 2];
+        if (mw1 != -INFINITY) L1 += ptx::ex2(mw1 - M1) * sm.ml[(w * rcap + r1) * 2 + 1];
       }
     }
     const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : ptx::ex2(m0 - M0) / L0;
     const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : ptx::ex2(m1 - M1) / L1;
     // each warp stores its rescaled O; then all four are summed per element
-    float* scr = sm.scratch + warp * g * kRowPad;
+    float* scr = sm.scratch + warp * rcap * kRowPad;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int d = i * 8 + cq;
-      if (r0 < g)
+      if (r0 < nrg)
         *reinterpret_cast<float2*>(scr + r0 * kRowPad + d) =
             make_float2(acc_o[i][0] * f0, acc_o[i][1] * f0);
-      if (r1 < g)
+      if (r1 < nrg)
         *reinterpret_cast<float2*>(scr + r1 * kRowPad + d) =
             make_float2(acc_o[i][2] * f1, acc_o[i][3] * f1);
     }
     ptx::named_bar_sync(1, kConsumers * 32);
     const int t = threadIdx.x;   // 0..127
-    for (int e = t; e < g * 32; e += kConsumers * 32) {
+    for (int e = t; e < nrg * 32; e += kConsumers * 32) {
       const int r = e >> 5, c4 = (e & 31) * 4;
       float4 a = *reinterpret_cast<const float4*>(sm.scratch + r * kRowPad + c4);
 #pragma unroll
       for (int w = 1; w < kConsumers; ++w) {
         const float4 b =
-            *reinterpret_cast<const float4*>(sm.scratch + (w * g + r) * kRowPad + c4);
+            *reinterpret_cast<const float4*>(sm.scratch + (w * rcap + r) * kRowPad + c4);
         a.x += b.x;
         a.y += b.y;
         a.z += b.z;
         a.w += b.w;
       }
       if (it.part < 0) {
-        __nv_bfloat16* orow = o + ((int64_t)it.row * shp.H_q + it.kv_head * g + r) * 128 + c4;
+        __nv_bfloat16* orow =
+            o + ((int64_t)(it.row + r / g) * shp.H_q + it.kv_head * g + r % g) * 128 + c4;
         uint2 packed;
         packed.x = ptx::pack_bf16x2(a.x, a.y);
         packed.y = ptx::pack_bf16x2(a.z, a.w);
@@ -405,10 +427,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (it.part >= 0 && t < g) {
       float M = -INFINITY, L = 0.f;
-      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, sm.ml[(w * g + t) * 2]);
+      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, sm.ml[(w * rcap + t) * 2]);
       for (int w = 0; w < kConsumers; ++w) {
-        const float mw = sm.ml[(w * g + t) * 2];
-        if (mw != -INFINITY) L += ptx::ex2(mw - M) * sm.ml[(w * g + t) * 2 + 1];
+        const float mw = sm.ml[(w * rcap + t) * 2];
+        if (mw != -INFINITY) L += ptx::ex2(mw - M) * sm.ml[(w * rcap + t) * 2 + 1];
       }
       part_lse[(int64_t)it.part * g + t] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
@@ -471,7 +493,7 @@ cudaError_t make_cache_tmap(CUtensorMap* m, const void* cache, int64_t rows, int
 int decode_ctas_per_sm(const ShapeInfo& s) {
   // two CTAs fit when each leaves room for the other (228 KB per SM, 1 KB
   // reserved per CTA; 160 threads x at most 204 registers each)
-  return 2 * (smem_bytes_for(s.g) + 1024) <= 228 * 1024 ? 2 : 1;
+  return 2 * (smem_bytes_for(s.g, true) + 1024) <= 228 * 1024 ? 2 : 1;
 }
 
 bool decode_fast_supported(const ShapeInfo& s) {
@@ -492,34 +514,38 @@ cudaError_t launch_decode_fast(const DevPass& dp, const ShapeInfo& s, const void
   cudaError_t e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
   if (e == cudaSuccess) e = make_cache_tmap(&tv, v_cache, rows, s.D, box_rows);
   if (e != cudaSuccess) return e;
-  // the shared-memory limit is raised once per device
+  // the shared-memory limit of each variant is raised once per device
   static std::atomic<uint64_t> attr_done{0};
   int attr_dev = 0;
   e = cudaGetDevice(&attr_dev);
   if (e != cudaSuccess) return e;
   const uint64_t attr_bit = 1ull << (attr_dev & 63);
   if (!(attr_done.load() & attr_bit)) {
-    e = cudaFuncSetAttribute(decode_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_splitkv_kernel,
-                               cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
+    for (int v = 0; v < 2 && e == cudaSuccess; ++v) {
+      auto fn = v ? decode_splitkv_kernel<true> : decode_splitkv_kernel<false>;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemBytes);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    }
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(attr_bit);
   }
+  const bool packed = dp.decode_packed != 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dp.decode_grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes_for(s.g);
+  cfg.dynamicSmemBytes = smem_bytes_for(s.g, packed);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel, tk, tv, dp, s, (const __nv_bfloat16*)q,
-                            (__nv_bfloat16*)o, part_o, part_lse, wait_first ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg,
+                            packed ? decode_splitkv_kernel<true> : decode_splitkv_kernel<false>,
+                            tk, tv, dp, s, (const __nv_bfloat16*)q, (__nv_bfloat16*)o, part_o,
+                            part_lse, wait_first ? 1 : 0);
 }
 
 }  // namespace rbkv

@@ -170,6 +170,7 @@ struct Plan {
   std::vector<CombineRow> combine;
   int32_t n_parts = 0;
   int32_t decode_grid = 0;
+  int32_t decode_packed = 0;  // some decode units pack several prompt rows
 };
 
 }  // namespace
@@ -304,12 +305,26 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
         pl.combine.push_back(CombineRow{row, h, part0, ns});
       }
       for (int32_t k = 0; k < ns; ++k)
-        dst.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1, table_off});
+        dst.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1, table_off,
+                               1, n_keys});
     }
   };
+  // rows of a short prompt chunk per decode unit: all g query heads of each
+  const int32_t pack = s.g <= kDecodeRowsCap ? kDecodeRowsCap / s.g : 1;
   for (int32_t i = 0; i < S; ++i) {
     if (p.n_new[i] == 1) {
       add_row(p.q_start[i], p.ctx[i], p.block_start[i], fast_decode ? decode : generic);
+    } else if (fast_decode && p.n_new[i] <= kPackedRowsMax && p.ctx[i] <= split) {
+      // a short prompt chunk whose keys fit one decode unit: causal rows packed
+      // `pack` at a time into decode units (no tensor-core tile of 128 rows)
+      for (int32_t j = 0; j < p.n_new[i]; j += pack) {
+        const int32_t n = std::min(pack, p.n_new[i] - j);
+        for (int32_t h = 0; h < s.H_kv; ++h)
+          decode.push_back(WorkItem{p.q_start[i] + j, h, 0, p.seen[i] + j + n, -1,
+                                    p.block_start[i], n, p.seen[i] + j + 1});
+      }
+      max_splits = std::max(max_splits, 1);
+      pl.decode_packed = 1;
     } else if (fast_chunk) {
       // 128-row tiles; a tile's key range [0, last position + 1) is cut into
       // 64-key-aligned pieces of at most `chunk_split` keys, merged later by
@@ -453,6 +468,7 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     dp.n_parts = pl.n_parts;
     dp.num_blocks = p->cfg.num_blocks;
     dp.decode_grid = pl.decode_grid;
+    dp.decode_packed = pl.decode_packed;
   } else if (st != p->upload_stream) {
     cudaError_t e = cudaStreamWaitEvent(st, p->upload_ev, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
@@ -1010,6 +1026,7 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   dp.n_parts = c.max_parts;
   dp.num_blocks = cfg->num_blocks;
   dp.decode_grid = (int32_t)std::min<int64_t>(slots, c.max_decode_items);
+  dp.decode_packed = 1;   // any pass may be loaded: the variant that handles packed rows
   if (caps_out) *caps_out = c;
   *out = f.release();
   return RBKV_OK;

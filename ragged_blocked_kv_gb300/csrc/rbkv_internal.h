@@ -12,19 +12,24 @@ struct CUtensorMap_st;  // cuda.h's tensor-map type
 namespace rbkv {
 
 // One unit of split attention work: the keys [key_begin, key_end) of one
-// sequence's KV head, for one pass row (all query heads of the group).
-// part < 0: the unit covers all keys of the row; write O directly.
-// part >= 0: write the normalised partial output and its log-sum-exp to
-// partial slot `part` of the workspace.
+// sequence's KV head, for n_rows consecutive pass rows of that sequence (all
+// query heads of the group each).  Row i of the unit (pass row row + i) sees
+// the keys below min(key_end, diag + i): a decode row has n_rows = 1 and
+// diag = key_end; a short prompt chunk packs several causal rows.
+// part < 0: the unit covers all keys of its rows; write O directly.
+// part >= 0 (n_rows = 1 only): write the normalised partial output and its
+// log-sum-exp to partial slot `part` of the workspace.
 struct WorkItem {
-  int32_t row;        // pass row (index into Q / O)
+  int32_t row;        // first pass row (index into Q / O)
   int32_t kv_head;
   int32_t key_begin;
   int32_t key_end;
   int32_t part;
   int32_t table_off;  // offset of the sequence's block table in block_ids
+  int32_t n_rows;
+  int32_t diag;       // keys visible to the unit's first row
 };
-static_assert(sizeof(WorkItem) == 24, "WorkItem is 6 int32");
+static_assert(sizeof(WorkItem) == 32, "WorkItem is 8 int32");
 
 // (row, kv head) whose keys were split: partial slots [part_begin, part_begin+nsplit).
 struct CombineRow {
@@ -72,6 +77,7 @@ struct DevPass {
   int32_t n_parts;
   int32_t num_blocks;
   int32_t decode_grid;             // CTAs of the persistent decode launch
+  int32_t decode_packed;           // 1: some decode units pack several prompt rows
   // A frame (rbkv_frame_*): the launches are sized by the frame's capacities
   // (the counts above), and the loaded pass's own counts are read from this
   // device array {num_tokens, n_decode, n_generic, n_chunk, n_combine}.
@@ -114,6 +120,9 @@ constexpr int kDecodeTileKeys = 64;      // keys per pipeline stage of the decod
 constexpr int kChunkTileRows = 128;      // query rows per tensor-core tile
 constexpr int kChunkTileKeys = 128;      // keys per tensor-core KV tile
 constexpr int kChunkMinSplitKeys = 512;  // shortest automatic key split of prompt-chunk tiles
+constexpr int kPackedRowsMax = 16;       // prompt chunks of at most this many rows, whose
+                                         // keys fit one decode split, go to the decode kernel
+constexpr int kDecodeRowsCap = 8;        // query rows x heads of a decode unit, g <= 8
 
 bool decode_fast_supported(const ShapeInfo& s);
 // Persistent decode CTAs resident per SM for this shape (1 or 2).

@@ -83,7 +83,29 @@ def test_many_prompt_chunks_persistent_grid(rbkv, hq, hkv):
                                                            if sid >= 5000) + 64
     scn = workloads.Scenario("many", shape, budget, 0, hist, reqs, nb)
     (r,) = run_scenario(rbkv, scn)
-    assert r["plan"]["chunk_tiles"] * hq > 4 * 152
+    # chunks of up to 16 rows with short contexts run as packed decode units,
+    # the rest as tensor-core tiles: both paths carry many items
+    assert r["plan"]["chunk_tiles"] * hq > 152 and r["plan"]["decode_items"] > 152
+    _ok(r)
+    assert r["pair"].cache_equal()
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4), (16, 2), (32, 2)])
+def test_short_prompts_packed_decode_units(rbkv, hq, hkv):
+    """Prompt chunks of 2..16 rows with short contexts run on the decode kernel,
+    several causal rows per unit (8 / g of them): fresh prompts, chunks behind a
+    short cached prefix, next to plain decodes.  Every output against the oracle."""
+    rng = np.random.default_rng(hq + 100 * hkv)
+    shape = workloads.Shape(hq, hkv, 128, 64, "bf16", 1.0 / np.sqrt(128.0))
+    hist = [(100 + i, int(rng.integers(1, 300))) for i in range(24)]
+    reqs = [(100 + i, c + int(rng.integers(2, 17)), c) for i, (_, c) in enumerate(hist[:12])]
+    reqs += [(100 + i, c, c) for i, (_, c) in enumerate(hist[12:], start=12)]
+    reqs += [(900 + i, int(rng.integers(2, 17)), 0) for i in range(40)]
+    budget = sum(p - s if p > s else 1 for _, p, s in reqs)
+    nb = sum(-(-(c + 40) // 64) for _, c in hist) + 40 + 16
+    scn = workloads.Scenario("short", shape, budget, 0, hist, reqs, nb)
+    (r,) = run_scenario(rbkv, scn)
+    assert r["plan"]["chunk_tiles"] == 0            # every chunk took the decode kernel
     _ok(r)
     assert r["pair"].cache_equal()
 
