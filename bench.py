@@ -40,8 +40,8 @@ HBM_FALLBACK_GBS = 6800.0
 # summarised under profiles/, keyed by (workload, kernel) and valid only for
 # the kernel source they were taken on (sha256 prefix of its .cu file)
 TRAFFIC_BYTES = {
-    ("llama2_7b", "decode"): ("rbkv_decode.cu", "9aeb83c3161f", 614_349_056),
-    ("mistral_7b", "decode"): ("rbkv_decode.cu", "9aeb83c3161f", 9_181_267_776),
+    ("llama2_7b", "decode"): ("rbkv_decode.cu", "629256aa99b0", 614_156_288),
+    ("mistral_7b", "decode"): ("rbkv_decode.cu", "629256aa99b0", 9_177_342_016),
 }
 BF16_FALLBACK_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
@@ -713,7 +713,7 @@ def measure_profile(torch, rbkv, cfg, caches, ws, stack, stream, hs, tokens=PROF
             if graph:
                 # room for one tensor-core tile per prompt, whatever the mix
                 runner = GraphRunner(torch, rbkv, cfg, stack, caches, ws, hs, T,
-                                     max_chunk_tiles=-(-T // 128) + n + 8)
+                                     max_chunk_tiles=-(-T // 128) + n + 8, packed_units=1)
                 run = runner.run
             else:
                 def run(p):

@@ -337,7 +337,9 @@ typedef struct rbkv_frame rbkv_frame;
  *   max_chunk_tiles   ceil(max_tokens / 128) + max_seqs, at least ceil(SMs / num_heads_q)
  *   max_combine_rows  max_tokens x num_heads_kv
  *   max_parts         max_decode_items + max_tokens x num_heads_kv x
- *                     max(1, SMs / num_heads_q) */
+ *                     max(1, SMs / num_heads_q)
+ *   packed_units      0 (passes whose short prompt chunks run as packed decode
+ *                     units are refused with RBKV_ERR_UNSUPPORTED) */
 typedef struct {
   int32_t max_tokens;       /* rows of Q/K/V/O the frame's launches address */
   int32_t max_seqs;
@@ -346,6 +348,9 @@ typedef struct {
   int32_t max_chunk_tiles;
   int32_t max_combine_rows;
   int32_t max_parts;        /* partial-output slots of the workspace */
+  int32_t packed_units;     /* 1: passes may hold short prompt chunks packed into decode
+                               units (the decode variant with per-row limits runs for
+                               every pass); 0: such passes are refused */
 } rbkv_frame_caps;
 
 /* Create a frame on the current device for passes of `cfg` (device memory for

@@ -66,7 +66,7 @@ class _PlanInfo(C.Structure):
 class _FrameCaps(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "max_tokens", "max_seqs", "max_blocks", "max_decode_items", "max_chunk_tiles",
-        "max_combine_rows", "max_parts")]
+        "max_combine_rows", "max_parts", "packed_units")]
 
 
 # Every symbol include/rbkv.h declares, with (restype, argtypes).

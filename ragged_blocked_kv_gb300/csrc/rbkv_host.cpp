@@ -967,7 +967,7 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   rbkv_frame_caps c = *caps;
   if (c.max_tokens < 1) return fail(RBKV_ERR_INVALID, "max_tokens must be >= 1");
   if (c.max_seqs < 0 || c.max_blocks < 0 || c.max_decode_items < 0 || c.max_chunk_tiles < 0 ||
-      c.max_combine_rows < 0 || c.max_parts < 0)
+      c.max_combine_rows < 0 || c.max_parts < 0 || c.packed_units < 0 || c.packed_units > 1)
     return fail(RBKV_ERR_INVALID, "capacities must be >= 0");
   int dev = -1, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1026,7 +1026,7 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   dp.n_parts = c.max_parts;
   dp.num_blocks = cfg->num_blocks;
   dp.decode_grid = (int32_t)std::min<int64_t>(slots, c.max_decode_items);
-  dp.decode_packed = 1;   // any pass may be loaded: the variant that handles packed rows
+  dp.decode_packed = c.packed_units ? 1 : 0;
   if (caps_out) *caps_out = c;
   *out = f.release();
   return RBKV_OK;
@@ -1064,6 +1064,10 @@ rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
       return over("max_combine_rows", pl->combine.size(), c.max_combine_rows);
     if (pl->n_parts > c.max_parts) return over("max_parts", (size_t)pl->n_parts, c.max_parts);
     if (!pl->generic.empty()) return fail(RBKV_ERR_UNSUPPORTED, "pass has CUDA-core work items");
+    if (pl->decode_packed && !c.packed_units)
+      return fail(RBKV_ERR_UNSUPPORTED,
+                  "pass has short prompt chunks packed into decode units; the frame was "
+                  "created without packed_units");
     counts[kCountTokens] = (int32_t)p->slot.size();
     counts[kCountDecode] = (int32_t)pl->decode.size();
     counts[kCountChunk] = (int32_t)pl->chunk.size();

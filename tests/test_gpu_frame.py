@@ -174,3 +174,39 @@ def test_capacity_refusals(rbkv):
     assert e.value.status == -5
     with pytest.raises(rbkv.RbkvError):
         rbkv.Frame(cfg, 0)
+
+
+def test_frame_with_packed_short_prompts(rbkv):
+    """Short prompt chunks run as packed decode units: a frame refuses such a
+    pass unless created with packed_units=1, and then matches the plain path."""
+    shape = workloads.Shape(16, 4, 128, 64, "bf16", 1.0 / np.sqrt(128.0))
+    cfg = rbkv.Config(16, 4, 128, 64, "bf16", 256)
+    comp = rbkv.Composer(cfg)
+    hist = [(1, 300), (2, 40)]
+    comp.compose(340, 0, [(s, n, 0) for s, n in hist])
+    states = [(1, 300, 300), (2, 52, 40)] + [(10 + i, 3 + i, 0) for i in range(12)]
+    p = comp.compose(512, 0, states)
+    assert p.plan()["chunk_tiles"] == 0
+    T = p.num_tokens
+    dt = cfg.torch_dtype
+    kc = torch.zeros(cfg.cache_shape(), dtype=dt, device="cuda")
+    vc = torch.zeros_like(kc)
+    q, k, v = workloads.make_qkv(shape, T, 0, 3, device="cuda")
+    with pytest.raises(rbkv.RbkvError) as e:
+        rbkv.Frame(cfg, 256).load(p)
+    assert e.value.status == -5
+    frame = rbkv.Frame(cfg, 256, packed_units=1)
+    frame.load(p)
+    kb = torch.zeros(256, 4, 128, dtype=dt, device="cuda")
+    vb, qb = torch.zeros_like(kb), torch.zeros(256, 16, 128, dtype=dt, device="cuda")
+    ob = torch.zeros_like(qb)
+    qb[:T], kb[:T], vb[:T] = q, k, v
+    ws = torch.empty(frame.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    kc2, vc2 = kc.clone(), vc.clone()
+    frame.kv_append(kb, vb, kc2, vc2)
+    frame.attention(qb, kc2, vc2, ob, ws)
+    rbkv.kv_append(p, k, v, kc, vc)
+    oa = rbkv.ragged_attention(p, q, kc, vc)
+    torch.cuda.synchronize()
+    assert torch.equal(ob[:T], oa)
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
