@@ -311,23 +311,15 @@ class GpuRunner:
             self.inputs.append((q, kk, vv, self.o[:self.T[k]]))
         torch.cuda.synchronize()
 
-    def step(self, i, host=None):
-        """Pass i of the run (position i % cycle length).  With ``host`` =
-        (q_h, k_h, v_h, o_h) pinned tensors, Q/K/V are copied in and O out."""
+    def step(self, i):
+        """Pass i of the run (position i % cycle length), inputs in HBM."""
         rbkv = self.rbkv
         kpos = i % len(self.cycle)
         q, k, v, o = self.inputs[kpos]
         p = self.comp.compose(self.scn.budget, self.scn.max_chunk, self.cycle[kpos])
-        if host is not None:
-            q_h, k_h, v_h, o_h = host[kpos]
-            q.copy_(q_h, non_blocking=True)
-            k.copy_(k_h, non_blocking=True)
-            v.copy_(v_h, non_blocking=True)
         rbkv.kv_append(p, k, v, self.kc, self.vc, stream=self.h_stream)
         rbkv.ragged_attention(p, q, self.kc, self.vc, o=o, workspace=self.ws,
                               stream=self.h_stream)
-        if host is not None:
-            o_h.copy_(o, non_blocking=True)
         self.pending.append(p)
         if kpos == len(self.cycle) - 1:
             for pp in reversed(self.pending):
@@ -335,17 +327,30 @@ class GpuRunner:
             self.pending.clear()
         return self.T[kpos]
 
-    def run_e2e(self, first, count, host):
+    def run_e2e(self, first, count):
         """Passes first .. first+count-1 with Q/K/V copied in from pinned host
         memory and O copied back, pipelined the way a serving loop would: the
-        next pass's inputs are copied in on one copy stream while this pass
-        computes, and O goes back on another once its pass has finished.
-        Every copy is inside the caller's timed region (the last O copy is
-        waited for on the compute stream).  Returns the pass tokens."""
+        next pass's inputs (Q, K and V of a pass in one buffer, one copy) go in
+        on one copy stream while this pass computes, and O goes back on another
+        once its pass has finished.  Every copy is inside the caller's timed
+        region (the last O copy is waited for on the compute stream).  Returns
+        the pass tokens."""
         torch, rbkv = self.torch, self.rbkv
         n = len(self.cycle)
-        if not hasattr(self, "o_sets"):
-            self.o_sets = [torch.empty_like(o) for (_, _, _, o) in self.inputs]
+        if not hasattr(self, "e2e_sets"):
+            self.e2e_sets = []
+            for (q, k, v, o) in self.inputs:
+                parts = (q, k, v)
+                flat = torch.empty(sum(t.numel() for t in parts), dtype=q.dtype,
+                                   device=q.device)
+                views, off = [], 0
+                for t in parts:
+                    views.append(flat[off:off + t.numel()].view(t.shape))
+                    off += t.numel()
+                host_flat = torch.cat([t.reshape(-1) for t in parts]).cpu().pin_memory()
+                o_dev = torch.empty_like(o)
+                o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+                self.e2e_sets.append((flat, views, o_dev, host_flat, o_host))
             self.cs_in, self.cs_out = torch.cuda.Stream(), torch.cuda.Stream()
             self.ev_in = [torch.cuda.Event() for _ in range(n)]
             self.ev_done = [torch.cuda.Event() for _ in range(n)]
@@ -354,13 +359,10 @@ class GpuRunner:
 
         def copy_in(i):
             kpos = i % n
-            q, k, v, _ = self.inputs[kpos]
-            q_h, k_h, v_h, _ = host[kpos]
+            flat, _, _, host_flat, _ = self.e2e_sets[kpos]
             self.cs_in.wait_event(self.ev_done[kpos])     # the set's last pass is done
             with torch.cuda.stream(self.cs_in):
-                q.copy_(q_h, non_blocking=True)
-                k.copy_(k_h, non_blocking=True)
-                v.copy_(v_h, non_blocking=True)
+                flat.copy_(host_flat, non_blocking=True)
             self.ev_in[kpos].record(self.cs_in)
 
         tokens = 0
@@ -369,8 +371,7 @@ class GpuRunner:
             kpos = i % n
             if i + 1 < first + count:
                 copy_in(i + 1)
-            q, k, v, _ = self.inputs[kpos]
-            o = self.o_sets[kpos]
+            _, (q, k, v), o, _, o_host = self.e2e_sets[kpos]
             p = self.comp.compose(self.scn.budget, self.scn.max_chunk, self.cycle[kpos])
             comp.wait_event(self.ev_in[kpos])
             comp.wait_event(self.ev_out[kpos])              # O of the set copied out
@@ -380,7 +381,7 @@ class GpuRunner:
             self.ev_done[kpos].record(comp)
             self.cs_out.wait_event(self.ev_done[kpos])
             with torch.cuda.stream(self.cs_out):
-                host[kpos][3].copy_(o, non_blocking=True)
+                o_host.copy_(o, non_blocking=True)
             self.ev_out[kpos].record(self.cs_out)
             self.pending.append(p)
             if kpos == n - 1:
@@ -390,13 +391,6 @@ class GpuRunner:
             tokens += self.T[kpos]
         comp.wait_event(self.ev_out[(first + count - 1) % n])
         return tokens
-
-    def host_sets(self):
-        sets = []
-        for q, k, v, o in self.inputs:
-            sets.append((q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory(),
-                         self.torch.empty(o.shape, dtype=o.dtype).pin_memory()))
-        return sets
 
     def work_of(self, first, count):
         acc = {}
@@ -477,8 +471,7 @@ def run_ours(args, rank, world, local_rank):
     prof_work = run.work_of(prof_first, P)
 
     # ---- e2e: the same passes through the same calls, host buffers ------
-    host = run.host_sets()
-    run.run_e2e(i, ncyc, host)
+    run.run_e2e(i, ncyc)
     i += ncyc
     torch.cuda.synchronize()
     barrier()
@@ -487,7 +480,7 @@ def run_ours(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     e2e_first = i
     e0.record(run.stream)
-    e2e_tokens = run.run_e2e(i, K, host)
+    e2e_tokens = run.run_e2e(i, K)
     i += K
     e1.record(run.stream)
     torch.cuda.synchronize()
