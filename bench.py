@@ -41,8 +41,8 @@ HBM_FALLBACK_GBS = 6800.0
 # summarised under profiles/, keyed by (workload, kernel) and valid only for
 # the kernel source they were taken on (sha256 prefix of its .cu file)
 TRAFFIC_BYTES = {
-    ("llama2_7b", "decode"): ("rbkv_decode.cu", "629256aa99b0", 614_156_288),
-    ("mistral_7b", "decode"): ("rbkv_decode.cu", "629256aa99b0", 9_177_342_016),
+    ("llama2_7b", "decode"): ("rbkv_decode.cu", "4af2001551f6", 614_156_288),
+    ("mistral_7b", "decode"): ("rbkv_decode.cu", "4af2001551f6", 9_177_342_016),
 }
 BF16_FALLBACK_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024

@@ -104,13 +104,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                           float* __restrict__ part_o, float* __restrict__ part_lse,
                           int wait_first) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // The kernel may run beside the prompt-chunk kernel that precedes it (it
-  // reads only the cache, Q and the pass metadata, and writes rows and
-  // partial slots the chunk kernel does not; the chunk kernel lets it start
-  // only once everything before the chunk kernel has finished).  With any
-  // other predecessor (`wait_first`) it waits for it before anything else.
-  // It lets the combine kernel launch early, and waits for its predecessor
-  // before ending, so that its completion covers both attention kernels.
+  // The kernel runs first among a pass's attention kernels.  With
+  // `wait_first` it waits for its predecessor (the cache append) before any
+  // global access, and only then lets the next kernel (prompt chunks, or the
+  // combine) launch: that kernel may then read the cache without a wait of
+  // its own.  It waits for its predecessor again before ending (needed when
+  // it was launched without `wait_first`), so that its completion covers it.
   if (wait_first) ptx::pdl_wait_previous();
   ptx::pdl_launch_dependents();
   const int rcap = rows_cap_for(shp.g, kPacked);
