@@ -5,22 +5,24 @@
 // p attends keys 0..p of its sequence: the cached prefix read through the
 // block table plus the chunk's own earlier rows (causal within the chunk).
 //
-// One CTA owns 128 consecutive rows of one chunk for one query head:
-//  - warp 4 (TMA): loads the 128x128 Q tile once and streams 64-key K and V
-//    tiles of the paged cache into a 4-stage ring (128-byte swizzle);
-//  - warp 5 (MMA): allocates 256 TMEM columns; one thread issues
-//    S = Q K^T (M=128, N=64, K=128) into one of two TMEM S buffers and
-//    O += P V (M=128, N=128, K=64) into the TMEM O accumulator, and signals
-//    completion with tcgen05.commit;
-//  - warps 0-3 (softmax): thread i owns query row i = TMEM lane i; it reads its
-//    64 scores with tcgen05.ld, masks causally, keeps a running max that is
+// Work items are (128 consecutive rows of one chunk, one query head) pairs; a
+// persistent grid of at most one CTA per SM walks them (longest first, snake
+// order), with barrier phases, the K/V ring and the S buffers continuing from
+// item to item and tensor memory allocated once:
+//  - warp 4 (TMA): streams 128-key K and V tiles of the paged cache into a
+//    3-stage ring (128-byte swizzle), looking block ids up a tile ahead;
+//  - warp 5 (MMA): allocates 512 TMEM columns; one thread issues
+//    S = Q K^T (M=128, N=128, K=128; Q in TMEM) into one of two TMEM S buffers
+//    and O += P V (M=128, N=128, K=128; P in TMEM) into the TMEM O
+//    accumulator, and signals completion with tcgen05.commit;
+//  - warps 0-3 (softmax): thread i owns query row i = TMEM lane i; it writes
+//    its row of Q into TMEM at the start of an item, reads its 128 scores with
+//    tcgen05.ld (two halves), masks causally, keeps a running max that is
 //    raised only when a row's max grows by more than 2^8 (the accumulator in
-//    TMEM is then rescaled in place), writes P as bf16 into shared memory in
-//    the MMA operand layout, and finally normalises O and stores it.
-// P is double-buffered, so the softmax of tile j+1 waits only for the PV of
-// tile j-1 (and for the PV of tile j only when it must rescale O); QK^T of the
-// next tile is queued on the tensor pipe before each PV.  One CTA per SM
-// (about 192 KB of shared memory, 256 TMEM columns).
+//    TMEM is then rescaled in place), writes P as bf16 pairs over the S
+//    columns it has read, and finally normalises O and stores it.
+// The QK^T of the next tile is queued on the tensor pipe before each PV, so it
+// overlaps the softmax of the current one.  About 192 KB of shared memory.
 // Every wait is bounded; on timeout the kernel records RBKV_ERR_TIMEOUT, lets
 // its copies and MMAs drain (bounded), frees its TMEM and returns.
 #include <algorithm>
