@@ -355,3 +355,24 @@ def test_budget_for_latency_random_bit_exact(rbkv, seed):
             assert oracle.latency_at(tok, lat, a) <= L
             if a < tok[-1]:
                 assert oracle.latency_at(tok, lat, a + 1) > L
+
+
+def test_planner_packs_short_prompt_chunks(rbkv):
+    """Prompt chunks of at most 16 rows whose keys fit one decode split become
+    decode units holding 8 / g consecutive rows each; longer chunks, or short
+    ones behind a long prefix, stay tensor-core tiles (CPU-side plan only)."""
+    for hq, hkv in [(8, 8), (16, 4), (16, 2), (32, 2)]:
+        g = hq // hkv
+        pack = 8 // g if g <= 8 else 1
+        c = rbkv.Composer(rbkv.Config(hq, hkv, 128, 64, "bf16", 4096))
+        c.compose(20000, 0, [(1, 12000, 0)])                  # a long cached prefix
+        states = [(1, 12010, 12000)]                           # 10 rows behind 12000 keys
+        states += [(10 + i, n, 0) for i, n in enumerate([2, 5, 16, 17, 300])]
+        p = c.compose(100000, 0, states)
+        info = p.plan_for_sms(152)
+        packed_rows = [2, 5, 16]
+        want_items = sum(-(-n // pack) for n in packed_rows) * hkv
+        assert info["decode_items"] == want_items, (hq, hkv, info)
+        # tiles: the 10-row chunk behind the prefix, 17 rows, 300 rows (3 tiles)
+        assert info["chunk_tiles"] >= 1 + 1 + 3
+        assert info["decode_rows"] == 0
