@@ -27,8 +27,9 @@ Pins (tests marked ``not gpu``): the tiny configuration's worked pass, budget
 and conservation invariants, brute force on tiny inputs, closed forms,
 PyTorch's scaled-dot-product attention as an independent library special case,
 split invariance and chunk invariance.  Block ids follow a stated rule (lowest
-free id first, in layout order) that the pages do not fix: parity of block ids
-is pinned only by that rule.
+free id first, in layout order) that the pages do not fix: for the choice of
+block ids, parity unpinned (only that rule and the pool invariants - distinct
+ids, ceil(ctx / B) held per sequence, all-or-nothing - hold them).
 """
 from .composer import Composer, PassMeta, InvalidRequest, NoBlocks, budget_for_latency, latency_at  # noqa: F401
 from .cache import BlockedCache, kv_append  # noqa: F401
