@@ -27,9 +27,12 @@ import argparse
 import json
 import math
 import os
+import resource
+import shutil
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +79,10 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-offset", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-core", type=int, default=-1, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-barrier", default="", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-world", type=int, default=1, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -557,6 +564,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess(args)
+        rss = resource.getrusage(resource.RUSAGE_CHILDREN).ru_maxrss * 1024
+        line["cpu_baseline"]["all_cores"] = cpu_all_cores(args, rss)
     print(json.dumps(line), flush=True)
 
 
@@ -980,7 +989,7 @@ class OracleRunner:
     head of the cycle is covered in turn.  A token counts as 1/H_q per output
     pair computed."""
 
-    def __init__(self, scn, seed):
+    def __init__(self, scn, seed, offset=0):
         import numpy as np
         import oracle
         import workloads
@@ -1005,7 +1014,7 @@ class OracleRunner:
             self.inputs.append((self._st(q), self._st(kk), self._st(vv)))
         self.pending = []
         self.i = 0
-        self.cursor = 0      # next (row * H_q + head) to compute, per pass
+        self.cursor = offset  # next (row * H_q + head) to compute, per pass
 
     def _st(self, t):
         import torch
@@ -1083,10 +1092,27 @@ class OracleTraceRunner:
                                  max_passes=steps)
 
 
-def oracle_measure(workload, seed, steps, warmup, pair_budget=2000):
+def _barrier(path, world, limit_s=300.0):
+    """File barrier between ``world`` concurrent oracle workers: announce this
+    one, then wait (at most ``limit_s``) until all have.  Returns whether all
+    arrived."""
+    fd, _ = tempfile.mkstemp(dir=path, prefix="ready")
+    os.close(fd)
+    end = time.monotonic() + limit_s
+    while time.monotonic() < end:
+        if sum(1 for f in os.listdir(path) if f.startswith("ready")) >= world:
+            return True
+        time.sleep(0.01)
+    return False
+
+
+def oracle_measure(workload, seed, steps, warmup, pair_budget=2000, offset=0, barrier="",
+                   world=1):
     """Time ``steps`` oracle steps after ``warmup``; each step computes
     max(1, pair_budget // (steps + warmup)) output pairs, so the whole run
-    stays within a few minutes whatever the step count."""
+    stays within a few minutes whatever the step count.  ``offset`` moves the
+    first output pair (concurrent workers cover disjoint pairs); with
+    ``barrier`` the timed region starts once ``world`` workers are ready."""
     import workloads
     pairs = max(1, pair_budget // max(1, steps + warmup))
     if workload == "trace":
@@ -1106,17 +1132,20 @@ def oracle_measure(workload, seed, steps, warmup, pair_budget=2000):
                 "setup_seconds": setup}
     scn = workloads.SCENARIOS[workload](seed)
     t0 = time.perf_counter()
-    r = OracleRunner(scn, seed)
+    r = OracleRunner(scn, seed, offset * pairs * (steps + warmup))
     setup = time.perf_counter() - t0
     for _ in range(warmup):
         r.step(pairs)
+    synced = _barrier(barrier, world) if barrier else True
+    wall0 = time.time()
     t0 = time.perf_counter()
     tokens = 0.0
     for _ in range(steps):
         tokens += r.step(pairs)
     dt = time.perf_counter() - t0
     return {"value": tokens / dt, "tokens": tokens, "pairs_per_step": pairs, "seconds": dt,
-            "setup_seconds": setup}
+            "setup_seconds": setup, "wall_start": wall0, "wall_end": wall0 + dt,
+            "synced": synced}
 
 
 def cpu_env():
@@ -1141,6 +1170,58 @@ def cpu_baseline_subprocess(args, steps=5, warmup=1):
                       f"appends the whole pass and computes {res['pairs_per_step']} (row, head) "
                       f"outputs ({res['tokens']:.1f} tokens in {res['seconds']:.1f} s; a token "
                       "counts 1/H_q per output); one thread (BLAS threads = 1)"}
+
+
+def _mem_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def cpu_all_cores(args, worker_bytes, steps=5, warmup=1):
+    """The same oracle sample on every host core at once: one single-threaded
+    worker per core (as many as half the free memory holds, ``worker_bytes``
+    each), each on its own output pairs, all starting their timed steps
+    together.  Throughput = all workers' tokens / (last end - first start)."""
+    cores = sorted(os.sched_getaffinity(0))
+    n = len(cores)
+    if worker_bytes > 0:
+        n = max(1, min(n, int(_mem_available() * 0.5 // worker_bytes)))
+    tmp = tempfile.mkdtemp(prefix="rbkv_oracle_")
+    procs = []
+    try:
+        for w in range(n):
+            cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload",
+                   args.workload, "--seed", str(args.seed), "--steps", str(steps), "--warmup",
+                   str(warmup), "--cpu-offset", str(w), "--cpu-core", str(cores[w]),
+                   "--cpu-barrier", tmp, "--cpu-world", str(n)]
+            procs.append(subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                          stderr=subprocess.DEVNULL, text=True, env=cpu_env()))
+        res = []
+        for p in procs:
+            out, _ = p.communicate(timeout=900)
+            res.append(json.loads(out.strip().splitlines()[-1]))
+    except Exception as e:  # reported, not fatal
+        for p in procs:
+            if p.poll() is None:
+                p.kill()
+                p.wait()
+        return {"value": None, "cores": n, "sample": f"failed: {e}"}
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    tokens = sum(r["tokens"] for r in res)
+    span = max(r["wall_end"] for r in res) - min(r["wall_start"] for r in res)
+    room = "" if n == len(cores) else f" (the free memory holds {n} of {len(cores)} cores' workers)"
+    return {"value": tokens / span, "cores": n,
+            "synced": all(r["synced"] for r in res),
+            "sample": f"{n} single-threaded oracle worker(s), one per core{room}, each the 1-core "
+                      f"sample on its own output pairs ({tokens:.1f} tokens in {span:.1f} s of wall "
+                      "time from the first start to the last end)"}
 
 
 def run_reference(args, rank):
@@ -1189,7 +1270,11 @@ def run_reference(args, rank):
 def main():
     args = parse_args()
     if args.cpu_worker:
-        res = oracle_measure(args.workload, args.seed, args.steps, args.warmup)
+        if args.cpu_core >= 0:
+            os.sched_setaffinity(0, {args.cpu_core})
+        res = oracle_measure(args.workload, args.seed, args.steps, args.warmup,
+                             offset=args.cpu_offset, barrier=args.cpu_barrier,
+                             world=args.cpu_world)
         print(json.dumps(res), flush=True)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
