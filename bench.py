@@ -1156,9 +1156,29 @@ def cpu_env():
     return env
 
 
+def cpu_model():
+    """The host CPU's model name (x86), or its architecture and part number (Arm)."""
+    import platform
+    part = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key, _, val = ln.partition(":")
+                key = key.strip()
+                if key == "model name":
+                    return val.strip()
+                if key == "CPU part" and not part:
+                    part = val.strip()
+    except OSError:
+        pass
+    return f"{platform.machine()} (CPU part {part})" if part else platform.machine()
+
+
 def cpu_baseline_subprocess(args, steps=5, warmup=1):
+    core = min(os.sched_getaffinity(0))
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload", args.workload,
-           "--seed", str(args.seed), "--steps", str(steps), "--warmup", str(warmup)]
+           "--seed", str(args.seed), "--steps", str(steps), "--warmup", str(warmup),
+           "--cpu-core", str(core)]
     try:
         out = subprocess.run(cmd, capture_output=True, text=True, env=cpu_env(), timeout=600)
         res = json.loads(out.stdout.strip().splitlines()[-1])
@@ -1169,7 +1189,8 @@ def cpu_baseline_subprocess(args, steps=5, warmup=1):
             "sample": f"{steps} passes after {warmup} warm-up; per pass the oracle composes and "
                       f"appends the whole pass and computes {res['pairs_per_step']} (row, head) "
                       f"outputs ({res['tokens']:.1f} tokens in {res['seconds']:.1f} s; a token "
-                      "counts 1/H_q per output); one thread (BLAS threads = 1)"}
+                      "counts 1/H_q per output); one thread (BLAS threads = 1) pinned to one core",
+            "cpu": cpu_model()}
 
 
 def _mem_available():
@@ -1261,7 +1282,8 @@ def run_reference(args, rank):
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"per pass: whole-pass composition and append, then "
                                    f"{res['pairs_per_step']} (row, head) outputs; a token counts "
-                                   "1/H_q per output; one thread (BLAS threads = 1)"},
+                                   "1/H_q per output; one thread (BLAS threads = 1)",
+                         "cpu": cpu_model()},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -1284,7 +1306,7 @@ def main():
         if rank == 0:
             # the oracle needs no GPU; run it with BLAS threads pinned to one
             for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-                os.environ.setdefault(v, "1")
+                os.environ[v] = "1"
             run_reference(args, rank)
         return
     import torch
