@@ -8,7 +8,7 @@
  *
  *   DeepSpeed-FastGen paper summary page, "Summary" and idea I3: every forward
  *     pass holds a fixed token budget; long prompts are cut into chunks over
- *     several passes, short prompts and generation tokens fill it up.
+ *     several passes, and decode tokens and small prompts take the rest.
  *   FastGen guide, "Paged KV Memory Management": the cache is non-contiguous
  *     fixed-size blocks reached through block tables, read directly by the
  *     attention kernels.
@@ -308,7 +308,7 @@ rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_str
 
 /* ---- frames: one fixed launch sequence for every pass (CUDA graphs) ---------
  *
- * Dynamic SplitFuse keeps every forward pass at about the same size (paper
+ * Under Dynamic SplitFuse the passes all have roughly one size (paper
  * summary page, Summary and idea I3; InfoQ release note: passes of a steady
  * size), so a serving loop can record the launches of one pass once, as a
  * CUDA graph, and replay them for every later pass.  A frame makes that
