@@ -1,6 +1,6 @@
 """User-facing serving metrics of a closed-loop trace of SplitFuse passes.
 
-Source: DeepSpeed-FastGen paper summary page, Key points and idea I4 - judge a
+Source: DeepSpeed-FastGen paper summary page, Key points and idea I4 - rate a
 chat service by an "effective throughput" tied to time to first token (TTFT)
 and how regularly the following tokens arrive, and report token-level tail
 latency; the FastGen guide's benchmark table reports TTFT P90, per-token P99
