@@ -1,5 +1,6 @@
-"""Host-side timing of the oracle baseline: the start barrier of the
-concurrent workers and the all-cores aggregate (CPU only)."""
+"""Host-side helpers of the benchmark (CPU only): the oracle baseline's start
+barrier and all-cores aggregate, and the rule that recorded DRAM traffic is
+reported only for the kernel source it was captured on."""
 import os
 import types
 
@@ -34,3 +35,23 @@ def test_offset_moves_the_first_output_pair():
     a.step(5)
     b.step(5)
     assert (a.cursor, b.cursor) == (5, 12)
+
+
+def test_traffic_is_reported_only_for_the_captured_source(monkeypatch):
+    import hashlib
+    path = os.path.join(bench.ROOT, "ragged_blocked_kv_gb300", "csrc", "rbkv_decode.cu")
+    with open(path, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:12]
+    monkeypatch.setattr(bench, "TRAFFIC_BYTES", {
+        ("w", "decode"): ("rbkv_decode.cu", sha, 123),
+        ("w", "stale"): ("rbkv_decode.cu", "000000000000", 456),
+        ("w", "missing"): ("no_such_file.cu", sha, 789),
+    })
+    assert bench.traffic_bytes("w", "decode") == 123
+    assert bench.traffic_bytes("w", "stale") is None
+    assert bench.traffic_bytes("w", "missing") is None
+    assert bench.traffic_bytes("other", "decode") is None
+
+
+def test_cpu_model_is_named():
+    assert bench.cpu_model()
