@@ -240,3 +240,44 @@ def test_closed_loop_trace_every_pass(rbkv):
             _ok(r)
     assert pair.cache_equal()
     assert pair.lib.free_blocks() == nb
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_mixed_passes(rbkv, seed):
+    """Seeded random passes: a random group shape and block size, decodes with
+    log-uniform contexts (1 … 4000 keys), fresh prompts and prompts behind a
+    cached prefix, a random budget and chunk cap; three passes with states
+    advanced between them, every output against the oracle and the whole
+    cache bit-exact at the end."""
+    rng = np.random.default_rng(1000 + seed)
+    hq, hkv, B = [(8, 2, 64), (16, 2, 64), (8, 8, 16), (32, 4, 64), (16, 1, 64),
+                  (8, 2, 32)][seed]
+    shape = workloads.Shape(hq, hkv, 128, B, "bf16", 1.0 / np.sqrt(128.0))
+    hist, reqs = [], []
+    sid = 100
+    for _ in range(int(rng.integers(1, 24))):           # decodes
+        c = int(np.exp(rng.uniform(0.0, np.log(4000.0))))
+        hist.append((sid, c))
+        reqs.append((sid, c, c))
+        sid += 1
+    for _ in range(int(rng.integers(0, 4))):            # prompts behind a cached prefix
+        s0 = int(rng.integers(1, 2000))
+        hist.append((sid, s0))
+        reqs.append((sid, s0 + int(rng.integers(1, 600)), s0))
+        sid += 1
+    for _ in range(int(rng.integers(0, 5))):            # fresh prompts
+        reqs.append((sid, int(rng.integers(1, 700)), 0))
+        sid += 1
+    order = rng.permutation(len(reqs))
+    reqs = [reqs[i] for i in order]
+    budget = int(rng.integers(32, 1025))
+    cap = int(rng.choice([0, 16, 100, 512]))
+    nb = sum(-(-(pl + 3) // B) for _, pl, _ in reqs) + 8
+    scn = workloads.Scenario("random", shape, budget, cap, hist, reqs, nb)
+    res = run_scenario(rbkv, scn, passes=3)
+    for r in res:
+        if r["tokens"]:
+            _ok(r)
+        else:
+            assert r["meta_equal"]
+    assert res[-1]["pair"].cache_equal()
