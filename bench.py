@@ -1,16 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the ragged SplitFuse attention pass (one pass per step).
 
-Workload (default): the Llama-2-7B attention shape - 32 query heads, 32 KV
-heads, head_dim 128, bf16, KV block 64, token budget 512, chunk cap 512.  A
-4096-token prompt is carried through 9 passes (8 chunks of 497 tokens and one
-of 120) next to 15 decode sequences whose contexts are round(N(2600, 780^2))
-clipped to [64, 8192] and grow by one token per pass.  After the 9th pass the
-cycle's passes are rolled back on the composer, so every cycle is the same 9
-passes (the decodes return to their starting contexts, the prompt starts
-again).  A step is one whole pass of the hot path: host composition and block
-allocation, the metadata upload, kv_append and ragged attention (tensor-core
-chunk tiles, split-KV decode, log-sum-exp combine).
+Workload (default, ``--workload mistral_7b``): the Mistral-7B attention
+shape - 32 query heads, 8 KV heads, head_dim 128, bf16, KV block 64, token
+budget 2048, chunk cap 768.  Each pass holds two 768-token prompt chunks (one
+at the start of a 2304-token prompt, one behind a 1536-token cached prefix)
+and 512 decode tokens whose contexts are uniform in [128, 8192]: about 9 GB of
+KV read per pass, the largest pass of the workloads.  After each pass it is
+rolled back on the composer, so every step is the same pass.  A step is one
+whole pass of the hot path: host composition and block allocation, the
+metadata upload, kv_append and ragged attention (tensor-core chunk tiles,
+split-KV decode, log-sum-exp combine).
+
+``--workload llama2_7b``: 32/32 heads, budget 512, chunk cap 512; a 4096-token
+prompt is carried through 9 passes (8 chunks of 497 tokens and one of 120)
+next to 15 decode sequences (contexts round(N(2600, 780^2)) clipped to [64,
+8192], one more token per pass); the 9 passes form a cycle that is rolled back
+and repeated.  ``--workload decode_stress``: 64/8 heads, 64 decodes with
+contexts log-uniform in [512, 16000].
 
 Output: one JSON line (rank 0).  ``value`` is pass tokens per second with
 inputs already resident in HBM; ``e2e`` is the same through the same calls with
@@ -58,7 +65,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3600)
     ap.add_argument("--warmup", type=int, default=90)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama2_7b",
+    ap.add_argument("--workload", default="mistral_7b",
                     choices=["llama2_7b", "decode_stress", "mistral_7b", "trace", "profile"])
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per pass (trace and profile workloads)")
@@ -113,6 +120,15 @@ def cycle_states(scn, compose, rollback):
     return out, metas
 
 
+def workload_label(scn, ncyc):
+    """The ``config.workload`` string, the same in both arms."""
+    sh = scn.shape
+    return (f"{scn.name}: {sh.num_heads_q}q/{sh.num_heads_kv}kv heads, head_dim {sh.head_dim}, "
+            f"block {sh.block_size}, budget {scn.budget}, chunk cap {scn.max_chunk}; a cycle of "
+            f"{ncyc} pass{'es' if ncyc != 1 else ''} repeated (rolled back on the composer after "
+            "each cycle)")
+
+
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
@@ -147,20 +163,71 @@ def read_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    """SM clocks and throttle reasons sampled while timing (read-only queries).
 
+    A thread reads the GPU's SM clock and its clock-event reasons through NVML
+    (libnvidia-ml, the library nvidia-smi uses) every 5 ms, so that even a
+    timed region of a few tens of milliseconds has samples inside it; without
+    NVML it falls back to ``nvidia-smi -lms 50``.  ``stop(t0, t1)`` reports the
+    samples between wall-clock times t0 and t1, or, when none landed there,
+    the nearest sample on each side of the region (``"window": "bracketing"``)."""
+
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid: str = ""):
         self.gpu = gpu_index
+        self.uuid = uuid
         self.proc = None
         self.path = None
+        self.thread = None
+        self.samples = []      # (wall time, sm MHz, max sm MHz, reason bits)
+        self.source = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.gpu, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        return lib, h
 
     def start(self):
+        import threading
         try:
-            import tempfile
+            import ctypes
+            lib, h = self._nvml()
+            self.stop_evt = threading.Event()
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+            def run():
+                clk = ctypes.c_uint()
+                rs = ctypes.c_ulonglong()
+                while not self.stop_evt.is_set():
+                    t = time.time()
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                        bits = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                        self.samples.append((t, float(clk.value), float(mx.value), int(bits)))
+                    self.stop_evt.wait(0.005)
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            self.source = "nvml, 5 ms"
+            return
+        except Exception:
+            self.thread = None
+        try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
@@ -168,23 +235,18 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi, 50 ms"
         except Exception:
             self.proc = None
 
-    def stop(self, t0=None, t1=None):
-        """Median SM clock and the throttle reasons seen between wall-clock
-        times t0 and t1 (all samples when not given)."""
-        if self.proc is None:
-            return None
+    def _read_smi(self):
+        import datetime
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.fh.close()
-        import datetime
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
@@ -195,18 +257,43 @@ class ClockSampler:
                     clk, cmax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                if t0 is not None and not (t0 <= ts <= t1):
-                    continue
-                sm.append(clk)
-                mx.append(cmax)
-                for n, v in zip(names, parts[6:10]):
+                bits = 0
+                for n, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                 "sw_power_cap"), parts[6:10]):
                     if v.lower().startswith("active"):
-                        reasons.add(n)
+                        bits |= self.REASON_BITS[n]
+                self.samples.append((ts, clk, cmax, bits))
         os.unlink(self.path)
-        if not sm:
+
+    def stop(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen between wall-clock
+        times t0 and t1 (all samples when not given)."""
+        if self.thread is not None:
+            self.stop_evt.set()
+            self.thread.join(timeout=5)
+        elif self.proc is not None:
+            self._read_smi()
+        else:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        smp = sorted(self.samples)
+        if not smp:
+            return None
+        window = "timed region"
+        if t0 is None:
+            sel = smp
+        else:
+            sel = [x for x in smp if t0 <= x[0] <= t1]
+            if not sel:
+                before = [x for x in smp if x[0] < t0][-1:]
+                after = [x for x in smp if x[0] > t1][:1]
+                sel = before + after
+                window = "bracketing (no sample inside the timed region)"
+        if not sel:
+            return None
+        reasons = sorted(n for n, b in self.REASON_BITS.items() if any(x[3] & b for x in sel))
+        return {"sm_mhz": statistics.median(x[1] for x in sel),
+                "sm_max_mhz": max(x[2] for x in sel), "samples": len(sel),
+                "reasons": reasons, "window": window, "source": self.source}
 
 
 def over_ranks(times, counts, world, device="cpu"):
@@ -438,7 +525,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     # ---- timed region: K passes, inputs resident in HBM -----------------
-    clocks = ClockSampler(local_rank)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        uuid = ""
+    clocks = ClockSampler(local_rank, uuid)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
@@ -513,8 +604,9 @@ def run_ours(args, rank, world, local_rank):
     dom_ms, dom_n = kinds[dom]
     avg_s = dom_ms / dom_n / 1e3
     if dom == "chunk":
+        # each launch is timed on its own (events around it): the burst peak
         per_launch = prof_work["chunk_flops"] / dom_n
-        roof = {"bound": "tensor", "achieved": per_launch / avg_s / 1e12, "peak": bf16_sus,
+        roof = {"bound": "tensor", "achieved": per_launch / avg_s / 1e12, "peak": bf16,
                 "unit": "TFLOP/s"}
     else:
         key = {"decode": "decode_bytes", "generic": "kv_read_bytes",
@@ -542,19 +634,17 @@ def run_ours(args, rank, world, local_rank):
         "dtype": sh.dtype,
         "data": "synthetic",
         "config": {
-            "workload": f"{scn.name}: {sh.num_heads_q}q/{sh.num_heads_kv}kv heads, head_dim "
-                        f"{sh.head_dim}, block {sh.block_size}, budget {scn.budget}, chunk cap "
-                        f"{scn.max_chunk}; a cycle of {ncyc} passes repeated (rolled back "
-                        "on the composer after each cycle)",
+            "workload": workload_label(scn, ncyc),
             "tokens_per_step": tot_tokens / K / world,
             "kv_read_gb_per_step": work["kv_read_bytes"] / K / 1e9,
             "kv_read_gbs": work["kv_read_bytes"] / (ms / 1e3) / 1e9,
             "kv_read_frac_of_hbm": work["kv_read_bytes"] / (ms / 1e3) / 1e9 / hbm,
+            "kv_read_frac_target": 0.70,
             "chunk_tflops": prof_work["chunk_flops"] / (kinds.get("chunk", (1e30, 1))[0] / 1e3) / 1e12,
-            # the chunk kernel's causal flops over its own launch time, against the
-            # sustained bf16 dense peak (it runs inside a long stream of passes)
+            # the chunk kernel's causal flops over its own launch time (each launch
+            # timed alone, between events), against the measured burst bf16 peak
             "chunk_frac_of_bf16_peak": prof_work["chunk_flops"]
-            / (kinds.get("chunk", (1e30, 1))[0] / 1e3) / 1e12 / bf16_sus,
+            / (kinds.get("chunk", (1e30, 1))[0] / 1e3) / 1e12 / bf16,
             "l2": "inputs larger than L2 (each pass reads "
                   f"{work['kv_read_bytes'] / K / 1e6:.0f} MB of KV > 129 MB L2); no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -807,7 +897,11 @@ def run_profile_bench(args, rank, world, local_rank):
     Decoupling")."""
     torch, rbkv, workloads, reqs, cfg, caches, ws, stack, stream, hs = _trace_setup(
         args, rank, world, local_rank, max(PROFILE_TOKENS))
-    clocks = ClockSampler(local_rank)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        uuid = ""
+    clocks = ClockSampler(local_rank, uuid)
     clocks.start()
     time.sleep(0.3)
     w0 = time.time()
@@ -905,7 +999,11 @@ def run_trace_bench(args, rank, world, local_rank):
     drive(warm, rbkv.Composer(cfg), False)
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local_rank)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        uuid = ""
+    clocks = ClockSampler(local_rank, uuid)
     clocks.start()
     time.sleep(0.5)
     comp = rbkv.Composer(cfg)
@@ -1151,7 +1249,7 @@ def oracle_measure(workload, seed, steps, warmup, pair_budget=2000, offset=0, ba
     dt = time.perf_counter() - t0
     return {"value": tokens / dt, "tokens": tokens, "pairs_per_step": pairs, "seconds": dt,
             "setup_seconds": setup, "wall_start": wall0, "wall_end": wall0 + dt,
-            "synced": synced}
+            "synced": synced, "cycle": len(r.cycle)}
 
 
 def cpu_env():
@@ -1282,9 +1380,9 @@ def run_reference(args, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{scn.name}: {sh.num_heads_q}q/{sh.num_heads_kv}kv heads, head_dim "
-                               f"{sh.head_dim}, block {sh.block_size}, budget {scn.budget}, chunk "
-                               f"cap {scn.max_chunk}"},
+        "config": {"workload": workload_label(scn, res.get("cycle", 1))
+                   if args.workload != "trace" else "trace: 512 requests, 32 clients, "
+                   "Llama-2-7B attention shape, budget 512, chunk cap 512 (one layer)"},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"per pass: whole-pass composition and append, then "
                                    f"{res['pairs_per_step']} (row, head) outputs; a token counts "

@@ -223,8 +223,9 @@ rbkv_status rbkv_pass_get_plan(rbkv_pass* p, rbkv_plan_info* info);
  * pass's own plan is not changed).  For inspecting the split planner. */
 rbkv_status rbkv_pass_plan_for_sms(const rbkv_pass* p, int32_t num_sms, rbkv_plan_info* info);
 
-/* Free a pass.  Its device metadata is released in stream order after the last
- * work launched with it, so the last stream it was used on must still exist. */
+/* Free a pass.  Its device metadata is released in stream order after the
+ * work launched with it on every stream it was used on (the last of them waits
+ * for the others), so all those streams must still exist. */
 void rbkv_pass_destroy(rbkv_pass* p);
 
 /* ---- device steps ---------------------------------------------------------- */
@@ -272,7 +273,11 @@ rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cac
  *  - A pass whose scratch need (rbkv_attention_workspace_bytes) exceeds
  *    16 MiB is rejected with RBKV_ERR_WORKSPACE.
  *  - The first call on a device looks up the array's device address for that
- *    device; make that first call before any stream capture.
+ *    device; make that first call before any stream capture.  The address is
+ *    kept for the life of the process: after cudaDeviceReset (or anything else
+ *    that tears down the device's context) the library's module may load at
+ *    another address, so this entry point must not be used on that device
+ *    again in the same process.
  *  - All calls share the one array: calls whose kernels overlap on the GPU
  *    race on it.  Order them on one stream (or with events).
  * Calls no cudaMalloc, cudaFree or other allocating routine. */

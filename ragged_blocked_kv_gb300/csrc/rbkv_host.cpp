@@ -200,8 +200,13 @@ struct rbkv_pass {
   size_t dev_bytes = 0;
   cudaStream_t upload_stream = nullptr;
   cudaStream_t last_stream = nullptr;
+  std::vector<cudaStream_t> streams;   // every stream device work of the pass was put on
   cudaEvent_t upload_ev = nullptr;
   DevPass dp{};
+  void use_stream(cudaStream_t st) {
+    last_stream = st;
+    if (std::find(streams.begin(), streams.end(), st) == streams.end()) streams.push_back(st);
+  }
 };
 
 namespace {
@@ -473,7 +478,7 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     cudaError_t e = cudaStreamWaitEvent(st, p->upload_ev, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
-  p->last_stream = st;
+  p->use_stream(st);
   return RBKV_OK;
 }
 
@@ -527,7 +532,7 @@ rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache
     e = cudaStreamWaitEvent(st, p->upload_ev, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
-  p->last_stream = st;
+  p->use_stream(st);
   const ShapeInfo s = shape_of(p->cfg);
   float* part_o = (float*)scratch;
   float* part_lse = (float*)((char*)scratch + partial_o_bytes(p->plan.n_parts, s));
@@ -798,7 +803,7 @@ rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_str
     cudaError_t e = cudaStreamWaitEvent(st, p->upload_ev, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
-  p->last_stream = st;
+  p->use_stream(st);
   cudaError_t e = launch_wait_timeout((int32_t*)p->dev, (long long)limit_cycles, st);
   if (e != cudaSuccess) return cuda_fail(e, "wait-timeout launch");
   return RBKV_OK;
@@ -806,7 +811,22 @@ rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_str
 
 void rbkv_pass_destroy(rbkv_pass* p) {
   if (!p) return;
-  if (p->dev) cudaFreeAsync(p->dev, p->last_stream);
+  if (p->dev) {
+    // the metadata is freed in order after the pass's work on every stream it
+    // was used on: the freeing stream first waits for each of the others
+    cudaStream_t fs = p->last_stream;
+    if (p->streams.size() > 1) {
+      cudaEvent_t ev = nullptr;
+      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess) {
+        for (cudaStream_t st : p->streams) {
+          if (st == fs) continue;
+          if (cudaEventRecord(ev, st) == cudaSuccess) cudaStreamWaitEvent(fs, ev, 0);
+        }
+        cudaEventDestroy(ev);
+      }
+    }
+    cudaFreeAsync(p->dev, fs);
+  }
   if (p->upload_ev) cudaEventDestroy(p->upload_ev);
   delete p;
 }

@@ -95,7 +95,8 @@ def test_replayed_graph_against_oracle(rbkv):
     pair = Pair(rbkv, sh, scn.num_blocks)
     b, st = scn.registration()
     pair.step(b, 0, st, attend=False)
-    frame = rbkv.Frame(pair.cfg, scn.budget)
+    # the prompt's last chunk (16 rows) runs as packed decode units
+    frame = rbkv.Frame(pair.cfg, scn.budget, packed_units=1)
     dt = pair.cfg.torch_dtype
     ws = torch.empty(frame.workspace_bytes(), dtype=torch.uint8, device="cuda")
     kc, vc = pair.kc.clone(), pair.vc.clone()

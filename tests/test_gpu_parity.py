@@ -40,6 +40,11 @@ def test_scaled_scenarios_all_outputs(rbkv, name, factor, split):
     (r,) = run_scenario(rbkv, scn, split_keys=split)
     _ok(r)
     assert r["pair"].cache_equal()
+    plan = r["plan"]
+    assert plan["decode_items"] > 0
+    if name != "decode_stress":
+        # the scaled pass keeps its prompt chunks, on the tensor-core kernel
+        assert plan["chunk_rows"] > 0 and plan["chunk_tiles"] > 0, plan
 
 
 @pytest.mark.parametrize("split", [None, 64, 192])
@@ -95,27 +100,27 @@ def test_short_prompts_packed_decode_units(rbkv, hq, hkv):
     """Prompt chunks of 2..16 rows with short contexts run on the decode kernel,
     several causal rows per unit (8 / g of them): fresh prompts, chunks behind a
     short cached prefix, next to plain decodes.  Every output against the oracle."""
-    rng = np.random.default_rng(hq + 100 * hkv)
-    shape = workloads.Shape(hq, hkv, 128, 64, "bf16", 1.0 / np.sqrt(128.0))
-    hist = [(100 + i, int(rng.integers(1, 300))) for i in range(24)]
-    reqs = [(100 + i, c + int(rng.integers(2, 17)), c) for i, (_, c) in enumerate(hist[:12])]
-    reqs += [(100 + i, c, c) for i, (_, c) in enumerate(hist[12:], start=12)]
-    reqs += [(900 + i, int(rng.integers(2, 17)), 0) for i in range(40)]
-    budget = sum(p - s if p > s else 1 for _, p, s in reqs)
-    nb = sum(-(-(c + 40) // 64) for _, c in hist) + 40 + 16
-    scn = workloads.Scenario("short", shape, budget, 0, hist, reqs, nb)
+    scn = workloads.short_prompts(hq, hkv, seed=hq + 100 * hkv)
     (r,) = run_scenario(rbkv, scn)
     assert r["plan"]["chunk_tiles"] == 0            # every chunk took the decode kernel
+    assert r["plan"]["chunk_rows"] > 0 and r["plan"]["decode_items"] > 0
     _ok(r)
     assert r["pair"].cache_equal()
 
 
-def test_garbage_in_unwritten_slots_does_not_leak(rbkv):
+@pytest.mark.parametrize("split", [None, 64])
+def test_garbage_in_unwritten_slots_does_not_leak(rbkv, split):
     """Slots past a sequence's context hold whatever the caller left there
-    (here NaN); outputs must not see them."""
+    (here NaN); outputs must not see them.  The pass has decode units and
+    tensor-core chunk tiles whose key ranges end inside a 128-key tile (96 and
+    288 keys), so both kernels meet NaN rows in their last K/V tile."""
     scn = workloads.scaled(workloads.mistral_7b(0), 8)
-    (r,) = run_scenario(rbkv, scn, cache_fill=float("nan"))
+    (r,) = run_scenario(rbkv, scn, cache_fill=float("nan"), split_keys=split)
     _ok(r)
+    plan = r["plan"]
+    assert plan["chunk_tiles"] > 0 and plan["decode_items"] > 0, plan
+    m = r["meta"]
+    assert any(n > 1 and c % 128 for n, c in zip(m.n_new, m.ctx))
 
 
 def test_empty_pass_and_repeat_determinism(rbkv):

@@ -31,11 +31,29 @@ def _pass_with_splits(rbkv, scn, split_keys):
     return pair, p, q
 
 
-def test_noalloc_matches_workspace_entry_twice(rbkv):
-    scn = workloads.scaled(workloads.llama2_7b(0), 4)    # a prompt chunk + split decodes
+def _chunk_only():
+    """One 128-row prompt chunk behind a 600-token cached prefix, no decodes:
+    the tensor-core kernel runs alone (it waits for the append itself) and its
+    key range is cut in 128-key pieces that the combine merges."""
+    shape = workloads.llama2_7b(0).shape
+    return workloads.Scenario("chunk_only", shape, 128, 128, [(2, 600)], [(2, 900, 600)],
+                              num_blocks=32)
+
+
+@pytest.mark.parametrize("case", ["mixed", "chunk_only"])
+def test_noalloc_matches_workspace_entry_twice(rbkv, case):
+    if case == "mixed":
+        scn = workloads.scaled(workloads.llama2_7b(0), 4)    # a prompt chunk + split decodes
+    else:
+        scn = _chunk_only()
     pair, p, q = _pass_with_splits(rbkv, scn, 128)
     assert p.workspace_bytes() > 0                        # the scratch is used
-    assert p.plan()["chunk_rows"] > 0
+    plan = p.plan()
+    assert plan["chunk_rows"] > 0 and plan["chunk_tiles"] > 0, plan
+    if case == "mixed":
+        assert plan["decode_items"] > 0, plan
+    else:
+        assert plan["decode_items"] == 0, plan
     ref = rbkv.ragged_attention(p, q, pair.kc, pair.vc)
     outs = []
     for _ in range(2):

@@ -133,6 +133,23 @@ def mistral_7b(seed: int = 0) -> Scenario:
     return Scenario("mistral_7b", shape, 2048, 768, hist, reqs, num_blocks=nb)
 
 
+def short_prompts(num_heads_q: int, num_heads_kv: int, seed: int = 0) -> Scenario:
+    """Short prompt chunks next to decodes, head_dim 128, bf16, block 64.
+
+    12 prompts of 2..16 new tokens behind a cached prefix of 1..299 tokens, 12
+    decodes with such contexts, and 40 fresh prompts of 2..16 tokens; the
+    budget holds every token (no chunk cap)."""
+    rng = np.random.default_rng(seed)
+    shape = Shape(num_heads_q, num_heads_kv, 128, 64, "bf16", 1.0 / math.sqrt(128.0))
+    hist = [(100 + i, int(rng.integers(1, 300))) for i in range(24)]
+    reqs = [(100 + i, c + int(rng.integers(2, 17)), c) for i, (_, c) in enumerate(hist[:12])]
+    reqs += [(100 + i, c, c) for i, (_, c) in enumerate(hist[12:], start=12)]
+    reqs += [(900 + i, int(rng.integers(2, 17)), 0) for i in range(40)]
+    budget = sum(p - s if p > s else 1 for _, p, s in reqs)
+    nb = sum(-(-(c + 40) // 64) for _, c in hist) + 40 + 16
+    return Scenario("short_prompts", shape, budget, 0, hist, reqs, nb)
+
+
 SCENARIOS = {
     "tiny": tiny,
     "llama2_7b": llama2_7b,
@@ -143,19 +160,29 @@ SCENARIOS = {
 
 def scaled(scn: Scenario, factor: int) -> Scenario:
     """Same scenario with every cached length and prompt divided by ``factor``
-    (at least 1 token each): a cheaper case of the same structure."""
+    (at least 1 token each): a cheaper case of the same structure.
+
+    Every decoding request is kept, and so is its one token in the budget;
+    only the budget's prompt share (budget minus the decode count) and the
+    chunk cap are divided by ``factor``.  The scaled pass therefore holds the
+    same kinds of rows as the full one: decodes and prompt chunks."""
     def d(n: int) -> int:
         return max(1, n // factor)
     hist = [(s, d(n)) for s, n in scn.histories]
     hmap = dict(hist)
     reqs = []
+    n_decode = 0
     for s, p, seen in scn.requests:
         if s in hmap and seen > 0:
             ns = hmap[s]
+            if seen >= p:
+                n_decode += 1
             reqs.append((s, ns if seen >= p else max(ns + 1, d(p)), ns))
         else:
             reqs.append((s, d(p), 0))
-    return Scenario(scn.name + f"/{factor}", scn.shape, max(1, scn.budget // factor),
+    prompt_share = max(0, scn.budget - n_decode)
+    budget = n_decode + (max(1, prompt_share // factor) if prompt_share else 0)
+    return Scenario(scn.name + f"/{factor}", scn.shape, max(1, budget),
                     max(0, scn.max_chunk // factor), hist, reqs, scn.num_blocks, scn.notes)
 
 
