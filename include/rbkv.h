@@ -234,8 +234,9 @@ void rbkv_pass_destroy(rbkv_pass* p);
  * Memory Management"): for pass row t of sequence s at position p,
  * k_cache[table_s[p/B]][h][p%B][:] = k_new[t][h][:] (same for V), all h.
  * k_new, v_new: [T][H_kv][D]; k_cache, v_cache: [num_blocks][H_kv][B][D].
- * The first device call of a pass uploads its metadata (one host-to-device
- * copy on `stream`).  A pass is bound to the device current at that call.
+ * The first device call of a pass uploads its metadata: a small kernel on
+ * `stream` copies it from mapped pinned host memory into a stream-ordered
+ * device allocation.  A pass is bound to the device current at that call.
  * Errors: RBKV_ERR_INVALID (null pointer with T > 0, other device),
  * RBKV_ERR_CUDA. */
 rbkv_status rbkv_kv_append(rbkv_pass* p, const void* k_new, const void* v_new,
@@ -403,7 +404,8 @@ typedef enum {
   RBKV_KERNEL_DECODE = 2,     /* split-KV decode attention (TMA + tensor cores) */
   RBKV_KERNEL_GENERIC = 3,    /* CUDA-core attention */
   RBKV_KERNEL_COMBINE = 4,    /* log-sum-exp combine */
-  RBKV_KERNEL_KINDS = 5
+  RBKV_KERNEL_META_UPLOAD = 5, /* a pass's metadata, host to device */
+  RBKV_KERNEL_KINDS = 6
 } rbkv_kernel_kind;
 
 /* Kernels this process has launched through the library so far. */

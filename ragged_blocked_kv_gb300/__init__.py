@@ -113,7 +113,8 @@ SIGNATURES = {
     "rbkv_profile_reset": (None, []),
 }
 
-KERNEL_KINDS = {"kv_append": 0, "chunk": 1, "decode": 2, "generic": 3, "combine": 4}
+KERNEL_KINDS = {"kv_append": 0, "chunk": 1, "decode": 2, "generic": 3, "combine": 4,
+                "upload": 5}
 
 _lib = None
 

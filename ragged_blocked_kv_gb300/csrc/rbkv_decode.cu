@@ -469,9 +469,27 @@ EncodeTiledFn encode_fn() {
 
 // A row-major bf16 matrix [rows][cols] as a 2-D TMA tensor: boxes of 64
 // columns (128 bytes) x box_rows rows, 128-byte swizzle; rows past the end
-// read as zero.
+// read as zero.  A descriptor depends only on these arguments, and a serving
+// loop passes the same cache arrays for every pass, so the last few encoded
+// descriptors are kept per host thread and reused.
 cudaError_t make_tmap_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
                          int box_rows) {
+  struct Entry {
+    CUtensorMap map;
+    const void* ptr;
+    int64_t rows, cols;
+    int box_rows;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries];
+  thread_local int filled = 0, next = 0;
+  for (int i = 0; i < filled; ++i) {
+    const Entry& e = cache[i];
+    if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows) {
+      *m = e.map;
+      return cudaSuccess;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -481,7 +499,16 @@ cudaError_t make_tmap_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t 
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  Entry& e = cache[next];
+  e.map = *m;
+  e.ptr = ptr;
+  e.rows = rows;
+  e.cols = cols;
+  e.box_rows = box_rows;
+  next = (next + 1) % kEntries;
+  if (filled < kEntries) ++filled;
+  return cudaSuccess;
 }
 
 cudaError_t make_cache_tmap(CUtensorMap* m, const void* cache, int64_t rows, int head_dim,

@@ -71,11 +71,12 @@ class BlockPool {
 };
 
 // ---- pinned staging buffers for the per-pass metadata upload ---------------
-// A buffer goes back to the pool as soon as its copy is enqueued; it is reused
-// only once the event recorded after that copy has completed, so no call ever
-// blocks on it.
+// Mapped pinned host memory: the upload kernel reads it directly.  A buffer
+// goes back to the pool as soon as its upload is enqueued; it is reused only
+// once the event recorded after that upload has completed.
 struct PinnedBuf {
   void* ptr = nullptr;
+  void* dptr = nullptr;   // the same memory's device-accessible address (mapped)
   size_t cap = 0;
   cudaEvent_t ev = nullptr;
 };
@@ -100,8 +101,10 @@ class PinnedPool {
     size_t cap = 4096;
     while (cap < bytes) cap *= 2;
     PinnedBuf b;
-    cudaError_t e = cudaHostAlloc(&b.ptr, cap, cudaHostAllocDefault);
+    cudaError_t e = cudaHostAlloc(&b.ptr, cap, cudaHostAllocMapped);
     if (e != cudaSuccess) return e;
+    e = cudaHostGetDevicePointer(&b.dptr, b.ptr, 0);
+    if (e != cudaSuccess) { cudaFreeHost(b.ptr); return e; }
     e = cudaEventCreateWithFlags(&b.ev, cudaEventDisableTiming);
     if (e != cudaSuccess) { cudaFreeHost(b.ptr); return e; }
     b.cap = cap;
@@ -298,7 +301,32 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   std::vector<int32_t> bounds;
   std::vector<WorkItem> decode, generic;
   int32_t max_splits = 0;
-  auto add_row = [&](int32_t row, int32_t n_keys, int32_t table_off, std::vector<WorkItem>& dst) {
+  // Decode-kernel work is planned per row first: the key split of a row is the
+  // same for all its KV heads, so a row's pieces (one per key split, or one per
+  // packed group of prompt rows) are made and sorted longest first, and only
+  // then expanded into one unit per KV head.  Partial slot of (row, head h,
+  // split k): part0 + h * nsplit + k.
+  struct Piece {
+    int32_t row, key_begin, key_end, part0, k, nsplit, table_off, n_rows, diag;
+  };
+  std::vector<Piece> pieces;
+  pieces.reserve((size_t)S * 2);
+  auto add_decode_row = [&](int32_t row, int32_t n_keys, int32_t table_off) {
+    split_keys(n_keys, split, gran, bounds);
+    const int32_t ns = (int32_t)bounds.size() - 1;
+    max_splits = std::max(max_splits, ns);
+    int32_t part0 = -1;
+    if (ns > 1) {
+      part0 = pl.n_parts;
+      pl.n_parts += ns * s.H_kv;
+      for (int32_t h = 0; h < s.H_kv; ++h)
+        pl.combine.push_back(CombineRow{row, h, part0 + h * ns, ns});
+    }
+    for (int32_t k = 0; k < ns; ++k)
+      pieces.push_back(Piece{row, bounds[k], bounds[k + 1], part0, k, ns, table_off, 1, n_keys});
+  };
+  // CUDA-core units: (row, kv head, split), as before
+  auto add_generic_row = [&](int32_t row, int32_t n_keys, int32_t table_off) {
     for (int32_t h = 0; h < s.H_kv; ++h) {
       split_keys(n_keys, split, gran, bounds);
       int32_t ns = (int32_t)bounds.size() - 1;
@@ -310,29 +338,29 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
         pl.combine.push_back(CombineRow{row, h, part0, ns});
       }
       for (int32_t k = 0; k < ns; ++k)
-        dst.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1, table_off,
-                               1, n_keys});
+        generic.push_back(WorkItem{row, h, bounds[k], bounds[k + 1], ns > 1 ? part0 + k : -1,
+                                   table_off, 1, n_keys});
     }
   };
   // rows of a short prompt chunk per decode unit: all g query heads of each
   const int32_t pack = s.g <= kDecodeRowsCap ? kDecodeRowsCap / s.g : 1;
   for (int32_t i = 0; i < S; ++i) {
     if (p.n_new[i] == 1) {
-      add_row(p.q_start[i], p.ctx[i], p.block_start[i], fast_decode ? decode : generic);
+      if (fast_decode) add_decode_row(p.q_start[i], p.ctx[i], p.block_start[i]);
+      else add_generic_row(p.q_start[i], p.ctx[i], p.block_start[i]);
     } else if (fast_decode && p.n_new[i] <= kPackedRowsMax && p.ctx[i] <= split) {
       // a short prompt chunk whose keys fit one decode unit: causal rows packed
       // `pack` at a time into decode units (no tensor-core tile of 128 rows)
       for (int32_t j = 0; j < p.n_new[i]; j += pack) {
         const int32_t n = std::min(pack, p.n_new[i] - j);
-        for (int32_t h = 0; h < s.H_kv; ++h)
-          decode.push_back(WorkItem{p.q_start[i] + j, h, 0, p.seen[i] + j + n, -1,
-                                    p.block_start[i], n, p.seen[i] + j + 1});
+        pieces.push_back(Piece{p.q_start[i] + j, 0, p.seen[i] + j + n, -1, 0, 1,
+                               p.block_start[i], n, p.seen[i] + j + 1});
       }
       max_splits = std::max(max_splits, 1);
       pl.decode_packed = 1;
     } else if (fast_chunk) {
       // 128-row tiles; a tile's key range [0, last position + 1) is cut into
-      // 64-key-aligned pieces of at most `chunk_split` keys, merged later by
+      // 128-key-aligned pieces of at most `chunk_split` keys, merged later by
       // the log-sum-exp combine like split decode rows
       for (int32_t r = 0; r < p.n_new[i]; r += kChunkTileRows) {
         const int32_t n = std::min(kChunkTileRows, p.n_new[i] - r);
@@ -356,13 +384,21 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
       }
     } else {
       for (int32_t j = 0; j < p.n_new[i]; ++j)
-        add_row(p.q_start[i] + j, p.seen[i] + j + 1, p.block_start[i], generic);
+        add_generic_row(p.q_start[i] + j, p.seen[i] + j + 1, p.block_start[i]);
     }
   }
+  std::stable_sort(pieces.begin(), pieces.end(), [](const Piece& a, const Piece& b) {
+    return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+  });
+  decode.reserve(pieces.size() * (size_t)s.H_kv);
+  for (const Piece& pc : pieces)
+    for (int32_t h = 0; h < s.H_kv; ++h)
+      decode.push_back(WorkItem{pc.row, h, pc.key_begin, pc.key_end,
+                                pc.part0 >= 0 ? pc.part0 + h * pc.nsplit + pc.k : -1,
+                                pc.table_off, pc.n_rows, pc.diag});
   auto longer = [](const WorkItem& a, const WorkItem& b) {
     return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
   };
-  std::stable_sort(decode.begin(), decode.end(), longer);
   std::stable_sort(generic.begin(), generic.end(), longer);
   std::stable_sort(pl.chunk.begin(), pl.chunk.end(), [](const ChunkTile& a, const ChunkTile& b) {
     return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
@@ -413,15 +449,6 @@ rbkv_status ensure_plan(rbkv_pass* p) {
   return RBKV_OK;
 }
 
-template <class T>
-void put(std::vector<int32_t>& w, size_t& off, const std::vector<T>& v) {
-  static_assert(sizeof(T) % 4 == 0, "int32 packing");
-  size_t words = v.size() * sizeof(T) / 4;
-  off = w.size();
-  w.resize(off + words);
-  if (words) std::memcpy(w.data() + off, v.data(), words * 4);
-  while (w.size() % 4) w.push_back(0);  // 16-byte aligned sections
-}
 
 // Plan (if needed), pack and upload the metadata on `st`; order `st` after
 // the upload when it is another stream.
@@ -430,23 +457,43 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
   if (rs != RBKV_OK) return rs;
   if (!p->dev) {
     const Plan& pl = p->plan;
-    std::vector<int32_t> w(4, 0);  // status words: code, wait site, index, block
-    size_t o_slot, o_blocks, o_dec, o_gen, o_chunk, o_comb;
-    put(w, o_slot, p->slot);
-    put(w, o_blocks, p->block_ids);
-    put(w, o_dec, pl.decode);
-    put(w, o_gen, pl.generic);
-    put(w, o_chunk, pl.chunk);
-    put(w, o_comb, pl.combine);
-    size_t bytes = w.size() * 4;
+    // sections of int32 words, each 16-byte aligned, after four status words:
+    // packed straight into pinned staging memory
+    size_t words = 4;
+    auto section = [&words](size_t bytes) {
+      const size_t off = words;
+      words = (words + bytes / 4 + 3) / 4 * 4;
+      return off;
+    };
+    const size_t o_slot = section(p->slot.size() * 4);
+    const size_t o_blocks = section(p->block_ids.size() * 4);
+    const size_t o_dec = section(pl.decode.size() * sizeof(WorkItem));
+    const size_t o_gen = section(pl.generic.size() * sizeof(WorkItem));
+    const size_t o_chunk = section(pl.chunk.size() * sizeof(ChunkTile));
+    const size_t o_comb = section(pl.combine.size() * sizeof(CombineRow));
+    const size_t bytes = words * 4;
     PinnedBuf pin;
     cudaError_t e = p->pinned->acquire(bytes, pin);
     if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
-    std::memcpy(pin.ptr, w.data(), bytes);
+    int32_t* hw = (int32_t*)pin.ptr;
+    std::memset(hw, 0, 16);   // status words: code, wait site, index, block
+    auto fill = [hw](size_t off, const void* src, size_t n) {
+      if (n) std::memcpy(hw + off, src, n);
+    };
+    fill(o_slot, p->slot.data(), p->slot.size() * 4);
+    fill(o_blocks, p->block_ids.data(), p->block_ids.size() * 4);
+    fill(o_dec, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
+    fill(o_gen, pl.generic.data(), pl.generic.size() * sizeof(WorkItem));
+    fill(o_chunk, pl.chunk.data(), pl.chunk.size() * sizeof(ChunkTile));
+    fill(o_comb, pl.combine.data(), pl.combine.size() * sizeof(CombineRow));
     void* dev = nullptr;
     e = cudaMallocAsync(&dev, bytes, st);
     if (e != cudaSuccess) { p->pinned->release(pin); return cuda_fail(e, "cudaMallocAsync"); }
-    e = cudaMemcpyAsync(dev, pin.ptr, bytes, cudaMemcpyHostToDevice, st);
+    // the upload is the pass's first kernel: it overlaps the previous kernel
+    // in the stream and stores only after that kernel has finished
+    e = launch_counted(RBKV_KERNEL_META_UPLOAD, st, [&] {
+      return launch_meta_upload(pin.dptr, dev, bytes, st, !g_prof.on);
+    });
     if (e == cudaSuccess) e = cudaEventRecord(pin.ev, st);
     p->pinned->release(pin);
     if (e != cudaSuccess) { cudaFreeAsync(dev, st); return cuda_fail(e, "metadata upload"); }

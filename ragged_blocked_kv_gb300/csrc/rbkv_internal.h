@@ -140,6 +140,11 @@ bool chunk_fast_supported(const ShapeInfo& s);
 cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* k_new,
                              const void* v_new, void* k_cache, void* v_cache, cudaStream_t st,
                              bool overlap_previous);
+// Copy `bytes` (a multiple of 16) of a pass's metadata from mapped pinned
+// host memory `src` (a device-accessible address) to device memory `dst`, as a
+// kernel that may overlap its predecessor and waits for it before storing.
+cudaError_t launch_meta_upload(const void* src, void* dst, size_t bytes, cudaStream_t st,
+                               bool overlap_previous);
 cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
                                      const void* k_cache, const void* v_cache, void* o,
                                      float* part_o, float* part_lse, cudaStream_t st);

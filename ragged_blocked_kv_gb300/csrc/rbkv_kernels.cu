@@ -44,13 +44,16 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // ---------------------------------------------------------------------------
 // kv_append
 // ---------------------------------------------------------------------------
-// One warp per (token, KV head): the first half of the warp copies the K row,
-// the second half the V row, 16 bytes per lane per step (32-bit index math).
-// A warp takes two rows at a time, with every load of both issued before the
-// first store (rows are at most 64 x 16 bytes).
-constexpr int kAppendWarps = 8;
+// A flat copy of 16-byte vectors: vector i of the 2 * T * H_kv * (D / vec)
+// new K and V vectors (K first, then V; inside each, the [T][H_kv][D] order of
+// the input, so consecutive threads read consecutive addresses) goes to its
+// token's cache slot.  Each thread keeps kAppendUnroll vectors in flight (all
+// loads, data and slot ids, issued before the first store); the grid strides
+// over the vectors, so one launch sized by a frame's capacity serves any pass.
+constexpr int kAppendThreads = 256;
+constexpr int kAppendUnroll = 4;
 
-__global__ void __launch_bounds__(kAppendWarps * 32)
+__global__ void __launch_bounds__(kAppendThreads)
     kv_append_kernel(DevPass dp, int32_t H_kv, int32_t B, int32_t vec_per_row,
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache, uint4* __restrict__ v_cache) {
@@ -60,46 +63,72 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
   // for this grid before reading the cache.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
-  const uint4* __restrict__ src = half ? v_new : k_new;
-  uint4* __restrict__ dst = half ? v_cache : k_cache;
-  const uint32_t rows = (uint32_t)pass_count(dp, kCountTokens, dp.num_tokens) * (uint32_t)H_kv;
-  const uint32_t stride = gridDim.x * kAppendWarps;
-  for (uint32_t r0 = blockIdx.x * kAppendWarps + warp; r0 < rows; r0 += 2 * stride) {
-    const uint32_t r1 = r0 + stride;
-    const bool two = r1 < rows;
-    const uint32_t t0 = r0 / (uint32_t)H_kv;
-    const uint32_t t1 = two ? r1 / (uint32_t)H_kv : t0;
-    const int32_t slot0 = dp.slot[t0];
-    const int32_t slot1 = dp.slot[t1];
-    uint4 b0[4], b1[4];
+  const uint32_t stride = gridDim.x * kAppendThreads;
+  const uint32_t per_tok = (uint32_t)H_kv * (uint32_t)vec_per_row;
+  const uint32_t half = (uint32_t)pass_count(dp, kCountTokens, dp.num_tokens) * per_tok;
+  const uint32_t total = 2 * half;
+  for (uint32_t i0 = blockIdx.x * kAppendThreads + threadIdx.x; i0 < total;
+       i0 += kAppendUnroll * stride) {
+    uint4 val[kAppendUnroll];
+    int32_t slot[kAppendUnroll];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int v = hl + 16 * i;
-      if (v < vec_per_row) {
-        b0[i] = src[(size_t)r0 * vec_per_row + v];
-        if (two) b1[i] = src[(size_t)r1 * vec_per_row + v];
+    for (int u = 0; u < kAppendUnroll; ++u) {
+      const uint32_t i = i0 + u * stride;
+      if (i < total) {
+        const bool is_v = i >= half;
+        const uint32_t j = is_v ? i - half : i;
+        val[u] = is_v ? v_new[j] : k_new[j];
+        slot[u] = dp.slot[j / per_tok];
       }
     }
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (k == 1 && !two) break;
-      const uint32_t r = k ? r1 : r0, t = k ? t1 : t0;
-      const int32_t slot = k ? slot1 : slot0;
-      const uint32_t h = r - t * (uint32_t)H_kv;
-      const int32_t blk = slot / B, off = slot - blk * B;
-      if (slot < 0 || blk >= dp.num_blocks) {
-        if (lane == 0) report(dp.status, kDevBounds);
+    for (int u = 0; u < kAppendUnroll; ++u) {
+      const uint32_t i = i0 + u * stride;
+      if (i >= total) break;
+      const bool is_v = i >= half;
+      const uint32_t j = is_v ? i - half : i;
+      const uint32_t hc = j % per_tok;
+      const uint32_t h = hc / (uint32_t)vec_per_row, c = hc - h * (uint32_t)vec_per_row;
+      const int32_t blk = slot[u] / B, off = slot[u] - blk * B;
+      if (slot[u] < 0 || blk >= dp.num_blocks) {
+        report(dp.status, kDevBounds);
         continue;
       }
-      uint4* d_row = dst + (((size_t)blk * H_kv + h) * B + off) * vec_per_row;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int v = hl + 16 * i;
-        if (v < vec_per_row) d_row[v] = k ? b1[i] : b0[i];
-      }
+      uint4* dst = is_v ? v_cache : k_cache;
+      dst[(((size_t)blk * H_kv + h) * B + off) * vec_per_row + c] = val[u];
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// metadata upload
+// ---------------------------------------------------------------------------
+// Copies a pass's packed metadata (status words, slots, block tables, work
+// lists) from pinned host memory mapped into the device's address space to
+// the pass's device buffer.  It is the first kernel of a pass, launched to
+// overlap the previous pass's last kernel: each thread reads its vectors from
+// host memory first, then waits for that kernel (the device buffer may be
+// memory the previous passes used), then stores them.  A pass's upload is so
+// part of the chain of kernels, with no copy between two passes' kernels.
+constexpr int kUploadThreads = 256;
+constexpr int kUploadUnroll = 4;
+
+__global__ void __launch_bounds__(kUploadThreads)
+    meta_upload_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int32_t vec) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t stride = gridDim.x * kUploadThreads;
+  const uint32_t i0 = blockIdx.x * kUploadThreads + threadIdx.x;
+  uint4 v[kUploadUnroll];
+#pragma unroll
+  for (int u = 0; u < kUploadUnroll; ++u) {
+    const uint32_t i = i0 + u * stride;
+    if (i < (uint32_t)vec) v[u] = src[i];
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#pragma unroll
+  for (int u = 0; u < kUploadUnroll; ++u) {
+    const uint32_t i = i0 + u * stride;
+    if (i < (uint32_t)vec) dst[i] = v[u];
   }
 }
 
@@ -194,6 +223,12 @@ __global__ void __launch_bounds__(kGenWarps * 32)
 // ---------------------------------------------------------------------------
 // log-sum-exp combine: one warp per (split row, query head of the group)
 // ---------------------------------------------------------------------------
+// The lanes first read the row's log-sum-exps together (lane k takes splits
+// k, k + 32, ...) for their maximum M and the weight sum; the weighted sum of
+// the partial outputs then takes four splits per round, so that their loads
+// are in flight together.
+constexpr int kCombineSplitsInFlight = 4;
+
 template <class T>
 __global__ void __launch_bounds__(128)
     combine_kernel(DevPass dp, ShapeInfo s, const float* __restrict__ part_o,
@@ -205,32 +240,54 @@ __global__ void __launch_bounds__(128)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x % 32;
   const int64_t n_warps = (int64_t)pass_count(dp, kCountCombine, dp.n_combine) * s.g;
+  const int D = s.D, dpl = D / 32;
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < n_warps;
        w += (int64_t)gridDim.x * blockDim.x / 32) {
-  const CombineRow cr = dp.combine_rows[w / s.g];
-  const int gi = (int)(w % s.g);
-  const int D = s.D, dpl = D / 32;
-  float M = -INFINITY;
-  for (int i = 0; i < cr.nsplit; ++i) M = fmaxf(M, part_lse[(int64_t)(cr.part_begin + i) * s.g + gi]);
-  float acc[kMaxDPerLane];
+    const CombineRow cr = dp.combine_rows[w / s.g];
+    const int gi = (int)(w % s.g);
+    const float* lse = part_lse + (int64_t)cr.part_begin * s.g + gi;   // stride g per split
+    float M = -INFINITY;
+    for (int i = lane; i < cr.nsplit; i += 32) M = fmaxf(M, lse[(int64_t)i * s.g]);
 #pragma unroll
-  for (int i = 0; i < kMaxDPerLane; ++i) acc[i] = 0.f;
-  float wsum = 0.f;
-  for (int i = 0; i < cr.nsplit; ++i) {
-    const int64_t part = cr.part_begin + i;
-    const float lse = part_lse[part * s.g + gi];
-    const float wi = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
-    wsum += wi;
-    const float* prow = part_o + (part * s.g + gi) * D;
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float wsum = 0.f;
+    for (int i = lane; i < cr.nsplit; i += 32) {
+      const float l = lse[(int64_t)i * s.g];
+      wsum += (l == -INFINITY) ? 0.f : exp2f(l - M);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    float acc[kMaxDPerLane];
+#pragma unroll
+    for (int k = 0; k < kMaxDPerLane; ++k) acc[k] = 0.f;
+    for (int i0 = 0; i0 < cr.nsplit; i0 += kCombineSplitsInFlight) {
+      float wv[kCombineSplitsInFlight];
+      float x[kCombineSplitsInFlight][kMaxDPerLane];
+#pragma unroll
+      for (int u = 0; u < kCombineSplitsInFlight; ++u) {
+        const int i = i0 + u;
+        wv[u] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxDPerLane; ++k) x[u][k] = 0.f;
+        if (i < cr.nsplit) {
+          const float l = lse[(int64_t)i * s.g];
+          wv[u] = (l == -INFINITY) ? 0.f : exp2f(l - M);
+          const float* prow = part_o + ((int64_t)(cr.part_begin + i) * s.g + gi) * D;
+#pragma unroll
+          for (int k = 0; k < kMaxDPerLane; ++k)
+            if (k < dpl) x[u][k] = prow[lane + 32 * k];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kCombineSplitsInFlight; ++u)
+#pragma unroll
+        for (int k = 0; k < kMaxDPerLane; ++k) acc[k] = fmaf(wv[u], x[u][k], acc[k]);
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    T* orow = o + ((int64_t)cr.row * s.H_q + cr.kv_head * s.g + gi) * D;
 #pragma unroll
     for (int k = 0; k < kMaxDPerLane; ++k)
-      if (k < dpl) acc[k] = fmaf(wi, prow[lane + 32 * k], acc[k]);
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  T* orow = o + ((int64_t)cr.row * s.H_q + cr.kv_head * s.g + gi) * D;
-#pragma unroll
-  for (int k = 0; k < kMaxDPerLane; ++k)
-    if (k < dpl) orow[lane + 32 * k] = from_f<T>(acc[k] * inv);
+      if (k < dpl) orow[lane + 32 * k] = from_f<T>(acc[k] * inv);
   }
 }
 
@@ -248,15 +305,16 @@ cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* 
                              bool overlap_previous) {
   const int esz = s.dtype == 0 ? 2 : 4;
   const int vec = s.D * esz / 16;
-  const int64_t rows = (int64_t)dp.num_tokens * s.H_kv;
-  if (rows == 0) return cudaSuccess;
-  if (rows >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
-  int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
+  const int64_t vectors = 2 * (int64_t)dp.num_tokens * s.H_kv * vec;
+  if (vectors == 0) return cudaSuccess;
+  if (vectors >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  // one wave: every thread takes kAppendUnroll vectors per round
+  int64_t blocks = (vectors + kAppendThreads * kAppendUnroll - 1) / (kAppendThreads * kAppendUnroll);
   const int64_t cap = (int64_t)num_sms_current() * 8;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kAppendWarps * 32);
+  cfg.blockDim = dim3(kAppendThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -265,6 +323,28 @@ cudaError_t launch_kv_append(const DevPass& dp, const ShapeInfo& s, const void* 
   cfg.numAttrs = overlap_previous ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kv_append_kernel, dp, s.H_kv, s.B, vec, (const uint4*)k_new,
                             (const uint4*)v_new, (uint4*)k_cache, (uint4*)v_cache);
+}
+
+cudaError_t launch_meta_upload(const void* src, void* dst, size_t bytes, cudaStream_t st,
+                               bool overlap_previous) {
+  if (bytes == 0) return cudaSuccess;
+  if ((bytes & 15) || ((uintptr_t)src & 15) || ((uintptr_t)dst & 15))
+    return cudaErrorMisalignedAddress;
+  const int64_t vec = (int64_t)(bytes / 16);
+  if (vec >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  // every thread holds kUploadUnroll vectors across the wait
+  const int64_t blocks = (vec + kUploadThreads * kUploadUnroll - 1) / (kUploadThreads * kUploadUnroll);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kUploadThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, meta_upload_kernel, (const uint4*)src, (uint4*)dst,
+                            (int32_t)vec);
 }
 
 cudaError_t launch_generic_attention(const DevPass& dp, const ShapeInfo& s, const void* q,
