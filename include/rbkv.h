@@ -118,10 +118,12 @@ typedef struct {
   int32_t split_keys;         /* keys per split used by the plan */
   int32_t partials;           /* partial outputs written to the workspace */
   int32_t chunk_rows;         /* pass rows of multi-token prompt chunks */
-  int32_t chunk_tiles;        /* tensor-core tiles (128 query rows, one head) */
+  int32_t chunk_tiles;        /* tensor-core query tiles (128 rows, one key piece) */
   int32_t generic_items;      /* work units on the CUDA-core path */
   int32_t fast_decode;        /* 1 if the TMA/tensor-core decode kernel is used */
   int32_t fast_chunk;         /* 1 if the tcgen05 chunk kernel is used */
+  int32_t chunk_items;        /* tensor-core work items: one or two query tiles
+                                 sharing the K/V tiles they read */
 } rbkv_plan_info;
 
 /* Library ABI version (RBKV_ABI_VERSION). */

@@ -60,7 +60,8 @@ class _PassMeta(C.Structure):
 class _PlanInfo(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_sms", "decode_rows", "decode_items", "max_splits", "split_keys", "partials",
-        "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk")]
+        "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk",
+        "chunk_items")]
 
 
 class _FrameCaps(C.Structure):

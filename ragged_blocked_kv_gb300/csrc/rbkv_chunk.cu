@@ -5,32 +5,43 @@
 // p attends keys 0..p of its sequence: the cached prefix read through the
 // block table plus the chunk's own earlier rows (causal within the chunk).
 //
-// Work items are (128 consecutive rows of one chunk, one query head) pairs; a
-// persistent grid of at most one CTA per SM walks them (longest first, snake
-// order), with barrier phases, the K/V ring and the S buffers continuing from
-// item to item and tensor memory allocated once:
-//  - warp 4 (TMA): streams 128-key K and V tiles of the paged cache into a
-//    3-stage ring (128-byte swizzle), looking block ids up a tile ahead;
-//  - warp 5 (MMA): allocates 512 TMEM columns; one thread issues
-//    S = Q K^T (M=128, N=128, K=128; Q in TMEM) into one of two TMEM S buffers
-//    and O += P V (M=128, N=128, K=128; P in TMEM) into the TMEM O
-//    accumulator, and signals completion with tcgen05.commit;
-//  - warps 0-3 (softmax): thread i owns query row i = TMEM lane i; it writes
-//    its row of Q into TMEM at the start of an item, reads its 128 scores with
-//    tcgen05.ld (two halves), masks causally, keeps a running max that is
-//    raised only when a row's max grows by more than 2^8 (the accumulator in
-//    TMEM is then rescaled in place), writes P as bf16 pairs over the S
-//    columns it has read, and finally normalises O and stores it.
-// The QK^T of the next tile is queued on the tensor pipe before each PV, so it
-// overlaps the softmax of the current one.  About 192 KB of shared memory.
+// A work item is one or two 128-row query tiles that read the same K/V tiles:
+// the same rows for two query heads of one KV group (K/V then cross HBM once
+// for both), or two consecutive row tiles of one head when a group has one
+// head.  A persistent grid of one CTA per SM walks the items (longest first,
+// snake order); barrier phases, the K/V ring and tensor memory carry over from
+// item to item.  Roles:
+//  - warp 8 (TMA): loads each item's query tiles (A and B) into shared memory
+//    and streams 128-key K and V tiles of the paged cache, in the order
+//    K0 V0 K1 V1 ..., through a 4-stage ring of 32 KB stages (128-byte
+//    swizzle), looking block ids up through the block table;
+//  - warp 9 (MMA): one thread issues, per query tile X, S_X = Q_X K^T
+//    (M=128, N=128 keys, K=128; Q from shared memory) into tensor memory and
+//    O_X += P_X V (M=128, N=128 head dims, K=128 keys; P from tensor memory),
+//    in the order QK_A(0) QK_B(0), then for each key tile j: PV_A(j)
+//    QK_A(j+1) PV_B(j) QK_B(j+1).  Each tile's products follow its softmax,
+//    so one tile's softmax runs while the tensor pipe works on the other
+//    tile (an issuing thread per tile was measured slower: interleaved, each
+//    tile's products take longer to finish);
+//  - warps 0-3 / 4-7 (softmax of tile A / B): thread i owns query row i = TMEM
+//    lane i: it reads its 128 scores with tcgen05.ld (one round trip), masks
+//    causally, keeps a running max that is raised only when the row max grows
+//    by more than 2^8 (the accumulator in tensor memory is then rescaled in
+//    place), writes P as bf16 pairs over the score columns it has read, and at
+//    the end of an item normalises O and stores it (or the partial output and
+//    its log-sum-exp when the item covers one piece of a split key range).
+// Tensor memory (512 columns x 128 lanes): S/P of A [0,128), O of A
+// [128,256), S/P of B [256,384), O of B [384,512).  Shared memory: Q of A and
+// B (32 KB each) and the ring (128 KB), about 193 KB: one CTA per SM.
 // Every wait is bounded; on timeout the kernel records RBKV_ERR_TIMEOUT, lets
-// its copies and MMAs drain (bounded), frees its TMEM and returns.
+// its copies and MMAs drain (bounded), frees its tensor memory and returns.
 #include <algorithm>
 
 #include <atomic>
 
 #include "rbkv_internal.h"
 #include "rbkv_ptx.cuh"
+#include "rbkv_tcgen05.cuh"
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -40,155 +51,102 @@ namespace rbkv {
 
 namespace {
 
+using namespace tc;
+
 constexpr int kRows = kChunkTileRows;       // 128 query rows (MMA M)
 constexpr int kKeys = kChunkTileKeys;       // 128 keys per KV tile (MMA N of QK^T)
-constexpr int kStages = 3;
-constexpr int kThreads = 6 * 32;
-constexpr int kKVHalf = kKeys * 128;        // 16 KB: 128 keys x 64 head dims
-constexpr int kKVTile = 2 * kKVHalf;        // 32 KB
-constexpr int kStage = 2 * kKVTile;         // K + V
-// Tensor memory (fp32 columns x 128 lanes, lane = query row): S0 [0,128) and
-// S1 [128,256) (scores of one KV tile each), O [256,384), Q [384,448) as
-// packed bf16 pairs (the QK^T A operand).  The probabilities P of a tile, as
-// bf16 pairs (the PV A operand), overwrite the first 64 columns of its S
-// buffer once they are read.
+constexpr int kStages = 4;                  // ring stages, each one K or one V tile
+constexpr int kHalf = kKeys * 128;          // 16 KB: 128 rows x 64 head dims
+constexpr int kTileBytes = 2 * kHalf;       // 32 KB: 128 rows x 128 head dims
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// three warpgroups: two softmax warpgroups and one with the TMA and MMA
+// warps (its other two warps idle), so that registers can move between
+// warpgroups:
+// launched at kLaunchRegs a thread, the third warpgroup gives back down to
+// kIssueRegs and the softmax warpgroups take kSoftmaxRegs.  The shares add up
+// to the launch's total exactly (a larger claim would wait forever).
+constexpr int kThreads = 12 * 32;
+constexpr int kLaunchRegs = 168;
+constexpr int kIssueRegs = 88;
+constexpr int kSoftmaxRegs = 208;
+static_assert(128 * kIssueRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's registers");
 constexpr int kTmemCols = 512;
-constexpr int kOCol = 256;
-constexpr int kQCol = 384;
-// 192 KB: one CTA per SM with a 3-deep ring of 128-key K/V tiles
-constexpr int kSmemBytes = kStages * kStage + 256;
+constexpr int kTileCols = 256;              // tensor-memory columns of one query tile
+constexpr int kOCol = 128;                  // O after S/P inside a tile's columns
+constexpr int kSmemBytes = 2 * kTileBytes + kStages * kTileBytes + 1024;
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
-// ---- tcgen05 wrappers ----------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   ptx::smem_u32(slot)),
-               "r"(cols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   ptx::smem_u32(bar))
-               : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16 (bf16 in, fp32 accumulate).  A is
-// M rows = TMEM lanes, its K elements packed two per 32-bit column.
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
-  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start address, leading and
-// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, A K-major,
-// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
-__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// Every barrier below is waited on in order of its phases and can never run
-// two phases ahead of a waiter (the parity of a wait is then unambiguous): S,
-// P and PV completion each have one barrier per buffer.
+// Each barrier is waited on in order of its phases and can never run two
+// phases ahead of a waiter (the parity of a wait is then unambiguous).
 struct Bars {
-  uint64_t q_full;      // the softmax threads wrote Q into tensor memory
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2];   // QK^T of tile j done: S buffer j & 1
-  uint64_t p_full[2];   // softmax of tile j done: P written over S buffer j & 1
-  uint64_t o_done[2];   // PV of tile j done
+  uint64_t q_full[2];    // query tile X landed (TMA)
+  uint64_t q_empty[2];   // the last QK^T of an item read query tile X
+  uint64_t kv_full[kStages];      // a K or V tile landed (TMA)
+  uint64_t kv_empty[kStages];     // the MMAs are done with the stage
+  uint64_t s_full[2];    // QK^T of tile X done: S_X readable
+  uint64_t p_full[2];    // softmax of tile X done: P_X written (and V tail rows zeroed)
+  uint64_t o_done[2];    // PV of tile X done
+  uint64_t o_free[2];    // epilogue of tile X read O_X: the next item may overwrite it
   uint32_t tmem_base;
   int abort_flag;
 };
-// shared memory: K/V ring | barriers
-static_assert(kStages * kStage + (int)sizeof(Bars) <= kSmemBytes,
+static_assert(2 * kTileBytes + kStages * kTileBytes + (int)sizeof(Bars) <= kSmemBytes,
               "shared-memory layout overflows its allocation");
 
+// An item as every role sees it (each role reads the rest of a query tile's
+// description itself, when it needs it).
+struct Item {
+  int tile[2];     // chunk tile of each query tile (-1: none)
+  int head[2];
+  int n[2];        // key tiles of each query tile (0: no such tile)
+  int kv_head;
+  int kb, ke;      // key range of the item (the union of its tiles')
+  int nmax;        // key tiles of the item
+};
+
+__device__ __forceinline__ Item load_item(const DevPass& dp, int w) {
+  const ChunkItem ci = dp.chunk_items[w];
+  Item it;
+  it.kv_head = ci.kv_head;
+  it.kb = ci.key_begin;
+  it.ke = ci.key_end;
+  it.nmax = (it.ke - it.kb + kKeys - 1) / kKeys;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    it.tile[x] = ci.tile[x];
+    it.head[x] = ci.head[x];
+    it.n[x] = ci.tile[x] >= 0
+                  ? (dp.chunk_tiles[ci.tile[x]].key_end - it.kb + kKeys - 1) / kKeys
+                  : 0;
+  }
+  return it;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_k,
+    chunk_attn_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                              const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, DevPass dp,
-                              ShapeInfo shp, const __nv_bfloat16* __restrict__ q,
-                              __nv_bfloat16* __restrict__ o,
+                              ShapeInfo shp, __nv_bfloat16* __restrict__ o,
                               float* __restrict__ part_o, float* __restrict__ part_lse,
                               int wait_first) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = smem_raw;
   if (ptx::smem_u32(smem_raw) & 1023) {
     // the swizzled operand layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) atomicCAS(dp.status, 0, kDevBounds);
     ptx::pdl_wait_previous();   // the grid's completion still covers its predecessor
     return;
   }
-  uint8_t* kv_s = base;
-  Bars* bars = reinterpret_cast<Bars*>(kv_s + kStages * kStage);
+  uint8_t* q_s = smem_raw;                       // [2][kTileBytes]
+  uint8_t* kv_s = smem_raw + 2 * kTileBytes;     // [kStages][kTileBytes]
+  Bars* bars = reinterpret_cast<Bars*>(kv_s + kStages * kTileBytes);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work items: (tile, query head) pairs, tiles sorted longest first, heads
-  // inner; this persistent CTA takes items in snake order over the grid
-  const int n_items = pass_count(dp, kCountChunk, dp.n_chunk) * shp.H_q;
+  const int n_items = pass_count(dp, kCountChunk, dp.n_chunk);
   if ((int)blockIdx.x >= n_items) {
     // a grid sized for a frame's capacity: nothing here.  Still wait for the
     // predecessor, so that this grid's completion covers it
@@ -203,20 +161,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = shp.B;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&bars->q_full, 4 * 32);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(&bars->q_full[x], 1);
+      ptx::mbar_init(&bars->q_empty[x], 1);
+      ptx::mbar_init(&bars->s_full[x], 1);
+      ptx::mbar_init(&bars->p_full[x], 4 * 32);
+      ptx::mbar_init(&bars->o_done[x], 1);
+      ptx::mbar_init(&bars->o_free[x], 4 * 32);
+    }
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars->kv_full[s], 1);
       ptx::mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&bars->s_full[b], 1);
-      ptx::mbar_init(&bars->p_full[b], 4 * 32);
-      ptx::mbar_init(&bars->o_done[b], 1);
-    }
     bars->abort_flag = 0;
     ptx::fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -232,246 +192,264 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // Every role walks the same items and KV tiles in the same order; `gi`
-  // numbers this CTA's KV tiles across items, so the ring stage (gi % kStages),
-  // the S/P buffer (gi & 1) and every barrier phase continue from item to item.
-  if (warp == 4) {
+  // Every role walks the same items in the same order.  The ring index `gi`
+  // numbers this CTA's K and V tiles across items (K_j of an item at 2j, V_j
+  // at 2j + 1 from the item's start), so stages and phases carry over.
+  if (warp >= 8) {
+  // the TMA, MMA and V warps' warpgroup gives registers to the softmax warpgroups
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIssueRegs));
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmap_q);
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
       const int box_rows = B < kKeys ? B : kKeys;
-      uint32_t gi = 0;
+      uint32_t gi = 0, qi[2] = {0, 0};
       bool stop = false;
       for (int k = 0; !stop; ++k) {
         const int w = item_of(k);
         if (w < 0) break;
-        const ChunkTile tile = dp.chunk_tiles[w / shp.H_q];
-        const int kvh = (w % shp.H_q) / shp.g;
-        const int kb = tile.key_begin;
-        const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
-        const int n_kv = (ke - kb + kKeys - 1) / kKeys;
-        const int32_t* table = dp.block_ids + tile.table_off;
-        // cache rows of the boxes of KV tile j (-1: out-of-range block,
-        // skipped); looked up one tile ahead, so that the block-table loads
-        // overlap the wait for a free stage
-        int32_t rows[kKeys / 8];
-        int nsub = 0, loads = 0;
-        auto lookup = [&](int j) {
-          nsub = 0;
-          loads = 0;
+        const Item it = load_item(dp, w);
+        for (int x = 0; x < 2 && !stop; ++x) {
+          if (it.n[x] == 0) continue;
+          if (qi[x] > 0 &&
+              !ptx::mbar_wait(&bars->q_empty[x], (qi[x] - 1) & 1, kWaitLimit)) {
+            ptx::report_wait(dp.status, kDevTimeout, 41, k);
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          uint8_t* dst = q_s + x * kTileBytes;
+          const int row0 = dp.chunk_tiles[it.tile[x]].row_begin;
+          ptx::mbar_arrive_expect_tx(&bars->q_full[x], kTileBytes);
+          ptx::tma_load_2d(dst, &tmap_q, it.head[x] * 128, row0, &bars->q_full[x]);
+          ptx::tma_load_2d(dst + kHalf, &tmap_q, it.head[x] * 128 + 64, row0, &bars->q_full[x]);
+          ++qi[x];
+        }
+        const int32_t* table = dp.block_ids + dp.chunk_tiles[it.tile[0]].table_off;
+        for (int j = 0; j < it.nmax && !stop; ++j) {
+          // cache rows of the boxes of key tile j (-1: out-of-range block, skipped)
+          int32_t rows[kKeys / 8];
+          int nsub = 0, loads = 0;
           for (int r = 0; r < kKeys; r += box_rows) {
-            const int key = kb + j * kKeys + r;
-            if (key >= ke) break;
+            const int key = it.kb + j * kKeys + r;
+            if (key >= it.ke) break;
             const int32_t blk = table[key / B];
             if (blk < 0 || blk >= dp.num_blocks) {
               atomicCAS(dp.status, 0, kDevBounds);
               rows[nsub++] = -1;
               continue;
             }
-            rows[nsub++] = (blk * shp.H_kv + kvh) * B + (key % B);
+            rows[nsub++] = (blk * shp.H_kv + it.kv_head) * B + (key % B);
             ++loads;
           }
-        };
-        if (n_kv > 0) lookup(0);
-        for (int j = 0; j < n_kv; ++j, ++gi) {
-          const int s = gi % kStages;
-          if (*abort_flag) {
-            stop = true;
-            break;
+          for (int kv = 0; kv < 2; ++kv, ++gi) {
+            const int s = gi % kStages;
+            if (*abort_flag) {
+              stop = true;
+              break;
+            }
+            if (gi >= (uint32_t)kStages &&
+                !ptx::mbar_wait(&bars->kv_empty[s], ((gi / kStages) - 1) & 1, kWaitLimit)) {
+              ptx::report_wait(dp.status, kDevTimeout, 42, (int)gi);
+              *abort_flag = 1;
+              stop = true;
+              break;
+            }
+            const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+            uint8_t* dst = kv_s + s * kTileBytes;
+            ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 2));
+            for (int i = 0; i < nsub; ++i) {
+              if (rows[i] < 0) continue;
+              const int off = i * box_rows * 128;
+              ptx::tma_load_2d(dst + off, map, 0, rows[i], &bars->kv_full[s]);
+              ptx::tma_load_2d(dst + kHalf + off, map, 64, rows[i], &bars->kv_full[s]);
+            }
           }
-          if (gi >= (uint32_t)kStages &&
-              !ptx::mbar_wait(&bars->kv_empty[s], ((gi / kStages) - 1) & 1, kWaitLimit)) {
-            ptx::report_wait(dp.status, kDevTimeout, 21, (int)gi);
-            *abort_flag = 1;
-            stop = true;
-            break;
-          }
-          uint8_t* kdst = kv_s + s * kStage;
-          uint8_t* vdst = kdst + kKVTile;
-          ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 4));
-          for (int i = 0; i < nsub; ++i) {
-            if (rows[i] < 0) continue;
-            const int off = i * box_rows * 128;
-            ptx::tma_load_2d(kdst + off, &tmap_k, 0, rows[i], &bars->kv_full[s]);
-            ptx::tma_load_2d(kdst + kKVHalf + off, &tmap_k, 64, rows[i], &bars->kv_full[s]);
-            ptx::tma_load_2d(vdst + off, &tmap_v, 0, rows[i], &bars->kv_full[s]);
-            ptx::tma_load_2d(vdst + kKVHalf + off, &tmap_v, 64, rows[i], &bars->kv_full[s]);
-          }
-          if (j + 1 < n_kv) lookup(j + 1);
         }
       }
       // every copy must land before the CTA may exit
       for (uint32_t t = gi > (uint32_t)kStages ? gi - kStages : 0; t < gi; ++t)
         ptx::mbar_wait(&bars->kv_full[t % kStages], (t / kStages) & 1, kWaitLimit);
+      for (int x = 0; x < 2; ++x)
+        if (qi[x] > 0) ptx::mbar_wait(&bars->q_full[x], (qi[x] - 1) & 1, kWaitLimit);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
       constexpr uint32_t idesc_o = instr_desc(kRows, 128, 1);
+      const uint32_t q_addr = ptx::smem_u32(q_s);
       const uint32_t kv_addr = ptx::smem_u32(kv_s);
-      auto issue_qk = [&](uint32_t t) {
-        const uint32_t kt = kv_addr + (t % kStages) * kStage;
-        const uint32_t d = tmem + (t & 1) * kKeys;
+      // S_X = Q_X K^T into tile X's S columns (after the previous PV of tile X
+      // read P_X over the same columns: MMAs of one thread run in order)
+      auto issue_qk = [&](int x, uint32_t gk, bool last) {
+        const uint32_t qt = q_addr + x * kTileBytes;
+        const uint32_t kt = kv_addr + (gk % kStages) * kTileBytes;
+        const uint32_t d = tmem + x * kTileCols;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          // head dims 16kk .. 16kk+15: Q columns 8kk.., K's half kk/4, 32-byte step kk%4;
-          // N = all 128 keys of the tile
-          const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-          tc_mma_ts(d, tmem + kQCol + kk * 8, smem_desc(kt + ko, 16, 1024), idesc_s, kk > 0);
+          // head dims 16kk .. 16kk+15: the half kk/4 of Q and K, 32-byte step kk%4
+          const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc_mma_ss(d, smem_desc(qt + ko, 16, 1024), smem_desc(kt + ko, 16, 1024), idesc_s,
+                    kk > 0);
         }
-        tc_commit(&bars->s_full[t & 1]);
+        tc_commit(&bars->s_full[x]);
+        if (last) tc_commit(&bars->q_empty[x]);
+      };
+      // O_X += P_X V
+      auto issue_pv = [&](int x, uint32_t gv, bool acc) {
+        const uint32_t vt = kv_addr + (gv % kStages) * kTileBytes;
+        const uint32_t pt = tmem + x * kTileCols;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
+          tc_mma_ts(pt + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kHalf, 1024), idesc_o,
+                    acc || kk > 0);
+        }
+        tc_commit(&bars->o_done[x]);
       };
       bool ok = true;
       int site = 0, at = 0;
-      uint32_t gi = 0;
-      long long pv_last = -1;   // the last PV issued (its tile number)
+      uint32_t gi = 0, qi[2] = {0, 0}, c[2] = {0, 0}, oi[2] = {0, 0};
+      auto wait_bar = [&](uint64_t* bar, uint32_t parity, int where, int index) {
+        if (!ptx::mbar_wait(bar, parity, kWaitLimit) || *abort_flag) {
+          ok = false;
+          site = where;
+          at = index;
+          return false;
+        }
+        tc_fence_after();
+        return true;
+      };
       for (int k = 0; ok; ++k) {
         const int w = item_of(k);
         if (w < 0) break;
-        const ChunkTile tile = dp.chunk_tiles[w / shp.H_q];
-        const int kb = tile.key_begin;
-        const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
-        const int n_kv = (ke - kb + kKeys - 1) / kKeys;
-        // this item's Q rows are in tensor memory
-        if (!ptx::mbar_wait(&bars->q_full, k & 1, kWaitLimit) || *abort_flag) {
-          ok = false;
-          site = 22;
-          at = k;
+        const Item it = load_item(dp, w);
+        const uint32_t base = gi;
+        gi += 2 * it.nmax;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (it.n[x] == 0) continue;
+          if (wait_bar(&bars->q_full[x], qi[x] & 1, 43, k)) ++qi[x];
+        }
+        // K_0: the first QK^T of both tiles
+        if (!ok || !wait_bar(&bars->kv_full[base % kStages], (base / kStages) & 1, 44, (int)base))
           break;
-        }
-        tc_fence_after();
-        if (n_kv > 0) {
-          if (!ptx::mbar_wait(&bars->kv_full[gi % kStages], (gi / kStages) & 1, kWaitLimit)) {
-            ok = false;
-            site = 23;
-            at = (int)gi;
-            break;
-          }
-          tc_fence_after();
-          issue_qk(gi);
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const uint32_t t = gi + j;
-          if (j + 1 < n_kv) {
-            if (!ptx::mbar_wait(&bars->kv_full[(t + 1) % kStages], ((t + 1) / kStages) & 1,
-                                kWaitLimit)) {
-              ok = false;
-              site = 24;
-              at = (int)t + 1;
+        for (int x = 0; x < 2; ++x)
+          if (it.n[x] > 0) issue_qk(x, base, it.n[x] == 1);
+        tc_commit(&bars->kv_empty[base % kStages]);
+        // then per key tile j: PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1), each tile's
+        // products as soon as its softmax has written P
+        for (int j = 0; ok && j < it.nmax; ++j) {
+          const uint32_t gv = base + 2 * j + 1, gk = gv + 1;
+          bool v_in = false, k_in = false;
+          for (int x = 0; ok && x < 2; ++x) {
+            if (j >= it.n[x]) continue;
+            if (!wait_bar(&bars->p_full[x], c[x] & 1, 46, (int)c[x])) break;
+            if (j == 0 && oi[x] > 0 &&   // the previous item's epilogue must have read O_X
+                !wait_bar(&bars->o_free[x], (oi[x] - 1) & 1, 47, (int)oi[x]))
               break;
+            if (!v_in && !wait_bar(&bars->kv_full[gv % kStages], (gv / kStages) & 1, 45, (int)gv))
+              break;
+            v_in = true;
+            issue_pv(x, gv, j > 0);
+            ++c[x];
+            if (j + 1 < it.n[x]) {
+              if (!k_in && !wait_bar(&bars->kv_full[gk % kStages], (gk / kStages) & 1, 48, (int)gk))
+                break;
+              k_in = true;
+              issue_qk(x, gk, j + 2 == it.n[x]);
             }
-            tc_fence_after();
-            issue_qk(t + 1);
           }
-          if (!ptx::mbar_wait(&bars->p_full[t & 1], (t >> 1) & 1, kWaitLimit) || *abort_flag) {
-            ok = false;
-            site = 25;
-            at = (int)t;
-            break;
+          if (!ok) break;
+          // a stage is released once every product that reads it was issued
+          tc_commit(&bars->kv_empty[gv % kStages]);
+          if (j + 1 < it.nmax) {
+            if (!k_in && !wait_bar(&bars->kv_full[gk % kStages], (gk / kStages) & 1, 49, (int)gk))
+              break;
+            tc_commit(&bars->kv_empty[gk % kStages]);
           }
-          tc_fence_after();
-          const uint32_t vt = kv_addr + (t % kStages) * kStage + kKVTile;
-          const uint32_t pt = tmem + (t & 1) * kKeys;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
-            tc_mma_ts(tmem + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kKVHalf, 1024),
-                      idesc_o, j > 0 || kk > 0);
-          }
-          tc_commit(&bars->o_done[t & 1]);
-          tc_commit(&bars->kv_empty[t % kStages]);
-          pv_last = t;
         }
-        gi += n_kv;
+        for (int x = 0; x < 2; ++x)
+          if (it.n[x] > 0) ++oi[x];
       }
       if (!ok) {
         ptx::report_wait(dp.status, kDevTimeout, site, at);
         *abort_flag = 1;
       }
-      // the last PV (and so every earlier one) must finish before TMEM is released
-      if (pv_last >= 0)
-        ptx::mbar_wait(&bars->o_done[pv_last & 1], (pv_last >> 1) & 1, kWaitLimit);
+      // the last PV of each tile (and so every earlier MMA) must finish before
+      // tensor memory is released
+      for (int x = 0; x < 2; ++x)
+        if (c[x] > 0) ptx::mbar_wait(&bars->o_done[x], (c[x] - 1) & 1, kWaitLimit);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax warps
-    const int row = threadIdx.x;                      // 0..127 = TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int x = warp >> 2;                          // query tile of this warpgroup
+    const int row = threadIdx.x & 127;                // 0..127 = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + x * kTileCols;
     const float qk_scale = shp.scale * kLog2e;
-    uint32_t gi = 0;
+    uint32_t cnt = 0, gbase = 0;
     bool ok = true;
     int site = 0, at = 0;
     for (int k = 0; ok; ++k) {
       const int w = item_of(k);
       if (w < 0) break;
-      const ChunkTile tile = dp.chunk_tiles[w / shp.H_q];
-      const int h = w % shp.H_q;
-      const int kvh = h / shp.g;
-      const int kb = tile.key_begin;
-      const int ke = min(tile.key_end, tile.pos_begin + tile.n_rows);
-      const int n_kv = (ke - kb + kKeys - 1) / kKeys;
-      const int pos = tile.pos_begin + row;           // position of this query row
-      {
-        // this thread's query row -> tensor memory (the QK^T A operand); rows
-        // past the tile's end are zero.  The previous item's MMAs have all
-        // finished (its epilogue waited for its last PV).
-        float qv[64];
-        uint4* q4 = reinterpret_cast<uint4*>(qv);
-        if (row < tile.n_rows) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              q + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) q4[i] = src[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) q4[i] = make_uint4(0, 0, 0, 0);
-        }
-        tmem_st32(lane_base + kQCol, qv);
-        tmem_st32(lane_base + kQCol + 32, qv + 32);
-        tmem_wait_st();
-        tc_fence_before();
-        ptx::mbar_arrive(&bars->q_full);
+      const Item it = load_item(dp, w);
+      const int nx = it.n[x];
+      if (nx == 0) {
+        gbase += 2 * it.nmax;
+        continue;
       }
+      const ChunkTile tile = dp.chunk_tiles[it.tile[x]];
+      const int h = it.head[x];
+      const int kb = it.kb;
+      const int ke = tile.key_end;
+      const int pos = tile.pos_begin + row;           // position of this query row
+      const uint32_t g_item = gbase;                  // ring index of the item's K_0
+      gbase += 2 * it.nmax;
+      // keys past the item's end in its last key tile may be anything (unwritten
+      // cache slots, and 0 * NaN is NaN): they are zeroed in V, before any PV
+      // reads that tile, by A's warpgroup when A reads it (the issuer runs A's
+      // PV first), else by B's
+      const bool zeroer = (x == 0) ? (nx == it.nmax) : (it.n[0] != it.nmax);
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < n_kv; ++j) {
-        const uint32_t t = gi + j;
+      for (int j = 0; j < nx; ++j) {
+        const uint32_t t = cnt + j;
         // tcgen05.ld/st are warp-collective: every decision below is warp-uniform
-        const bool got = ptx::mbar_wait(&bars->s_full[t & 1], (t >> 1) & 1, kWaitLimit);
+        const bool got = ptx::mbar_wait(&bars->s_full[x], t & 1, kWaitLimit);
         if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *abort_flag != 0)) {
           ok = false;
-          site = 31;
+          site = 51;
           at = (int)t;
           break;
         }
         tc_fence_after();
-        const uint32_t s_col = lane_base + (t & 1) * kKeys;  // S of tile t; then its P
+        const uint32_t s_col = lane_base;               // S of key tile j; then its P
         const int key0 = kb + j * kKeys;
         // this row sees the tile's first `lim` keys: those <= its position and
-        // before the split's end (a prefix of the tile, possibly empty or all)
+        // before its tile's end (a prefix of the key tile, possibly empty or all)
         const int lim = min(pos + 1, ke) - key0;
         const bool full = __all_sync(0xffffffffu, lim >= kKeys);
-        // row max over 8 independent partial maxima, in two 64-key halves (the
-        // second half first, so that the first stays in registers)
-        float sc[64];
+        // the whole row of scores in one round trip (four loads, one wait)
+        float sc[128];
+        tmem_ld32(s_col, sc);
+        tmem_ld32(s_col + 32, sc + 32);
+        tmem_ld32(s_col + 64, sc + 64);
+        tmem_ld32(s_col + 96, sc + 96);
+        tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) sc[c] = c < lim ? sc[c] : -INFINITY;
+        }
+        // row max over 8 independent partial maxima
         float mx8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+        for (int u = 0; u < 8; ++u) mx8[u] = sc[u];
 #pragma unroll
-        for (int hf = 1; hf >= 0; --hf) {
-          tmem_ld32(s_col + hf * 64, sc);
-          tmem_ld32(s_col + hf * 64 + 32, sc + 32);
-          tmem_wait_ld();
-          const int lh = lim - hf * 64;
-          if (full) {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              mx8[c & 7] = fmaxf(mx8[c & 7], c < lh ? sc[c] : -INFINITY);
-          }
-        }
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
         const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         // the scale is positive, so the row max scales with it
@@ -485,52 +463,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rescaling O needs every earlier PV of this item finished (only when
         // a row's max rose)
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          const bool done =
-              ptx::mbar_wait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, kWaitLimit);
+          const bool done = ptx::mbar_wait(&bars->o_done[x], (t - 1) & 1, kWaitLimit);
           if (!__all_sync(0xffffffffu, done)) {
             ok = false;
-            site = 33;
+            site = 53;
             at = (int)t;
             break;
           }
           tc_fence_after();
-          {
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              float ov[32];
-              tmem_ld32(lane_base + kOCol + c4 * 32, ov);
-              tmem_wait_ld();
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float ov[32];
+            tmem_ld32(lane_base + kOCol + c4 * 32, ov);
+            tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < 32; ++c) ov[c] *= corr;
-              tmem_st32(lane_base + kOCol + c4 * 32, ov);
-            }
-            tmem_wait_st();
+            for (int c = 0; c < 32; ++c) ov[c] *= corr;
+            tmem_st32(lane_base + kOCol + c4 * 32, ov);
           }
+          tmem_wait_st();
         }
-        // a row with no key in this split so far keeps m_ref = -inf: its p are 0
+        // a row with no key in this piece so far keeps m_ref = -inf: its p are 0
         const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
         float ps8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+        // P as bf16 pairs over the first 64 S columns (already read), 64 keys
+        // (32 columns) per store
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          if (hf == 1) {
-            tmem_ld32(s_col + 64, sc);
-            tmem_ld32(s_col + 96, sc + 32);
-            tmem_wait_ld();
-          }
-          const int lh = lim - hf * 64;
-          if (!full) {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) sc[c] = c < lh ? sc[c] : -INFINITY;
-          }
-          // P of these 64 keys as bf16 pairs over S columns already read
           float pk[32];
           uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float p0 = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
-            const float p1 = ptx::ex2(fmaf(sc[c + 1], qk_scale, nbase));
+            const float p0 = ptx::ex2(fmaf(sc[hf * 64 + c], qk_scale, nbase));
+            const float p1 = ptx::ex2(fmaf(sc[hf * 64 + c + 1], qk_scale, nbase));
             ps8[c & 7] += p0;
             ps8[(c + 1) & 7] += p1;
             pk32[c / 2] = ptx::pack_bf16x2(p0, p1);
@@ -541,76 +507,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ps =
             ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
         l = l * corr + ps;
-        if (j == n_kv - 1 && (ke % kKeys) != 0) {
-          // keys past the split's end may be anything (unwritten slots): zero their V rows
-          const int s = t % kStages;
-          ptx::mbar_wait(&bars->kv_full[s], (t / kStages) & 1, kWaitLimit);
-          uint8_t* vt = kv_s + s * kStage + kKVTile;
-          const int valid = ke - key0;
+        if (zeroer && j == it.nmax - 1 && (it.ke % kKeys) != 0) {
+          const uint32_t gv = g_item + 2 * j + 1;     // ring index of V_j
+          const int s = gv % kStages;
+          const bool landed = ptx::mbar_wait(&bars->kv_full[s], (gv / kStages) & 1, kWaitLimit);
+          if (!__all_sync(0xffffffffu, landed)) {
+            ok = false;
+            site = 52;
+            at = (int)gv;
+            break;
+          }
+          uint8_t* vt = kv_s + s * kTileBytes;
+          const int valid = it.ke - key0;
           for (int e = row; e < (kKeys - valid) * 16; e += kRows) {
             const int key = valid + e / 16, c = e % 16;
-            *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVHalf + key * 128 + ((c & 7) << 4)) =
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalf + key * 128 + ((c & 7) << 4)) =
                 make_uint4(0, 0, 0, 0);
           }
-          // the PV MMA reads these rows through the async proxy
+          // the PV MMAs read these rows through the async proxy
           ptx::fence_proxy_async_smem();
         }
         tc_fence_before();
-        ptx::mbar_arrive(&bars->p_full[t & 1]);
+        ptx::mbar_arrive(&bars->p_full[x]);
       }
-      bool fin = ok;
-      if (fin && n_kv > 0) {
-        const uint32_t tl = gi + n_kv - 1;
-        fin = ptx::mbar_wait(&bars->o_done[tl & 1], (tl >> 1) & 1, kWaitLimit);
+      if (!ok) break;
+      const uint32_t tl = cnt + nx - 1;
+      cnt += nx;
+      const bool fin = ptx::mbar_wait(&bars->o_done[x], tl & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, fin)) {
+        ok = false;
+        site = 54;
+        at = (int)tl;
+        break;
       }
-      if (__all_sync(0xffffffffu, fin)) {
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const bool store = row < tile.n_rows;
-        const bool partial = tile.part_base >= 0;
-        __nv_bfloat16* orow = o + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128;
-        // partial slot of (row, KV head, split); query head h % g inside it
-        const int64_t slot =
-            ((int64_t)tile.part_base + ((int64_t)row * shp.H_kv + kvh) * tile.nsplit +
-             tile.split) * shp.g + (h % shp.g);
-        float* prow = part_o + slot * 128;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = row < tile.n_rows;
+      const bool partial = tile.part_base >= 0;
+      const int kvh = it.kv_head;
+      __nv_bfloat16* orow = o + ((int64_t)(tile.row_begin + row) * shp.H_q + h) * 128;
+      // partial slot of (row, KV head, split); query head h % g inside it
+      const int64_t slot =
+          ((int64_t)tile.part_base + ((int64_t)row * shp.H_kv + kvh) * tile.nsplit + tile.split) *
+              shp.g + (h % shp.g);
+      float* prow = part_o + slot * 128;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float ov[32];
-          if (n_kv > 0) {
-            tmem_ld32(lane_base + kOCol + c4 * 32, ov);
-            tmem_wait_ld();
-          } else {
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float ov[32];
+        tmem_ld32(lane_base + kOCol + c4 * 32, ov);
+        tmem_wait_ld();
+        if (store && !partial) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = 0.f;   // an empty key range: no PV ran
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 v;
+            v.x = ptx::pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
+            v.y = ptx::pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
+            v.z = ptx::pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
+            v.w = ptx::pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = v;
           }
-          if (store && !partial) {
+        } else if (store) {
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              uint4 v;
-              v.x = ptx::pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
-              v.y = ptx::pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
-              v.z = ptx::pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
-              v.w = ptx::pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
-              *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = v;
-            }
-          } else if (store) {
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-              *reinterpret_cast<float4*>(prow + c4 * 32 + c8 * 4) =
-                  make_float4(ov[c8 * 4 + 0] * inv, ov[c8 * 4 + 1] * inv, ov[c8 * 4 + 2] * inv,
-                              ov[c8 * 4 + 3] * inv);
-          }
-        }
-        if (store && partial) part_lse[slot] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-      } else {
-        if (ok) {
-          ok = false;
-          site = 34;
-          at = (int)(gi + n_kv);
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<float4*>(prow + c4 * 32 + c8 * 4) =
+                make_float4(ov[c8 * 4 + 0] * inv, ov[c8 * 4 + 1] * inv, ov[c8 * 4 + 2] * inv,
+                            ov[c8 * 4 + 3] * inv);
         }
       }
-      gi += n_kv;
+      if (store && partial) part_lse[slot] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+      // O_X has been read: the next item's first PV may overwrite it
+      tc_fence_before();
+      ptx::mbar_arrive(&bars->o_free[x]);
     }
     if (!ok) {
       ptx::report_wait(dp.status, kDevTimeout, site, at);
@@ -618,10 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // all roles done (every wait above is bounded): release TMEM
+  // all roles done (every wait above is bounded): release tensor memory
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -644,19 +611,30 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   if (dp.n_chunk == 0) return cudaSuccess;
   if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
     return cudaErrorMisalignedAddress;
+  if (dp.chunk_single)
+    return launch_chunk_single(dp, s, q, k_cache, v_cache, o, part_o, part_lse, st,
+                               overlap_previous, wait_first);
   const int64_t rows = (int64_t)dp.num_blocks * s.H_kv * s.B;
   const int box_rows = s.B < kKeys ? s.B : kKeys;
-  CUtensorMap tk, tv;
-  cudaError_t e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
+  CUtensorMap tq, tk, tv;
+  // Q as [T][H_q * 128]: a query tile is the box at (head * 128, first row),
+  // 128 rows high; rows past the end of Q read as zero
+  cudaError_t e = make_tmap_2d(&tq, q, dp.num_tokens, (int64_t)s.H_q * 128, kRows);
+  if (e == cudaSuccess) e = make_cache_tmap(&tk, k_cache, rows, s.D, box_rows);
   if (e == cudaSuccess) e = make_cache_tmap(&tv, v_cache, rows, s.D, box_rows);
   if (e != cudaSuccess) return e;
   // the shared-memory limit is raised once per device
   static std::atomic<uint64_t> attr_done{0};
-  int attr_dev = 0;
-  e = cudaGetDevice(&attr_dev);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t attr_bit = 1ull << (attr_dev & 63);
+  const uint64_t attr_bit = 1ull << (dev & 63);
   if (!(attr_done.load() & attr_bit)) {
+    // the register split assumes the kernel was built at kLaunchRegs a thread
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, chunk_attn_tcgen05_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
     e = cudaFuncSetAttribute(chunk_attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e == cudaSuccess)
@@ -666,19 +644,15 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(attr_bit);
   }
-  // persistent: at most one CTA per SM, each walking (tile, head) items
+  // persistent: at most one CTA per SM, each walking work items
   static int sms_of[64] = {0};
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   int sms = dev < 64 ? sms_of[dev] : 0;
   if (sms == 0) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (dev < 64) sms_of[dev] = sms;
   }
-  const int64_t items = (int64_t)dp.n_chunk * s.H_q;
-  dim3 grid((unsigned)std::min<int64_t>(items, std::max(1, sms)));
+  dim3 grid((unsigned)std::min<int64_t>(dp.n_chunk, std::max(1, sms)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
@@ -689,9 +663,8 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_tcgen05_kernel, tk, tv, dp, s,
-                            (const __nv_bfloat16*)q, (__nv_bfloat16*)o, part_o, part_lse,
-                            wait_first ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tcgen05_kernel, tq, tk, tv, dp, s,
+                            (__nv_bfloat16*)o, part_o, part_lse, wait_first ? 1 : 0);
 }
 
 }  // namespace rbkv

@@ -170,10 +170,12 @@ struct Plan {
   rbkv_plan_info info{};
   std::vector<WorkItem> decode, generic;
   std::vector<ChunkTile> chunk;
+  std::vector<ChunkItem> chunk_items;
   std::vector<CombineRow> combine;
   int32_t n_parts = 0;
   int32_t decode_grid = 0;
   int32_t decode_packed = 0;  // some decode units pack several prompt rows
+  int32_t chunk_single = 0;   // chunk items hold one query tile each
 };
 
 }  // namespace
@@ -278,26 +280,37 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
     split = std::max<int32_t>(512, round_up(std::max<int64_t>(target, 1), gran));
   }
 
-  // prompt-chunk tiles (one CTA per 128-row tile and query head, one CTA per
-  // SM): their key ranges are split only when there are fewer tiles x heads
-  // than SMs, into pieces that bring the count up to about one full wave
+  // prompt chunks: 128-row query tiles in work items.  When there are at
+  // least as many pairs of tiles that read the same K/V tiles (two query heads
+  // of a KV group, or two consecutive row tiles for groups of one) as SMs,
+  // items are such pairs (the paired kernel overlaps one tile's softmax with
+  // the other's products); otherwise items hold one tile and query head each
+  // (the one-tile kernel, whose double-buffered scores overlap each tile's
+  // softmax with its own next product), and a chunk's key range is split only
+  // when even those are fewer than SMs, into pieces that bring the count up to
+  // about one full wave.  The persistent grid has one CTA per SM.
   int32_t chunk_split = 0x7fffffff;
-  if (p.split_keys > 0) {
-    chunk_split = round_up(p.split_keys, kChunkTileKeys);
-  } else if (fast_chunk) {
-    int64_t pairs = 0;
+  bool chunk_single = false;
+  if (fast_chunk) {
+    int64_t pairs = 0, singles = 0;
     int32_t max_keys = 0;
     for (int32_t i = 0; i < S; ++i) {
       if (p.n_new[i] <= 1) continue;
-      pairs += (int64_t)ceil_div(p.n_new[i], kChunkTileRows) * s.H_q;
+      const int64_t tiles = ceil_div(p.n_new[i], kChunkTileRows);
+      pairs += s.g >= 2 ? tiles * s.H_kv * ceil_div(s.g, 2) : ceil_div(tiles, 2) * s.H_q;
+      singles += tiles * s.H_q;
       max_keys = std::max(max_keys, p.ctx[i]);
     }
-    if (pairs > 0 && pairs < num_sms) {
-      const int32_t per = std::max<int32_t>(1, (int32_t)(num_sms / pairs));
+    chunk_single = pairs < num_sms;
+    if (p.split_keys > 0) {
+      chunk_split = round_up(p.split_keys, kChunkTileKeys);
+    } else if (singles > 0 && singles < num_sms) {
+      const int32_t per = std::max<int32_t>(1, (int32_t)(num_sms / singles));
       chunk_split = std::max<int32_t>(kChunkMinSplitKeys,
                                       round_up(ceil_div(max_keys, per), kChunkTileKeys));
     }
   }
+  pl.chunk_single = chunk_single ? 1 : 0;
   std::vector<int32_t> bounds;
   std::vector<WorkItem> decode, generic;
   int32_t max_splits = 0;
@@ -311,6 +324,7 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   };
   std::vector<Piece> pieces;
   pieces.reserve((size_t)S * 2);
+  std::vector<int32_t> tile_of;   // chunk tile of (row tile, key piece), or -1
   auto add_decode_row = [&](int32_t row, int32_t n_keys, int32_t table_off) {
     split_keys(n_keys, split, gran, bounds);
     const int32_t ns = (int32_t)bounds.size() - 1;
@@ -359,15 +373,21 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
       max_splits = std::max(max_splits, 1);
       pl.decode_packed = 1;
     } else if (fast_chunk) {
-      // 128-row tiles; a tile's key range [0, last position + 1) is cut into
-      // 128-key-aligned pieces of at most `chunk_split` keys, merged later by
-      // the log-sum-exp combine like split decode rows
-      for (int32_t r = 0; r < p.n_new[i]; r += kChunkTileRows) {
+      // the chunk's keys [0, ctx) are cut into 128-key-aligned pieces of at
+      // most `chunk_split` keys; 128-row tile t takes from piece k the keys
+      // below its own causal end (pieces that start past it are left out), and
+      // a tile with several pieces has them merged by the log-sum-exp combine
+      split_keys(p.ctx[i], chunk_split, kChunkTileKeys, bounds);
+      const int32_t npiece = (int32_t)bounds.size() - 1;
+      const int32_t ntile = ceil_div(p.n_new[i], kChunkTileRows);
+      tile_of.assign((size_t)ntile * npiece, -1);
+      for (int32_t t = 0; t < ntile; ++t) {
+        const int32_t r = t * kChunkTileRows;
         const int32_t n = std::min(kChunkTileRows, p.n_new[i] - r);
         const int32_t pos0 = p.seen[i] + r;
-        const int32_t n_keys = pos0 + n;
-        split_keys(n_keys, chunk_split, kChunkTileKeys, bounds);
-        const int32_t ns = (int32_t)bounds.size() - 1;
+        const int32_t tile_end = pos0 + n;
+        int32_t ns = 0;
+        while (ns < npiece && bounds[ns] < tile_end) ++ns;
         max_splits = std::max(max_splits, ns);
         int32_t part0 = -1;
         if (ns > 1) {
@@ -378,9 +398,54 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
               pl.combine.push_back(
                   CombineRow{p.q_start[i] + r + rr, h, part0 + (rr * s.H_kv + h) * ns, ns});
         }
-        for (int32_t k = 0; k < ns; ++k)
+        for (int32_t k = 0; k < ns; ++k) {
+          tile_of[(size_t)t * npiece + k] = (int32_t)pl.chunk.size();
           pl.chunk.push_back(ChunkTile{p.block_start[i], p.q_start[i] + r, n, pos0, bounds[k],
-                                       bounds[k + 1], part0, k, ns, {0, 0, 0}});
+                                       std::min(bounds[k + 1], tile_end), part0, k, ns,
+                                       {0, 0, 0}});
+        }
+      }
+      auto key_end_of = [&](int32_t a, int32_t b) {
+        const int32_t ea = a >= 0 ? pl.chunk[a].key_end : 0;
+        const int32_t eb = b >= 0 ? pl.chunk[b].key_end : 0;
+        return std::max(ea, eb);
+      };
+      for (int32_t k = 0; k < npiece; ++k) {
+        if (chunk_single) {
+          // one tile and query head per item
+          for (int32_t t = 0; t < ntile; ++t) {
+            const int32_t c = tile_of[(size_t)t * npiece + k];
+            if (c < 0) continue;
+            for (int32_t h = 0; h < s.H_q; ++h)
+              pl.chunk_items.push_back(ChunkItem{{c, -1}, {h, 0}, h / s.g,
+                                                 pl.chunk[c].key_begin, pl.chunk[c].key_end, 0});
+          }
+        } else if (s.g >= 2) {
+          // each tile with two query heads of a KV group per item
+          for (int32_t t = 0; t < ntile; ++t) {
+            const int32_t c = tile_of[(size_t)t * npiece + k];
+            if (c < 0) continue;
+            for (int32_t h = 0; h < s.H_kv; ++h)
+              for (int32_t q = 0; q < s.g; q += 2) {
+                const bool two = q + 1 < s.g;
+                pl.chunk_items.push_back(ChunkItem{{c, two ? c : -1},
+                                                   {h * s.g + q, two ? h * s.g + q + 1 : 0}, h,
+                                                   pl.chunk[c].key_begin, pl.chunk[c].key_end,
+                                                   0});
+              }
+          }
+        } else {
+          // groups of one: two consecutive row tiles of one head per item
+          for (int32_t t = 0; t < ntile; t += 2) {
+            int32_t a = tile_of[(size_t)t * npiece + k];
+            int32_t b = t + 1 < ntile ? tile_of[(size_t)(t + 1) * npiece + k] : -1;
+            if (a < 0) { a = b; b = -1; }
+            if (a < 0) continue;
+            for (int32_t h = 0; h < s.H_q; ++h)
+              pl.chunk_items.push_back(ChunkItem{{a, b}, {h, h}, h, bounds[k], key_end_of(a, b),
+                                                 0});
+          }
+        }
       }
     } else {
       for (int32_t j = 0; j < p.n_new[i]; ++j)
@@ -400,9 +465,10 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
     return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
   };
   std::stable_sort(generic.begin(), generic.end(), longer);
-  std::stable_sort(pl.chunk.begin(), pl.chunk.end(), [](const ChunkTile& a, const ChunkTile& b) {
-    return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
-  });
+  std::stable_sort(pl.chunk_items.begin(), pl.chunk_items.end(),
+                   [](const ChunkItem& a, const ChunkItem& b) {
+                     return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+                   });
   int32_t grid = (int32_t)std::min<int64_t>((int64_t)decode.size(),
                                             (int64_t)std::max(1, num_sms) * decode_ctas_per_sm(s));
   if (grid > 0) snake_order(decode, grid);
@@ -419,6 +485,7 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   in.partials = pl.n_parts;
   in.chunk_rows = chunk_rows;
   in.chunk_tiles = (int32_t)pl.chunk.size();
+  in.chunk_items = (int32_t)pl.chunk_items.size();
   in.generic_items = (int32_t)pl.generic.size();
   in.fast_decode = fast_decode ? 1 : 0;
   in.fast_chunk = fast_chunk ? 1 : 0;
@@ -470,6 +537,7 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     const size_t o_dec = section(pl.decode.size() * sizeof(WorkItem));
     const size_t o_gen = section(pl.generic.size() * sizeof(WorkItem));
     const size_t o_chunk = section(pl.chunk.size() * sizeof(ChunkTile));
+    const size_t o_items = section(pl.chunk_items.size() * sizeof(ChunkItem));
     const size_t o_comb = section(pl.combine.size() * sizeof(CombineRow));
     const size_t bytes = words * 4;
     PinnedBuf pin;
@@ -485,6 +553,7 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     fill(o_dec, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
     fill(o_gen, pl.generic.data(), pl.generic.size() * sizeof(WorkItem));
     fill(o_chunk, pl.chunk.data(), pl.chunk.size() * sizeof(ChunkTile));
+    fill(o_items, pl.chunk_items.data(), pl.chunk_items.size() * sizeof(ChunkItem));
     fill(o_comb, pl.combine.data(), pl.combine.size() * sizeof(CombineRow));
     void* dev = nullptr;
     e = cudaMallocAsync(&dev, bytes, st);
@@ -511,16 +580,18 @@ rbkv_status ensure_device(rbkv_pass* p, cudaStream_t st) {
     dp.decode_items = (const WorkItem*)(base + o_dec);
     dp.generic_items = (const WorkItem*)(base + o_gen);
     dp.chunk_tiles = (const ChunkTile*)(base + o_chunk);
+    dp.chunk_items = (const ChunkItem*)(base + o_items);
     dp.combine_rows = (const CombineRow*)(base + o_comb);
     dp.num_tokens = (int32_t)p->slot.size();
     dp.n_decode = (int32_t)pl.decode.size();
     dp.n_generic = (int32_t)pl.generic.size();
-    dp.n_chunk = (int32_t)pl.chunk.size();
+    dp.n_chunk = (int32_t)pl.chunk_items.size();
     dp.n_combine = (int32_t)pl.combine.size();
     dp.n_parts = pl.n_parts;
     dp.num_blocks = p->cfg.num_blocks;
     dp.decode_grid = pl.decode_grid;
     dp.decode_packed = pl.decode_packed;
+    dp.chunk_single = pl.chunk_single;
   } else if (st != p->upload_stream) {
     cudaError_t e = cudaStreamWaitEvent(st, p->upload_ev, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
@@ -993,7 +1064,8 @@ struct rbkv_frame {
   int sms = 0;
   int32_t* dev = nullptr;   // device words: status[4] | counts[8] | sections
   size_t words = 0;
-  size_t o_slot = 0, o_blocks = 0, o_dec = 0, o_chunk = 0, o_comb = 0;
+  size_t o_slot = 0, o_blocks = 0, o_dec = 0, o_chunk = 0, o_items = 0, o_comb = 0;
+  int32_t max_items = 0;   // chunk work items: max_chunk_tiles x num_heads_q
   static constexpr int kStages = 4;
   int32_t* host[kStages] = {};   // pinned staging, same layout
   cudaEvent_t ev[kStages] = {};
@@ -1064,6 +1136,8 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   f->o_blocks = w; w = align4(w + (size_t)c.max_blocks);
   f->o_dec = w;    w = align4(w + (size_t)c.max_decode_items * (sizeof(WorkItem) / 4));
   f->o_chunk = w;  w = align4(w + (size_t)c.max_chunk_tiles * (sizeof(ChunkTile) / 4));
+  f->max_items = (int32_t)std::min<int64_t>((int64_t)c.max_chunk_tiles * s.H_q, 1 << 28);
+  f->o_items = w;  w = align4(w + (size_t)f->max_items * (sizeof(ChunkItem) / 4));
   f->o_comb = w;   w = align4(w + (size_t)c.max_combine_rows * (sizeof(CombineRow) / 4));
   f->words = w;
   e = cudaMalloc((void**)&f->dev, w * 4);
@@ -1084,11 +1158,12 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   dp.decode_items = (const WorkItem*)(base + f->o_dec);
   dp.generic_items = nullptr;
   dp.chunk_tiles = (const ChunkTile*)(base + f->o_chunk);
+  dp.chunk_items = (const ChunkItem*)(base + f->o_items);
   dp.combine_rows = (const CombineRow*)(base + f->o_comb);
   dp.num_tokens = c.max_tokens;
   dp.n_decode = c.max_decode_items;
   dp.n_generic = 0;
-  dp.n_chunk = c.max_chunk_tiles;
+  dp.n_chunk = f->max_items;
   dp.n_combine = c.max_combine_rows;
   dp.n_parts = c.max_parts;
   dp.num_blocks = cfg->num_blocks;
@@ -1127,6 +1202,9 @@ rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
       return over("max_decode_items", pl->decode.size(), c.max_decode_items);
     if (pl->chunk.size() > (size_t)c.max_chunk_tiles)
       return over("max_chunk_tiles", pl->chunk.size(), c.max_chunk_tiles);
+    if (pl->chunk_items.size() > (size_t)f->max_items)
+      return over("chunk items (max_chunk_tiles x num_heads_q)", pl->chunk_items.size(),
+                  f->max_items);
     if (pl->combine.size() > (size_t)c.max_combine_rows)
       return over("max_combine_rows", pl->combine.size(), c.max_combine_rows);
     if (pl->n_parts > c.max_parts) return over("max_parts", (size_t)pl->n_parts, c.max_parts);
@@ -1137,7 +1215,7 @@ rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
                   "created without packed_units");
     counts[kCountTokens] = (int32_t)p->slot.size();
     counts[kCountDecode] = (int32_t)pl->decode.size();
-    counts[kCountChunk] = (int32_t)pl->chunk.size();
+    counts[kCountChunk] = (int32_t)pl->chunk_items.size();
     counts[kCountCombine] = (int32_t)pl->combine.size();
   }
   const int k = f->next;
@@ -1164,6 +1242,7 @@ rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
   if (pl) {
     section(f->o_dec, pl->decode.data(), pl->decode.size() * sizeof(WorkItem));
     section(f->o_chunk, pl->chunk.data(), pl->chunk.size() * sizeof(ChunkTile));
+    section(f->o_items, pl->chunk_items.data(), pl->chunk_items.size() * sizeof(ChunkItem));
     section(f->o_comb, pl->combine.data(), pl->combine.size() * sizeof(CombineRow));
   }
   if (e == cudaSuccess) e = cudaEventRecord(f->ev[k], st);

@@ -60,6 +60,21 @@ struct ChunkTile {
 };
 static_assert(sizeof(ChunkTile) == 48, "ChunkTile is 12 int32");
 
+// Work of one tensor-core CTA step: one or two query tiles that read the same
+// K/V tiles - the same rows for two query heads of one KV group, or two
+// consecutive 128-row tiles of one chunk for one head (groups of one) - over
+// the keys [key_begin, key_end) (the union of the two tiles' key ranges; each
+// tile stops at its own key_end).  tile[1] < 0: one query tile.
+struct ChunkItem {
+  int32_t tile[2];    // indices into the pass's chunk tiles
+  int32_t head[2];    // query head of each tile
+  int32_t kv_head;
+  int32_t key_begin;
+  int32_t key_end;
+  int32_t pad;
+};
+static_assert(sizeof(ChunkItem) == 32, "ChunkItem is 8 int32");
+
 // Device view of a pass (pointers into its uploaded metadata buffer).
 struct DevPass {
   int32_t* status;                 // device status words (rbkv_status code, wait site, ...)
@@ -67,20 +82,23 @@ struct DevPass {
   const int32_t* block_ids;        // all block tables
   const WorkItem* decode_items;    // fast decode path
   const WorkItem* generic_items;   // CUDA-core path
-  const ChunkTile* chunk_tiles;    // tensor-core prompt path
+  const ChunkTile* chunk_tiles;    // tensor-core prompt path: query tiles
+  const ChunkItem* chunk_items;    // ... and the work items over them
   const CombineRow* combine_rows;
   int32_t num_tokens;
   int32_t n_decode;
   int32_t n_generic;
-  int32_t n_chunk;
+  int32_t n_chunk;                 // chunk work items (ChunkItem)
   int32_t n_combine;
   int32_t n_parts;
   int32_t num_blocks;
   int32_t decode_grid;             // CTAs of the persistent decode launch
   int32_t decode_packed;           // 1: some decode units pack several prompt rows
+  int32_t chunk_single;            // 1: chunk items hold one query tile each (the
+                                   // one-tile kernel runs them); 0: pairs
   // A frame (rbkv_frame_*): the launches are sized by the frame's capacities
   // (the counts above), and the loaded pass's own counts are read from this
-  // device array {num_tokens, n_decode, n_generic, n_chunk, n_combine}.
+  // device array {num_tokens, n_decode, n_generic, n_chunk (items), n_combine}.
   // Null for a plain pass.
   const int32_t* counts;
 };
@@ -160,6 +178,12 @@ cudaError_t launch_chunk_fast(const DevPass& dp, const ShapeInfo& s, const void*
                               const void* k_cache, const void* v_cache, void* o,
                               float* part_o, float* part_lse, cudaStream_t st,
                               bool overlap_previous, bool wait_first);
+// The one-tile prompt-chunk kernel (rbkv_chunk_single.cu), for items of one
+// query tile each; launch_chunk_fast runs it when dp.chunk_single is set.
+cudaError_t launch_chunk_single(const DevPass& dp, const ShapeInfo& s, const void* q,
+                                const void* k_cache, const void* v_cache, void* o,
+                                float* part_o, float* part_lse, cudaStream_t st,
+                                bool overlap_previous, bool wait_first);
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
 // One CTA waiting `limit` cycles on a barrier nothing completes; reports the
