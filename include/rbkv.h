@@ -124,6 +124,7 @@ typedef struct {
   int32_t fast_chunk;         /* 1 if the tcgen05 chunk kernel is used */
   int32_t chunk_items;        /* tensor-core work items: one or two query tiles
                                  sharing the K/V tiles they read */
+  int32_t chunk_single;       /* 1 if every work item holds one query tile */
 } rbkv_plan_info;
 
 /* Library ABI version (RBKV_ABI_VERSION). */
@@ -217,6 +218,21 @@ rbkv_status rbkv_pass_get_meta(const rbkv_pass* p, rbkv_pass_meta* view);
  * be called before the pass's first device call.  Results do not depend on it
  * beyond floating-point rounding. */
 rbkv_status rbkv_pass_set_split_keys(rbkv_pass* p, int32_t keys_per_split);
+
+/* How prompt-chunk tiles are grouped into tensor-core work items. */
+typedef enum {
+  RBKV_CHUNK_ITEMS_AUTO = 0,   /* pairs when there are at least as many as SMs, else one
+                                  tile per item */
+  RBKV_CHUNK_ITEMS_PAIRS = 1,  /* two tiles that read the same K/V tiles per item (two
+                                  query heads of a KV group, or two consecutive row tiles
+                                  when the group has one head) */
+  RBKV_CHUNK_ITEMS_SINGLE = 2  /* one tile and query head per item */
+} rbkv_chunk_items;
+
+/* Override how the pass's prompt-chunk tiles are grouped into work items
+ * (rbkv_chunk_items); must be called before the pass's first device call.
+ * Results do not depend on it beyond floating-point rounding. */
+rbkv_status rbkv_pass_set_chunk_items(rbkv_pass* p, int32_t mode);
 
 /* Plan summary; makes the plan for the current device if not made yet. */
 rbkv_status rbkv_pass_get_plan(rbkv_pass* p, rbkv_plan_info* info);
@@ -347,7 +363,14 @@ typedef struct rbkv_frame rbkv_frame;
  *   max_parts         max_decode_items + max_tokens x num_heads_kv x
  *                     max(1, SMs / num_heads_q)
  *   packed_units      0 (passes whose short prompt chunks run as packed decode
- *                     units are refused with RBKV_ERR_UNSUPPORTED) */
+ *                     units are refused with RBKV_ERR_UNSUPPORTED)
+ *   chunk_items       RBKV_CHUNK_ITEMS_AUTO: pairs when a pass of max_tokens
+ *                     prompt rows would give at least as many pairs of tiles
+ *                     as SMs, else one tile per item.  Every pass loaded into
+ *                     the frame is planned with the frame's grouping (a pass
+ *                     already planned with another is refused with
+ *                     RBKV_ERR_UNSUPPORTED) and the frame's launches run the
+ *                     kernel for that grouping. */
 typedef struct {
   int32_t max_tokens;       /* rows of Q/K/V/O the frame's launches address */
   int32_t max_seqs;
@@ -359,6 +382,7 @@ typedef struct {
   int32_t packed_units;     /* 1: passes may hold short prompt chunks packed into decode
                                units (the decode variant with per-row limits runs for
                                every pass); 0: such passes are refused */
+  int32_t chunk_items;      /* rbkv_chunk_items grouping of every pass's chunk tiles */
 } rbkv_frame_caps;
 
 /* Create a frame on the current device for passes of `cfg` (device memory for

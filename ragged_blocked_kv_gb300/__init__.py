@@ -61,13 +61,13 @@ class _PlanInfo(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_sms", "decode_rows", "decode_items", "max_splits", "split_keys", "partials",
         "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk",
-        "chunk_items")]
+        "chunk_items", "chunk_single")]
 
 
 class _FrameCaps(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "max_tokens", "max_seqs", "max_blocks", "max_decode_items", "max_chunk_tiles",
-        "max_combine_rows", "max_parts", "packed_units")]
+        "max_combine_rows", "max_parts", "packed_units", "chunk_items")]
 
 
 # Every symbol include/rbkv.h declares, with (restype, argtypes).
@@ -90,6 +90,7 @@ SIGNATURES = {
     "rbkv_composer_free_blocks": (C.c_int32, [_P]),
     "rbkv_pass_get_meta": (C.c_int, [_P, C.POINTER(_PassMeta)]),
     "rbkv_pass_set_split_keys": (C.c_int, [_P, C.c_int32]),
+    "rbkv_pass_set_chunk_items": (C.c_int, [_P, C.c_int32]),
     "rbkv_pass_get_plan": (C.c_int, [_P, C.POINTER(_PlanInfo)]),
     "rbkv_pass_plan_for_sms": (C.c_int, [_P, C.c_int32, C.POINTER(_PlanInfo)]),
     "rbkv_pass_destroy": (None, [_P]),
@@ -223,6 +224,11 @@ class Pass:
 
     def set_split_keys(self, keys: int) -> None:
         _check(lib().rbkv_pass_set_split_keys(self._h, int(keys)))
+
+    def set_chunk_items(self, mode: str) -> None:
+        """Group prompt-chunk tiles as "auto", "pairs" or "single" work items."""
+        m = {"auto": 0, "pairs": 1, "single": 2}[mode]
+        _check(lib().rbkv_pass_set_chunk_items(self._h, m))
 
     def plan(self) -> dict:
         info = _PlanInfo()
@@ -407,7 +413,11 @@ class Frame:
     stream.  Q/K/V/O buffers have ``max_tokens`` rows; rows past the loaded
     pass's tokens are ignored."""
 
+    CHUNK_ITEMS = {"auto": 0, "pairs": 1, "single": 2}
+
     def __init__(self, config: Config, max_tokens: int, **caps):
+        if isinstance(caps.get("chunk_items"), str):
+            caps["chunk_items"] = self.CHUNK_ITEMS[caps["chunk_items"]]
         want = _FrameCaps(max_tokens=int(max_tokens), **{k: int(v) for k, v in caps.items()})
         got = _FrameCaps()
         h = _P()
@@ -417,6 +427,8 @@ class Frame:
         self.config = config
         self.caps = {n: getattr(got, n) for n, _ in _FrameCaps._fields_}
         self.max_tokens = self.caps["max_tokens"]
+        # the grouping of chunk tiles every pass loaded here is planned with
+        self.chunk_items = {1: "pairs", 2: "single"}[self.caps["chunk_items"]]
 
     def workspace_bytes(self) -> int:
         return int(lib().rbkv_frame_workspace_bytes(self._h))

@@ -196,6 +196,7 @@ struct rbkv_pass {
   std::vector<int64_t> seq_ids;
   std::vector<int32_t> q_start{0}, n_new, seen, ctx, block_start{0}, block_ids, slot;
   int32_t split_keys = 0;
+  int32_t chunk_items = RBKV_CHUNK_ITEMS_AUTO;
   // plan, made once for the device of the first device call
   bool planned = false;
   int device = -1;
@@ -301,7 +302,8 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
       singles += tiles * s.H_q;
       max_keys = std::max(max_keys, p.ctx[i]);
     }
-    chunk_single = pairs < num_sms;
+    chunk_single = p.chunk_items == RBKV_CHUNK_ITEMS_AUTO ? pairs < num_sms
+                                                          : p.chunk_items == RBKV_CHUNK_ITEMS_SINGLE;
     if (p.split_keys > 0) {
       chunk_split = round_up(p.split_keys, kChunkTileKeys);
     } else if (singles > 0 && singles < num_sms) {
@@ -486,6 +488,7 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   in.chunk_rows = chunk_rows;
   in.chunk_tiles = (int32_t)pl.chunk.size();
   in.chunk_items = (int32_t)pl.chunk_items.size();
+  in.chunk_single = pl.chunk_single;
   in.generic_items = (int32_t)pl.generic.size();
   in.fast_decode = fast_decode ? 1 : 0;
   in.fast_chunk = fast_chunk ? 1 : 0;
@@ -887,6 +890,15 @@ rbkv_status rbkv_pass_set_split_keys(rbkv_pass* p, int32_t keys) {
   return RBKV_OK;
 }
 
+rbkv_status rbkv_pass_set_chunk_items(rbkv_pass* p, int32_t mode) {
+  if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
+  if (mode < RBKV_CHUNK_ITEMS_AUTO || mode > RBKV_CHUNK_ITEMS_SINGLE)
+    return fail(RBKV_ERR_INVALID, "unknown chunk item mode");
+  if (p->planned) return fail(RBKV_ERR_INVALID, "the pass was already planned by a device call");
+  p->chunk_items = mode;
+  return RBKV_OK;
+}
+
 rbkv_status rbkv_pass_get_plan(rbkv_pass* p, rbkv_plan_info* info) {
   if (!p || !info) return fail(RBKV_ERR_INVALID, "pass or info is NULL");
   rbkv_status st = ensure_plan(p);
@@ -1106,7 +1118,8 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   rbkv_frame_caps c = *caps;
   if (c.max_tokens < 1) return fail(RBKV_ERR_INVALID, "max_tokens must be >= 1");
   if (c.max_seqs < 0 || c.max_blocks < 0 || c.max_decode_items < 0 || c.max_chunk_tiles < 0 ||
-      c.max_combine_rows < 0 || c.max_parts < 0 || c.packed_units < 0 || c.packed_units > 1)
+      c.max_combine_rows < 0 || c.max_parts < 0 || c.packed_units < 0 || c.packed_units > 1 ||
+      c.chunk_items < RBKV_CHUNK_ITEMS_AUTO || c.chunk_items > RBKV_CHUNK_ITEMS_SINGLE)
     return fail(RBKV_ERR_INVALID, "capacities must be >= 0");
   int dev = -1, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1123,6 +1136,13 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
                                                     c.max_seqs,
                                                 ceil_div(sms, s.H_q)));
   if (!c.max_combine_rows) c.max_combine_rows = clamp((int64_t)c.max_tokens * s.H_kv);
+  if (c.chunk_items == RBKV_CHUNK_ITEMS_AUTO) {
+    // the grouping the planner would take for a pass of max_tokens prompt rows
+    const int64_t tiles = ceil_div(c.max_tokens, kChunkTileRows);
+    const int64_t pairs =
+        s.g >= 2 ? tiles * s.H_kv * ceil_div(s.g, 2) : ceil_div(tiles, 2) * s.H_q;
+    c.chunk_items = pairs >= sms ? RBKV_CHUNK_ITEMS_PAIRS : RBKV_CHUNK_ITEMS_SINGLE;
+  }
   if (!c.max_parts)
     c.max_parts = clamp((int64_t)c.max_decode_items +
                         (int64_t)c.max_tokens * s.H_kv * std::max(1, sms / s.H_q));
@@ -1169,6 +1189,7 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
   dp.num_blocks = cfg->num_blocks;
   dp.decode_grid = (int32_t)std::min<int64_t>(slots, c.max_decode_items);
   dp.decode_packed = c.packed_units ? 1 : 0;
+  dp.chunk_single = c.chunk_items == RBKV_CHUNK_ITEMS_SINGLE ? 1 : 0;
   if (caps_out) *caps_out = c;
   *out = f.release();
   return RBKV_OK;
@@ -1187,9 +1208,14 @@ rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
   int32_t counts[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const Plan* pl = nullptr;
   if (!p->slot.empty()) {
+    if (!p->planned) p->chunk_items = c.chunk_items;   // the frame's grouping
     rbkv_status rs = ensure_plan(p);
     if (rs != RBKV_OK) return rs;
     pl = &p->plan;
+    if (pl->chunk_single != f->dp.chunk_single)
+      return fail(RBKV_ERR_UNSUPPORTED,
+                  "the pass was planned with another grouping of its chunk tiles than the "
+                  "frame's");
     auto over = [](const char* what, size_t n, int32_t cap) {
       return fail(RBKV_ERR_WORKSPACE, std::string("pass exceeds the frame's ") + what + " (" +
                                           std::to_string(n) + " > " + std::to_string(cap) + ")");

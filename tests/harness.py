@@ -72,7 +72,7 @@ class Pair:
 
     def step(self, budget: int, max_chunk: int, states: Sequence[Tuple[int, int, int]],
              attend: bool = True, split_keys: Optional[int] = None,
-             tokens: Optional[Iterable[int]] = None) -> dict:
+             tokens: Optional[Iterable[int]] = None, chunk_items: Optional[str] = None) -> dict:
         """Compose, append and (optionally) attend one pass on both sides."""
         res: dict = {}
         p = self.lib.compose(budget, max_chunk, states, policy=self.policy)
@@ -90,6 +90,8 @@ class Pair:
             return res
         if split_keys is not None:
             p.set_split_keys(split_keys)
+        if chunk_items is not None:
+            p.set_chunk_items(chunk_items)
         which = "qkv" if attend else "kv"
         ten = workloads.make_qkv(self.shape, T, self.seed, idx, device=self.input_device, which=which)
         if attend:
@@ -169,7 +171,7 @@ class Pair:
 def run_scenario(rbkv, scn: workloads.Scenario, seed: int = 0, split_keys: Optional[int] = None,
                  passes: int = 1, only_seqs: Optional[Set[int]] = None,
                  input_device: str = "cpu", cache_fill: Optional[float] = None,
-                 policy: str = "greedy") -> List[dict]:
+                 policy: str = "greedy", chunk_items: Optional[str] = None) -> List[dict]:
     """Registration pass, then ``passes`` measured passes with states advanced
     between them.  Returns the measured passes' results."""
     pair = Pair(rbkv, scn.shape, scn.num_blocks, seed, only_seqs, input_device, cache_fill,
@@ -181,7 +183,8 @@ def run_scenario(rbkv, scn: workloads.Scenario, seed: int = 0, split_keys: Optio
     states = list(scn.requests)
     out = []
     for _ in range(passes):
-        r = pair.step(scn.budget, scn.max_chunk, states, split_keys=split_keys)
+        r = pair.step(scn.budget, scn.max_chunk, states, split_keys=split_keys,
+                      chunk_items=chunk_items)
         r["pair"] = pair
         out.append(r)
         n = dict(zip(r["meta"].seq_ids, r["meta"].n_new))

@@ -47,6 +47,7 @@ def _drive(rbkv, scn, passes, use_graph, split_keys=None, caps=None, seed=0):
         p = comp.compose(scn.budget, scn.max_chunk, states)
         if split_keys:
             p.set_split_keys(split_keys)
+        p.set_chunk_items(frame.chunk_items)   # the plain path plans the pass first
         T = p.num_tokens
         q, k, v = workloads.make_qkv(sh, T, seed, i, device="cuda")
         rbkv.kv_append(p, k, v, kc_a, vc_a)

@@ -47,6 +47,26 @@ def test_scaled_scenarios_all_outputs(rbkv, name, factor, split):
         assert plan["chunk_rows"] > 0 and plan["chunk_tiles"] > 0, plan
 
 
+@pytest.mark.parametrize("mode", ["pairs", "single"])
+@pytest.mark.parametrize("name,factor", [("mistral_7b", 8), ("llama2_7b", 2), ("llama2_7b", 4)])
+@pytest.mark.parametrize("split", [None, 128])
+def test_chunk_work_item_modes(rbkv, mode, name, factor, split):
+    """Both tensor-core chunk kernels on the same passes: items that pair two
+    query tiles reading the same K/V tiles (two heads of a KV group for
+    Mistral-7B's groups of four; two consecutive row tiles for Llama-2-7B's
+    groups of one, 248- and 124-row chunks: a pair and a lone tile) and items
+    of one tile; with a forced split every tile's keys come in 128-key pieces
+    merged by the combine.  Every output against the oracle."""
+    scn = workloads.scaled(workloads.SCENARIOS[name](0), factor)
+    (r,) = run_scenario(rbkv, scn, split_keys=split, chunk_items=mode)
+    plan = r["plan"]
+    assert plan["chunk_tiles"] > 0 and plan["chunk_single"] == (mode == "single"), plan
+    if mode == "pairs" and (name == "mistral_7b" or factor == 2):
+        assert plan["chunk_items"] < plan["chunk_tiles"] * scn.shape.num_heads_q, plan
+    _ok(r)
+    assert r["pair"].cache_equal()
+
+
 @pytest.mark.parametrize("split", [None, 64, 192])
 def test_chunked_prompt_over_passes(rbkv, split):
     """Every pass of a prompt chunked over several passes, with decodes; with a
@@ -109,13 +129,15 @@ def test_short_prompts_packed_decode_units(rbkv, hq, hkv):
 
 
 @pytest.mark.parametrize("split", [None, 64])
-def test_garbage_in_unwritten_slots_does_not_leak(rbkv, split):
+@pytest.mark.parametrize("mode", ["pairs", "single"])
+def test_garbage_in_unwritten_slots_does_not_leak(rbkv, split, mode):
     """Slots past a sequence's context hold whatever the caller left there
     (here NaN); outputs must not see them.  The pass has decode units and
     tensor-core chunk tiles whose key ranges end inside a 128-key tile (96 and
-    288 keys), so both kernels meet NaN rows in their last K/V tile."""
+    288 keys), so the decode kernel and both chunk kernels meet NaN rows in
+    their last K/V tile."""
     scn = workloads.scaled(workloads.mistral_7b(0), 8)
-    (r,) = run_scenario(rbkv, scn, cache_fill=float("nan"), split_keys=split)
+    (r,) = run_scenario(rbkv, scn, cache_fill=float("nan"), split_keys=split, chunk_items=mode)
     _ok(r)
     plan = r["plan"]
     assert plan["chunk_tiles"] > 0 and plan["decode_items"] > 0, plan
