@@ -330,6 +330,43 @@ rbkv_status rbkv_debug_corrupt_pass(rbkv_pass* p, int32_t which, int32_t index, 
  * Read the result with rbkv_pass_device_status. */
 rbkv_status rbkv_debug_wait_timeout(rbkv_pass* p, int64_t limit_cycles, rbkv_stream stream);
 
+/* ---- routing over replicas (host only) ------------------------------------
+ *
+ * InfoQ release note on DeepSpeed-FastGen: throughput scales with the number
+ * of replicas behind a load balancer (16 replicas, 23.7 queries/s).  Every
+ * replica (one GPU, one composer, one cache) serves its requests on its own;
+ * a router only decides which replica takes a request, so there is no
+ * exchange between replicas on the data path.  Policy: the replica with the
+ * fewest outstanding tokens (prompt tokens not yet prefilled plus output
+ * tokens not yet generated, over the requests it holds) takes the next
+ * request; ties go to the replica holding fewer requests, then to the lowest
+ * index.  Replicas report the tokens each request consumed after every pass
+ * (rbkv_router_progress) and its end (rbkv_router_finish).  A router is not
+ * thread-safe. */
+
+typedef struct rbkv_router rbkv_router;
+
+/* Errors: RBKV_ERR_INVALID for num_replicas < 1. */
+rbkv_status rbkv_router_create(int32_t num_replicas, rbkv_router** out);
+void rbkv_router_destroy(rbkv_router* r);
+
+/* Route a new request; *replica receives the replica that takes it.
+ * Errors: RBKV_ERR_INVALID (lengths < 1, an id already routed). */
+rbkv_status rbkv_router_assign(rbkv_router* r, int64_t request_id, int32_t prompt_len,
+                               int32_t output_len, int32_t* replica);
+
+/* `tokens` more of the request's prompt or output were served (at most its
+ * outstanding tokens).  Errors: RBKV_ERR_INVALID (unknown id, bad count). */
+rbkv_status rbkv_router_progress(rbkv_router* r, int64_t request_id, int32_t tokens);
+
+/* The request ended; its replica's load drops by what it still had
+ * outstanding.  Errors: RBKV_ERR_INVALID (unknown id). */
+rbkv_status rbkv_router_finish(rbkv_router* r, int64_t request_id);
+
+/* Outstanding tokens / requests held by a replica (-1 for a bad index). */
+int64_t rbkv_router_load(const rbkv_router* r, int32_t replica);
+int32_t rbkv_router_active(const rbkv_router* r, int32_t replica);
+
 /* ---- frames: one fixed launch sequence for every pass (CUDA graphs) ---------
  *
  * Under Dynamic SplitFuse the passes all have roughly one size (paper

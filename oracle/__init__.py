@@ -23,6 +23,11 @@ What it computes, plainly and slowly:
   (``split_attention`` / ``lse_combine``) so that its equivalence can be
   checked; the oracle's own outputs never go through it.
 
+* ``router``     - routing requests over independent replicas: the replica
+  with the fewest outstanding tokens takes the next request (InfoQ release
+  note: replicas behind a load balancer; the policy is this repository's
+  reading), loads recomputed from the held requests at every decision.
+
 Pins (tests marked ``not gpu``): the tiny configuration's worked pass, budget
 and conservation invariants, brute force on tiny inputs, closed forms,
 PyTorch's scaled-dot-product attention as an independent library special case,
@@ -32,6 +37,7 @@ block ids, parity unpinned (only that rule and the pool invariants - distinct
 ids, ceil(ctx / B) held per sequence, all-or-nothing - hold them).
 """
 from .composer import Composer, PassMeta, InvalidRequest, NoBlocks, budget_for_latency, latency_at  # noqa: F401
+from . import router  # noqa: F401
 from .cache import BlockedCache, kv_append  # noqa: F401
 from .attention import (  # noqa: F401
     widen,

@@ -113,6 +113,14 @@ SIGNATURES = {
     "rbkv_profile_enable": (None, [C.c_int32]),
     "rbkv_profile_read": (C.c_int, [C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
     "rbkv_profile_reset": (None, []),
+    "rbkv_router_create": (C.c_int, [C.c_int32, C.POINTER(_P)]),
+    "rbkv_router_destroy": (None, [_P]),
+    "rbkv_router_assign": (C.c_int, [_P, C.c_int64, C.c_int32, C.c_int32,
+                                     C.POINTER(C.c_int32)]),
+    "rbkv_router_progress": (C.c_int, [_P, C.c_int64, C.c_int32]),
+    "rbkv_router_finish": (C.c_int, [_P, C.c_int64]),
+    "rbkv_router_load": (C.c_int64, [_P, C.c_int32]),
+    "rbkv_router_active": (C.c_int32, [_P, C.c_int32]),
 }
 
 KERNEL_KINDS = {"kv_append": 0, "chunk": 1, "decode": 2, "generic": 3, "combine": 4,
@@ -507,5 +515,46 @@ def profile_read() -> dict:
     return out
 
 
-__all__ = ["Frame", "budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+class Router:
+    """Routing of requests over independent replicas (host only): the replica
+    with the fewest outstanding tokens takes the next request (ties: fewer
+    requests held, then the lower index)."""
+
+    def __init__(self, num_replicas: int):
+        h = _P()
+        _check(lib().rbkv_router_create(int(num_replicas), C.byref(h)))
+        self._h = h
+        self.num_replicas = int(num_replicas)
+
+    def assign(self, request_id: int, prompt_len: int, output_len: int) -> int:
+        out = C.c_int32()
+        _check(lib().rbkv_router_assign(self._h, int(request_id), int(prompt_len),
+                                        int(output_len), C.byref(out)))
+        return int(out.value)
+
+    def progress(self, request_id: int, tokens: int) -> None:
+        _check(lib().rbkv_router_progress(self._h, int(request_id), int(tokens)))
+
+    def finish(self, request_id: int) -> None:
+        _check(lib().rbkv_router_finish(self._h, int(request_id)))
+
+    def load(self, replica: int) -> int:
+        return int(lib().rbkv_router_load(self._h, int(replica)))
+
+    def active(self, replica: int) -> int:
+        return int(lib().rbkv_router_active(self._h, int(replica)))
+
+    def close(self) -> None:
+        if self._h:
+            lib().rbkv_router_destroy(self._h)
+            self._h = _P(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+__all__ = ["Router", "Frame", "budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
            "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

@@ -24,7 +24,7 @@ LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "librbkv.so"
 
 SOURCES = ["rbkv_host.cpp", "rbkv_kernels.cu", "rbkv_decode.cu", "rbkv_chunk.cu",
-           "rbkv_chunk_single.cu", "rbkv_noalloc.cu"]
+           "rbkv_chunk_single.cu", "rbkv_noalloc.cu", "rbkv_router.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
