@@ -670,53 +670,42 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 class DenseStack:
     """Random-weight Llama-2-7B-shaped decoder layers around the library's
-    attention: RMSNorm, a fused Q/K/V projection, the KV append and ragged
-    attention, the output projection, RMSNorm and a SwiGLU MLP (hidden 4096,
-    intermediate 11008), with residual adds.  The projections are plain cuBLAS
-    GEMMs (torch.matmul); rotary embeddings are left out (elementwise work that
-    does not change the shape of the pass).  It exists to measure pass latency
-    against token count (paper summary page, ideas I1/I2)."""
+    attention, every step a library kernel (ragged_blocked_kv_gb300.layer):
+    RMSNorm, the QKV projection as one tensor-core GEMM writing Q, K and V,
+    the KV append and ragged attention, the output projection with a fused
+    residual, RMSNorm, the gate/up GEMM with a fused SwiGLU, the down
+    projection with a fused residual (hidden 4096, intermediate 11008).
+    Rotary embeddings are left out (elementwise work that does not change the
+    shape of the pass).  It exists to measure pass latency against token
+    count (paper summary page, ideas I1/I2)."""
 
     HIDDEN, INTER = 4096, 11008
 
     def __init__(self, torch, rbkv, cfg, layers, max_tokens, device, seed):
-        H, I = self.HIDDEN, self.INTER
+        from ragged_blocked_kv_gb300.layer import DecoderLayer, random_weights
+        hq, hkv, d = cfg.num_heads_q, cfg.num_heads_kv, cfg.head_dim
+        self.layers = []
+        for l in range(layers):
+            w = random_weights(self.HIDDEN, hq, hkv, d, self.INTER, seed * 1000 + l, device)
+            del w["w_gate"], w["w_up"]          # the interleaved w_gu is what runs
+            self.layers.append(DecoderLayer(rbkv, w, hq, hkv, d))
         g = torch.Generator(device=device)
         g.manual_seed(seed)
-
-        def w(*shape, fan_in):
-            return (torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
-                    * fan_in ** -0.5).to(torch.bfloat16)
-        self.layers = []
-        for _ in range(layers):
-            self.layers.append({"qkv": w(3, H, H, fan_in=H), "o": w(H, H, fan_in=H),
-                                "gu": w(2, H, I, fan_in=H), "down": w(I, H, fan_in=I),
-                                "n1": torch.ones(H, device=device, dtype=torch.bfloat16),
-                                "n2": torch.ones(H, device=device, dtype=torch.bfloat16)})
-        self.x0 = torch.randn(max_tokens, H, generator=g, device=device,
+        self.x0 = torch.randn(max_tokens, self.HIDDEN, generator=g, device=device,
                               dtype=torch.float32).to(torch.bfloat16)
-        self.o = torch.empty(max_tokens, cfg.num_heads_q, cfg.head_dim, device=device,
-                             dtype=torch.bfloat16)
+        self.xs = [torch.empty_like(self.x0), torch.empty_like(self.x0)]
+        self.buf = self.layers[0].buffers(max_tokens, device)
         self.torch, self.rbkv, self.cfg = torch, rbkv, cfg
 
     def weight_bytes(self):
-        return sum(t.numel() * t.element_size() for l in self.layers for t in l.values())
+        return sum(t.numel() * t.element_size() for l in self.layers for t in l.w.values())
 
-    def _layers(self, T, caches, attend):
-        torch = self.torch
-        F = torch.nn.functional
-        hq, d = self.cfg.num_heads_q, self.cfg.head_dim
+    def _layers(self, T, attend):
         x = self.x0[:T]
-        o = self.o[:T]
-        for l, W in enumerate(self.layers):
-            h = F.rms_norm(x, (self.HIDDEN,), W["n1"], 1e-5)
-            qkv = torch.matmul(h, W["qkv"])                 # [3][T][hidden], each contiguous
-            q, k, v = (qkv[i].view(T, hq, d) for i in range(3))
-            attend(l, q, k, v, o)
-            x = x + torch.matmul(o.view(T, self.HIDDEN), W["o"])
-            h = F.rms_norm(x, (self.HIDDEN,), W["n2"], 1e-5)
-            gu = torch.matmul(h, W["gu"])
-            x = x + torch.matmul(F.silu(gu[0]) * gu[1], W["down"])
+        for l, layer in enumerate(self.layers):
+            out = self.xs[l & 1][:T]
+            layer.forward_into(x, out, self.buf, lambda q, k, v, o, l=l: attend(l, q, k, v, o), T)
+            x = out
         return x
 
     def forward(self, p, caches, ws, hs):
@@ -726,7 +715,7 @@ class DenseStack:
             kc, vc = caches[l]
             rbkv.kv_append(p, k, v, kc, vc, stream=hs)
             rbkv.ragged_attention(p, q, kc, vc, o=o, workspace=ws, stream=hs)
-        return self._layers(p.num_tokens, caches, attend)
+        return self._layers(p.num_tokens, attend)
 
     def forward_frame(self, frame, caches, ws):
         """The pass loaded in ``frame``, on frame-sized buffers and the current
@@ -735,7 +724,7 @@ class DenseStack:
             kc, vc = caches[l]
             frame.kv_append(k, v, kc, vc)
             frame.attention(q, kc, vc, o, ws)
-        return self._layers(frame.max_tokens, caches, attend)
+        return self._layers(frame.max_tokens, attend)
 
 
 def _trace_setup(args, rank, world, local_rank, max_tokens):
@@ -802,7 +791,7 @@ class AttentionStack:
 
 class GraphRunner:
     """Runs passes of a stack through a frame and one CUDA graph: the first
-    pass runs eagerly (warming cuBLAS and the library), then the stack's
+    pass runs eagerly (warming the library's kernels), then the stack's
     launches are captured once; every later pass is a metadata load plus a
     replay.  A pass the frame cannot hold runs eagerly through the plain entry
     points."""

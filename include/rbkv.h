@@ -458,6 +458,62 @@ rbkv_status rbkv_frame_attention(rbkv_frame* f, const void* q, const void* k_cac
  * passes loaded since it was last read). */
 rbkv_status rbkv_frame_device_status(rbkv_frame* f, rbkv_stream stream);
 
+/* ---- the rest of a decoder layer: tensor-core GEMM and RMSNorm --------------
+ *
+ * DeepSpeed-FastGen paper summary page, idea I1: a forward pass's latency
+ * follows its token count; the token-proportional work of a layer besides
+ * attention is its projections (QKV, output, the two MLP products) and the
+ * normalisations around them.  These calls run those steps on the device, so
+ * that a whole decoder layer can be put around the attention pass. */
+
+typedef enum {
+  RBKV_GEMM_PLAIN = 0,     /* C[m][n] = A B^T */
+  RBKV_GEMM_RESIDUAL = 1,  /* C[m][n] = A B^T + R[m][n] */
+  RBKV_GEMM_SWIGLU = 2     /* B's rows in blocks of 256: 128 gate rows, then the 128 up
+                              rows of the same outputs; C[m][n/2] = silu(gate) * up with
+                              output j of block b at column 128 b + j */
+} rbkv_gemm_epilogue;
+
+/* Device workspace that rbkv_gemm_bf16 / rbkv_gemm_bf16_qkv can use for a
+ * product of this size: when its 128 x 256 output tiles are fewer than the
+ * SMs (few rows: a weight-streaming product), K is split into pieces run by
+ * different SMs, their fp32 partial sums kept here and added by a second
+ * kernel that applies the epilogue.  0 when the product does not split. */
+size_t rbkv_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
+
+/* C = A . B^T in bf16 with fp32 accumulation on the tensor cores (tcgen05),
+ * with a fused epilogue (rbkv_gemm_epilogue).  a: [m][k] row-major (the
+ * activations); b: [n][k] row-major (a weight stored [out][in]); c: [m][n]
+ * ([m][n/2] for RBKV_GEMM_SWIGLU); residual: [m][n] or NULL.  Device
+ * pointers, 16-byte aligned; k a multiple of 8; n a multiple of 32 (256 for
+ * SwiGLU); c must not overlap a or b (it may be the residual itself).
+ * workspace: NULL, or device memory of workspace_bytes (256-byte aligned,
+ * owned by the caller, not used by other work until this call's kernels end):
+ * with at least rbkv_gemm_workspace_bytes(m, n, k) bytes the product may
+ * split K (results then differ only by fp32 rounding order).
+ * status: NULL or a device array of 4 int32 (code, wait site, index, block)
+ * that a bounded wait that gives up writes, as a pass's status words.
+ * Launches on `stream`.  Errors: RBKV_ERR_INVALID, RBKV_ERR_CUDA. */
+rbkv_status rbkv_gemm_bf16(const void* a, const void* b, void* c, int64_t m, int64_t n, int64_t k,
+                           const void* residual, int32_t epilogue, void* workspace,
+                           size_t workspace_bytes, int32_t* status, rbkv_stream stream);
+
+/* The QKV projection as one GEMM whose outputs are the attention pass's
+ * inputs: w_qkv is [n_q + 2 n_kv][k] (the Q rows, then K, then V); q receives
+ * [m][n_q], k_out and v_out [m][n_kv] (Q [T][H_q][D] and K_new, V_new
+ * [T][H_kv][D] for n_q = H_q D, n_kv = H_kv D).  n_q and n_kv multiples of
+ * 32; otherwise as rbkv_gemm_bf16. */
+rbkv_status rbkv_gemm_bf16_qkv(const void* a, const void* w_qkv, void* q, void* k_out,
+                               void* v_out, int64_t m, int64_t n_q, int64_t n_kv, int64_t k,
+                               void* workspace, size_t workspace_bytes, int32_t* status,
+                               rbkv_stream stream);
+
+/* y[i][:] = x[i][:] / sqrt(mean_j x[i][j]^2 + eps) * weight[:] for m rows of
+ * `hidden` bf16 values (fp32 arithmetic, bf16 out); hidden a multiple of 8,
+ * 16-byte aligned device pointers.  Errors: RBKV_ERR_INVALID, RBKV_ERR_CUDA. */
+rbkv_status rbkv_rmsnorm_bf16(const void* x, const void* weight, void* y, int64_t m,
+                              int64_t hidden, float eps, rbkv_stream stream);
+
 /* ---- measurement ----------------------------------------------------------- */
 
 /* Kernel kinds for rbkv_profile_read. */

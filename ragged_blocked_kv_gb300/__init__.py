@@ -113,6 +113,12 @@ SIGNATURES = {
     "rbkv_profile_enable": (None, [C.c_int32]),
     "rbkv_profile_read": (C.c_int, [C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
     "rbkv_profile_reset": (None, []),
+    "rbkv_gemm_bf16": (C.c_int, [_P, _P, _P, C.c_int64, C.c_int64, C.c_int64, _P, C.c_int32,
+                                 _P, C.c_size_t, _P, _P]),
+    "rbkv_gemm_workspace_bytes": (C.c_size_t, [C.c_int64, C.c_int64, C.c_int64]),
+    "rbkv_rmsnorm_bf16": (C.c_int, [_P, _P, _P, C.c_int64, C.c_int64, C.c_float, _P]),
+    "rbkv_gemm_bf16_qkv": (C.c_int, [_P, _P, _P, _P, _P, C.c_int64, C.c_int64, C.c_int64,
+                                     C.c_int64, _P, C.c_size_t, _P, _P]),
     "rbkv_router_create": (C.c_int, [C.c_int32, C.POINTER(_P)]),
     "rbkv_router_destroy": (None, [_P]),
     "rbkv_router_assign": (C.c_int, [_P, C.c_int64, C.c_int32, C.c_int32,
@@ -515,6 +521,84 @@ def profile_read() -> dict:
     return out
 
 
+GEMM_EPILOGUES = {"plain": 0, "residual": 1, "swiglu": 2}
+
+
+def gemm_workspace_bytes(m: int, n: int, k: int) -> int:
+    """Workspace a GEMM of this size can use to split K (0: it does not)."""
+    return int(lib().rbkv_gemm_workspace_bytes(int(m), int(n), int(k)))
+
+
+def _ws(workspace):
+    if workspace is None:
+        return _P(None), 0
+    return _P(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
+def gemm(a, b, c=None, residual=None, epilogue: str = "plain", workspace=None, status=None,
+         stream=None):
+    """C = A B^T (bf16, fp32 accumulation) on the tensor cores with a fused
+    epilogue: "plain", "residual" (+ residual) or "swiglu" (B's rows in blocks
+    of 128 gate rows and the 128 up rows of the same outputs; C = silu(gate) *
+    up).  a: [m][k], b: [n][k]; returns c ([m][n], [m][n/2] for SwiGLU)."""
+    import torch
+    m, k = a.shape
+    n = b.shape[0]
+    out_n = n // 2 if epilogue == "swiglu" else n
+    if c is None:
+        c = torch.empty((m, out_n), dtype=torch.bfloat16, device=a.device)
+    dt = torch.bfloat16
+    r = _P(None)
+    if residual is not None:
+        r = _dev_ptr(residual, "residual", dt, (m, n))
+    st = _P(status.data_ptr()) if status is not None else _P(None)
+    wsp, wsb = _ws(workspace)
+    _check(lib().rbkv_gemm_bf16(_dev_ptr(a, "a", dt, (m, k)), _dev_ptr(b, "b", dt, (n, k)),
+                                _dev_ptr(c, "c", dt, (m, out_n)), int(m), int(n), int(k), r,
+                                GEMM_EPILOGUES[epilogue], wsp, wsb, st, _stream(stream)))
+    return c
+
+
+def gemm_qkv(a, w_qkv, num_heads_q: int, num_heads_kv: int, head_dim: int, out=None,
+             workspace=None, status=None, stream=None):
+    """The QKV projection in one GEMM: returns Q [m][H_q][D], K and V
+    [m][H_kv][D] (contiguous, the attention pass's inputs; written into `out`
+    = (q, k, v) when given)."""
+    import torch
+    m, k = a.shape
+    n_q, n_kv = num_heads_q * head_dim, num_heads_kv * head_dim
+    dt = torch.bfloat16
+    if out is None:
+        q = torch.empty((m, num_heads_q, head_dim), dtype=dt, device=a.device)
+        kk = torch.empty((m, num_heads_kv, head_dim), dtype=dt, device=a.device)
+        vv = torch.empty_like(kk)
+    else:
+        q, kk, vv = out
+    st = _P(status.data_ptr()) if status is not None else _P(None)
+    wsp, wsb = _ws(workspace)
+    _check(lib().rbkv_gemm_bf16_qkv(_dev_ptr(a, "a", dt, (m, k)),
+                                    _dev_ptr(w_qkv, "w_qkv", dt, (n_q + 2 * n_kv, k)),
+                                    _dev_ptr(q, "q", dt, (m, num_heads_q, head_dim)),
+                                    _dev_ptr(kk, "k", dt, (m, num_heads_kv, head_dim)),
+                                    _dev_ptr(vv, "v", dt, (m, num_heads_kv, head_dim)),
+                                    int(m), int(n_q), int(n_kv), int(k), wsp, wsb, st,
+                                    _stream(stream)))
+    return q, kk, vv
+
+
+def rmsnorm(x, weight, y=None, eps: float = 1e-5, stream=None):
+    """RMSNorm of the rows of x ([m][hidden] bf16) with a bf16 weight."""
+    import torch
+    m, h = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    dt = torch.bfloat16
+    _check(lib().rbkv_rmsnorm_bf16(_dev_ptr(x, "x", dt, (m, h)), _dev_ptr(weight, "weight", dt, (h,)),
+                                   _dev_ptr(y, "y", dt, (m, h)), int(m), int(h), float(eps),
+                                   _stream(stream)))
+    return y
+
+
 class Router:
     """Routing of requests over independent replicas (host only): the replica
     with the fewest outstanding tokens takes the next request (ties: fewer
@@ -556,5 +640,5 @@ class Router:
             pass
 
 
-__all__ = ["Router", "Frame", "budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
+__all__ = ["gemm", "gemm_qkv", "gemm_workspace_bytes", "rmsnorm", "Router", "Frame", "budget_for_latency", "seq_states", "SeqStates", "ragged_attention_noalloc", "kernel_launches", "profile_enable", "profile_reset", "profile_read", "Config", "Composer", "Pass", "PassMeta", "kv_append", "ragged_attention",
            "RbkvError", "NoBlocksError", "lib", "library_path", "SIGNATURES"]

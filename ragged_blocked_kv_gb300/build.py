@@ -24,7 +24,8 @@ LIBDIR = PKG / "_lib"
 LIB = LIBDIR / "librbkv.so"
 
 SOURCES = ["rbkv_host.cpp", "rbkv_kernels.cu", "rbkv_decode.cu", "rbkv_chunk.cu",
-           "rbkv_chunk_single.cu", "rbkv_noalloc.cu", "rbkv_router.cpp"]
+           "rbkv_chunk_single.cu", "rbkv_noalloc.cu", "rbkv_router.cpp",
+           "rbkv_gemm.cu", "rbkv_layer.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -630,6 +630,8 @@ namespace rbkv {
 
 rbkv_status set_error(rbkv_status st, const char* msg) { return fail(st, msg); }
 
+void note_launches(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
 rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache,
                                 const void* v_cache, void* o, void* scratch,
                                 size_t scratch_bytes, cudaStream_t st) {

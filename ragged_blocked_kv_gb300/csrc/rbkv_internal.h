@@ -186,6 +186,19 @@ cudaError_t launch_chunk_single(const DevPass& dp, const ShapeInfo& s, const voi
                                 bool overlap_previous, bool wait_first);
 cudaError_t launch_combine(const DevPass& dp, const ShapeInfo& s, const float* part_o,
                            const float* part_lse, void* o, cudaStream_t st);
+// Decoder-layer dense steps (rbkv_gemm.cu): C = A B^T with an epilogue
+// (0 plain, 1 + residual, 2 SwiGLU over 128-row gate/up blocks of B, 3 C's
+// columns split at split1 and split2 into c, c2 and c3; ldc is C's row
+// stride), and RMSNorm of M rows of H.
+cudaError_t launch_gemm_bf16(const void* a, const void* b, void* c, const void* r, int64_t M,
+                             int64_t N, int64_t K, int64_t ldc, int epilogue, int32_t* status,
+                             cudaStream_t st, void* c2 = nullptr, void* c3 = nullptr,
+                             int64_t split1 = 0, int64_t split2 = 0, void* ws = nullptr,
+                             size_t ws_bytes = 0);
+// Workspace a GEMM of this size uses to split K (0: it does not split).
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_rmsnorm_bf16(const void* x, const void* w, void* y, int64_t M, int64_t H,
+                                float eps, cudaStream_t st);
 // One CTA waiting `limit` cycles on a barrier nothing completes; reports the
 // timeout in `status` (diagnostics).
 cudaError_t launch_wait_timeout(int32_t* status, long long limit, cudaStream_t st);
@@ -198,4 +211,6 @@ rbkv_status attention_on_device(rbkv_pass* p, const void* q, const void* k_cache
                                 const void* v_cache, void* o, void* scratch,
                                 size_t scratch_bytes, cudaStream_t st);
 rbkv_status set_error(rbkv_status st, const char* msg);
+// Count n kernel launches made outside rbkv_host.cpp (rbkv_kernel_launches).
+void note_launches(int64_t n);
 }  // namespace rbkv
