@@ -658,11 +658,62 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    try:
+        line["layer"] = layer_profile(torch, rbkv, device)
+    except Exception as e:  # reported, not fatal: the headline is the attention pass
+        line["layer"] = {"error": str(e)[:200]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess(args)
         rss = resource.getrusage(resource.RUSAGE_CHILDREN).ru_maxrss * 1024
         line["cpu_baseline"]["all_cores"] = cpu_all_cores(args, rss)
     print(json.dumps(line), flush=True)
+
+
+def layer_profile(torch, rbkv, device, tokens=(16, 512, 2048), reps=5):
+    """One Llama-2-7B decoder layer on the library's kernels (RMSNorm, the QKV,
+    output and MLP projections as tensor-core GEMMs with fused epilogues, the
+    KV append and ragged attention) on a pass of one fresh prompt of T
+    tokens: median device time over `reps` runs (each composed, run and
+    rolled back), and the projections' rate (their flops over that time)."""
+    from ragged_blocked_kv_gb300.layer import DecoderLayer, random_weights
+    hidden, hq, hkv, d, ffn = 4096, 32, 32, 128, 11008
+    w = random_weights(hidden, hq, hkv, d, ffn, seed=7, device=device)
+    del w["w_gate"], w["w_up"]
+    layer = DecoderLayer(rbkv, w, hq, hkv, d)
+    tmax = max(tokens)
+    buf = layer.buffers(tmax, device)
+    cfg = rbkv.Config(hq, hkv, d, 64, "bf16", -(-tmax // 64) + 4)
+    comp = rbkv.Composer(cfg)
+    kc = torch.zeros(cfg.cache_shape(), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=device)
+    x = torch.randn(tmax, hidden, device=device).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    gemm_macs = hidden * ((hq + 2 * hkv) * d) + hq * d * hidden + 2 * ffn * hidden + ffn * hidden
+    res = {"model": "Llama-2-7B decoder layer (hidden 4096, 32/32 heads, ffn 11008), random bf16 "
+                    "weights, every step a library kernel; one fresh prompt of T tokens",
+           "tokens": list(tokens), "ms": [], "projection_tflops": []}
+    for T in tokens:
+        times = []
+        for r in range(reps + 2):
+            p = comp.compose(T, 0, [(1, T, 0)])
+
+            def attend(q, k, v, o, p=p):
+                rbkv.kv_append(p, k, v, kc, vc)
+                rbkv.ragged_attention(p, q, kc, vc, o=o, workspace=ws)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            layer.forward_into(x[:T], out[:T], buf, attend, T)
+            e1.record()
+            torch.cuda.synchronize()
+            comp.rollback(p)
+            if r >= 2:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        res["ms"].append(round(ms, 4))
+        res["projection_tflops"].append(round(2.0 * T * gemm_macs / (ms / 1e3) / 1e12, 1))
+    return res
 
 
 # ---------------------------------------------------------------------------
