@@ -17,7 +17,9 @@ prompt is carried through 9 passes (8 chunks of 497 tokens and one of 120)
 next to 15 decode sequences (contexts round(N(2600, 780^2)) clipped to [64,
 8192], one more token per pass); the 9 passes form a cycle that is rolled back
 and repeated.  ``--workload decode_stress``: 64/8 heads, 64 decodes with
-contexts log-uniform in [512, 16000].
+contexts log-uniform in [512, 16000].  ``--workload prefill_mistral``: a
+chunk-dominated pass, 16 prompts each taking a 768-token chunk behind 1536
+cached tokens at the Mistral-7B shape (tensor-core bound).
 
 Output: one JSON line (rank 0).  ``value`` is pass tokens per second with
 inputs already resident in HBM; ``e2e`` is the same through the same calls with
@@ -51,8 +53,8 @@ HBM_FALLBACK_GBS = 6800.0
 # summarised under profiles/, keyed by (workload, kernel) and valid only for
 # the kernel source they were taken on (sha256 prefix of its .cu file)
 TRAFFIC_BYTES = {
-    ("llama2_7b", "decode"): ("rbkv_decode.cu", "4af2001551f6", 614_156_288),
-    ("mistral_7b", "decode"): ("rbkv_decode.cu", "4af2001551f6", 9_177_342_016),
+    ("mistral_7b", "decode"): ("rbkv_decode.cu", "b394238259fb", 9_182_830_000),
+    ("prefill_mistral", "chunk"): ("rbkv_chunk.cu", "69ff5bb693b5", 909_876_736),
 }
 BF16_FALLBACK_TFLOPS = 1900.0
 BF16_SUSTAINED_FALLBACK_TFLOPS = 1700.0   # the same GEMM held for seconds under the power cap
@@ -66,7 +68,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=90)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mistral_7b",
-                    choices=["llama2_7b", "decode_stress", "mistral_7b", "trace", "profile"])
+                    choices=["llama2_7b", "decode_stress", "mistral_7b", "prefill_mistral", "trace",
+                             "profile"])
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per pass (trace and profile workloads)")
     ap.add_argument("--layer", choices=["attention", "full"], default="attention",

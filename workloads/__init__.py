@@ -133,6 +133,20 @@ def mistral_7b(seed: int = 0) -> Scenario:
     return Scenario("mistral_7b", shape, 2048, 768, hist, reqs, num_blocks=nb)
 
 
+def prefill_mistral(seed: int = 0, prompts: int = 16) -> Scenario:
+    """A chunk-dominated pass at the Mistral-7B attention shape (32/8 heads,
+    head_dim 128, bf16, block 64): ``prompts`` prompts of 2304 tokens, each
+    with 1536 tokens cached and its last 768-token chunk in the pass (the
+    second prompt of the Mistral-7B workload, ``prompts`` times); budget
+    768 x prompts, chunk cap 768, no decodes."""
+    del seed  # lengths are fixed
+    shape = Shape(32, 8, 128, 64, "bf16", 1.0 / math.sqrt(128.0))
+    hist = [(10 + i, 1536) for i in range(prompts)]
+    reqs = [(10 + i, 2304, 1536) for i in range(prompts)]
+    nb = _blocks_for([2304] * prompts, 64) + 16
+    return Scenario("prefill_mistral", shape, 768 * prompts, 768, hist, reqs, num_blocks=nb)
+
+
 def short_prompts(num_heads_q: int, num_heads_kv: int, seed: int = 0) -> Scenario:
     """Short prompt chunks next to decodes, head_dim 128, bf16, block 64.
 
@@ -155,6 +169,7 @@ SCENARIOS = {
     "llama2_7b": llama2_7b,
     "decode_stress": decode_stress,
     "mistral_7b": mistral_7b,
+    "prefill_mistral": prefill_mistral,
 }
 
 
