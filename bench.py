@@ -967,8 +967,8 @@ def run_profile_bench(args, rank, world, local_rank):
         "data": "synthetic, random weights",
         "config": {
             "workload": f"profile: {args.layers} layers, "
-                        + ("Llama-2-7B-shaped decoder layers (cuBLAS projections, library "
-                           "attention)" if args.layer == "full" else
+                        + ("Llama-2-7B-shaped decoder layers (library tensor-core "
+                           "projections and attention)" if args.layer == "full" else
                            "library KV append + attention only") + ", fresh prompts, "
                         + ("one CUDA graph per pass" if args.graph else "eager launches"),
             "weights_gb": stack.weight_bytes() / 1e9,
@@ -1079,8 +1079,8 @@ def run_trace_bench(args, rank, world, local_rank):
     (total_ms,), (ntok,) = over_ranks([total_ms], [sum(tokens)], world, device=f"cuda:{local_rank}")
     if rank != 0:
         return
-    what = ("Llama-2-7B-shaped decoder layers (random weights, cuBLAS projections, library "
-            "KV append + attention)" if args.layer == "full" else
+    what = ("Llama-2-7B-shaped decoder layers (random weights, library tensor-core "
+            "projections, KV append and attention)" if args.layer == "full" else
             "library KV append + attention of 32q/32kv heads, head_dim 128, block 64")
     line = {
         "metric": ("SplitFuse forward pass tokens/s" if args.layer == "full"
