@@ -280,33 +280,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
       constexpr uint32_t idesc_o = instr_desc(kRows, 128, 1);
-      const uint32_t q_addr = ptx::smem_u32(q_s);
-      const uint32_t kv_addr = ptx::smem_u32(kv_s);
+      // descriptor words: the high word is common to every operand; the low
+      // words of the Q tiles and of ring stage 0 (as K, K-major, and as V,
+      // MN-major with the two 64-column halves kHalf apart) are offset per MMA
+      const uint32_t hi = desc_hi(1024);
+      const uint32_t q_lo = desc_lo(ptx::smem_u32(q_s), 16);
+      const uint32_t k_lo = desc_lo(ptx::smem_u32(kv_s), 16);
+      const uint32_t v_lo = desc_lo(ptx::smem_u32(kv_s), kHalf);
       // S_X = Q_X K^T into tile X's S columns (after the previous PV of tile X
       // read P_X over the same columns: MMAs of one thread run in order)
       auto issue_qk = [&](int x, uint32_t gk, bool last) {
-        const uint32_t qt = q_addr + x * kTileBytes;
-        const uint32_t kt = kv_addr + (gk % kStages) * kTileBytes;
+        const uint32_t qt = q_lo + ((x * kTileBytes) >> 4);
+        const uint32_t kt = k_lo + (((gk % kStages) * kTileBytes) >> 4);
         const uint32_t d = tmem + x * kTileCols;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // head dims 16kk .. 16kk+15: the half kk/4 of Q and K, 32-byte step kk%4
-          const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc_mma_ss(d, smem_desc(qt + ko, 16, 1024), smem_desc(kt + ko, 16, 1024), idesc_s,
-                    kk > 0);
+          const uint32_t ko = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+          tc_mma_ss_w(d, qt + ko, kt + ko, hi, idesc_s, kk > 0);
         }
         tc_commit(&bars->s_full[x]);
         if (last) tc_commit(&bars->q_empty[x]);
       };
       // O_X += P_X V
       auto issue_pv = [&](int x, uint32_t gv, bool acc) {
-        const uint32_t vt = kv_addr + (gv % kStages) * kTileBytes;
+        const uint32_t vt = v_lo + (((gv % kStages) * kTileBytes) >> 4);
         const uint32_t pt = tmem + x * kTileCols;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
-          tc_mma_ts(pt + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kHalf, 1024), idesc_o,
-                    acc || kk > 0);
+          tc_mma_ts_w(pt + kOCol, pt + kk * 8, vt + ((kk * 2048) >> 4), hi, idesc_o,
+                      acc || kk > 0);
         }
         tc_commit(&bars->o_done[x]);
       };
@@ -444,14 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) sc[c] = c < lim ? sc[c] : -INFINITY;
         }
-        // row max over 8 independent partial maxima
+        // row max: eight independent partial maxima over columns u, u+8, ...,
+        // u+120, each built from three-input maxima (half the instructions)
         float mx8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = sc[u];
+        for (int u = 0; u < 8; ++u) {
+          float a = ptx::fmax3(sc[u], sc[u + 8], sc[u + 16]);
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
-        const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int i = 0; i < 6; ++i) a = ptx::fmax3(a, sc[u + 24 + 16 * i], sc[u + 32 + 16 * i]);
+          mx8[u] = fmaxf(a, sc[u + 120]);
+        }
+        const float mraw = ptx::fmax3(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                                      ptx::fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         // the scale is positive, so the row max scales with it
         const float mt = mraw * qk_scale;
         float corr = 1.f;
@@ -484,21 +492,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // a row with no key in this piece so far keeps m_ref = -inf: its p are 0
         const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+        // P as bf16 pairs over the first 64 S columns (already read), 64 keys
+        // (32 columns) per store.  The scaling and the row sum run as packed
+        // pairs (one instruction for two columns): the softmax is bound by
+        // instruction issue and the exponentials, and it runs while the
+        // tensor pipe works on the other query tile.
         float ps8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
-        // P as bf16 pairs over the first 64 S columns (already read), 64 keys
-        // (32 columns) per store
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float pk[32];
           uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float p0 = ptx::ex2(fmaf(sc[hf * 64 + c], qk_scale, nbase));
-            const float p1 = ptx::ex2(fmaf(sc[hf * 64 + c + 1], qk_scale, nbase));
-            ps8[c & 7] += p0;
-            ps8[(c + 1) & 7] += p1;
+            float x0, x1;
+            ptx::fma2(x0, x1, sc[hf * 64 + c], sc[hf * 64 + c + 1], qk_scale, qk_scale, nbase,
+                      nbase);
+            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+            const int a = (c >> 1) & 3;
+            ptx::add2(ps8[2 * a], ps8[2 * a + 1], p0, p1);
             pk32[c / 2] = ptx::pack_bf16x2(p0, p1);
           }
           tmem_st32(s_col + hf * 32, pk);

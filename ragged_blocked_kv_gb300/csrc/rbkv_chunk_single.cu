@@ -227,16 +227,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc(kRows, kKeys, 0);
       constexpr uint32_t idesc_o = instr_desc(kRows, 128, 1);
-      const uint32_t kv_addr = ptx::smem_u32(kv_s);
+      // descriptor words of ring stage 0 as K (K-major) and as V (MN-major,
+      // halves kKVHalf apart); each MMA adds its offset to the low word
+      const uint32_t hi = desc_hi(1024);
+      const uint32_t k_lo = desc_lo(ptx::smem_u32(kv_s), 16);
+      const uint32_t v_lo = desc_lo(ptx::smem_u32(kv_s) + kKVTile, kKVHalf);
       auto issue_qk = [&](uint32_t t) {
-        const uint32_t kt = kv_addr + (t % kStages) * kStage;
+        const uint32_t kt = k_lo + (((t % kStages) * kStage) >> 4);
         const uint32_t d = tmem + (t & 1) * kKeys;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // head dims 16kk .. 16kk+15: Q columns 8kk.., K's half kk/4, 32-byte step kk%4;
           // N = all 128 keys of the tile
-          const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-          tc_mma_ts(d, tmem + kQCol + kk * 8, smem_desc(kt + ko, 16, 1024), idesc_s, kk > 0);
+          const uint32_t ko = ((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4;
+          tc_mma_ts_w(d, tmem + kQCol + kk * 8, kt + ko, hi, idesc_s, kk > 0);
         }
         tc_commit(&bars->s_full[t & 1]);
       };
@@ -289,13 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t vt = kv_addr + (t % kStages) * kStage + kKVTile;
+          const uint32_t vt = v_lo + (((t % kStages) * kStage) >> 4);
           const uint32_t pt = tmem + (t & 1) * kKeys;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
             // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
-            tc_mma_ts(tmem + kOCol, pt + kk * 8, smem_desc(vt + kk * 2048, kKVHalf, 1024),
-                      idesc_o, j > 0 || kk > 0);
+            tc_mma_ts_w(tmem + kOCol, pt + kk * 8, vt + ((kk * 2048) >> 4), hi, idesc_o,
+                        j > 0 || kk > 0);
           }
           tc_commit(&bars->o_done[t & 1]);
           tc_commit(&bars->kv_empty[t % kStages]);
@@ -382,8 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           const int lh = lim - hf * 64;
           if (full) {
+            // columns u, u+8, ..., u+56 into accumulator u: three-input maxima
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+            for (int u = 0; u < 8; ++u) {
+              float a = ptx::fmax3(mx8[u], sc[u], sc[u + 8]);
+#pragma unroll
+              for (int i = 0; i < 3; ++i) a = ptx::fmax3(a, sc[u + 16 + 16 * i], sc[u + 24 + 16 * i]);
+              mx8[u] = a;
+            }
           } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
@@ -447,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t* pk32 = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float p0 = ptx::ex2(fmaf(sc[c], qk_scale, nbase));
-            const float p1 = ptx::ex2(fmaf(sc[c + 1], qk_scale, nbase));
-            ps8[c & 7] += p0;
-            ps8[(c + 1) & 7] += p1;
+            // scaling and row sum as packed pairs: one instruction per two columns
+            float x0, x1;
+            ptx::fma2(x0, x1, sc[c], sc[c + 1], qk_scale, qk_scale, nbase, nbase);
+            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+            const int a = (c >> 1) & 3;
+            ptx::add2(ps8[2 * a], ps8[2 * a + 1], p0, p1);
             pk32[c / 2] = ptx::pack_bf16x2(p0, p1);
           }
           tmem_st32(s_col + hf * 32, pk);

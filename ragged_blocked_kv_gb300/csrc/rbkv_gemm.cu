@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = instr_desc(kBM, kBN, 0);
-      const uint32_t base = ptx::smem_u32(smem_raw);
+      const uint32_t base_lo = desc_lo(ptx::smem_u32(smem_raw), 16);
+      const uint32_t hi = desc_hi(1024);
       uint32_t it = 0, n = 0;
       bool ok = true;
       int site = 0, at = 0;
@@ -178,12 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = base + s * kStageBytes;
-          const uint32_t b_addr = a_addr + kABytes;
+          // descriptor low words of this stage's A and B tiles (the high word
+          // is common); each 16-column step adds 32 bytes (2 in address units)
+          const uint32_t a_lo = base_lo + ((s * kStageBytes) >> 4);
+          const uint32_t b_lo = a_lo + (kABytes >> 4);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_ss(d, smem_desc(a_addr + kk * 32, 16, 1024), smem_desc(b_addr + kk * 32, 16, 1024),
-                      idesc, ks > k_begin || kk > 0);
+            tc_mma_ss_w(d, a_lo + kk * 2, b_lo + kk * 2, hi, idesc, ks > k_begin || kk > 0);
           tc_commit(&bars->empty[s]);
         }
         if (!ok) break;

@@ -81,14 +81,10 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
-  return d;
+__host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);  // 128-byte swizzle
 }
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, A K-major,
@@ -98,6 +94,49 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+
+// A descriptor split in its two 32-bit words.  Between operands of one
+// layout only the start address (bits 0-13 of the low word, address >> 4)
+// changes, so the issuing thread keeps one low word per operand base and adds
+// (byte offset >> 4) for each MMA: one integer add instead of rebuilding the
+// 64-bit descriptor.  Shared-memory addresses stay below 2^18, so the sum
+// never carries out of the address field.
+__host__ __device__ constexpr uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
+  return ((addr & 0x3FFFF) >> 4) | (((lbo >> 4) & 0x3FFF) << 16);
+}
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFF) | (1u << 14) | (2u << 29);   // version 1, 128-byte swizzle
+}
+static_assert((((uint64_t)desc_hi(1024) << 32) | desc_lo(0x2F3C0, 16)) ==
+                  smem_desc(0x2F3C0, 16, 1024) &&
+              (((uint64_t)desc_hi(1024) << 32) | desc_lo(0x08000, 16384)) ==
+                  smem_desc(0x08000, 16384, 1024) &&
+              desc_lo(0x08000, 16384) + (0x2000 >> 4) == desc_lo(0x0A000, 16384),
+              "descriptor words must match the 64-bit descriptor");
+
+// D[tmem] (+)= A[smem] * B[smem] with the descriptors given as words.
+__device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                            uint32_t hi, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.u32 p, %5, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] with B's descriptor given as words.
+__device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t hi, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.u32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
 
 // D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 in, fp32 accumulate).
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
