@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define RBKV_ABI_VERSION 1
+#define RBKV_ABI_VERSION 2
 
 typedef enum {
   RBKV_OK = 0,
@@ -125,6 +125,11 @@ typedef struct {
   int32_t chunk_items;        /* tensor-core work items: one or two query tiles
                                  sharing the K/V tiles they read */
   int32_t chunk_single;       /* 1 if every work item holds one query tile */
+  int32_t chunk_steps_total;  /* chunk work in key-tile steps (each item: its
+                                 tiles' key tiles, plus one) */
+  int32_t chunk_steps_max;    /* the most of it that one CTA of the persistent
+                                 chunk grid walks, after the items' placement
+                                 was balanced over min(items, SMs) CTAs */
 } rbkv_plan_info;
 
 /* Library ABI version (RBKV_ABI_VERSION). */

@@ -61,7 +61,7 @@ class _PlanInfo(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_sms", "decode_rows", "decode_items", "max_splits", "split_keys", "partials",
         "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk",
-        "chunk_items", "chunk_single")]
+        "chunk_items", "chunk_single", "chunk_steps_total", "chunk_steps_max")]
 
 
 class _FrameCaps(C.Structure):

@@ -8,12 +8,13 @@
 // A work item is one or two 128-row query tiles that read the same K/V tiles:
 // the same rows for two query heads of one KV group (K/V then cross HBM once
 // for both), or two consecutive row tiles of one head when a group has one
-// head.  A persistent grid of one CTA per SM walks the items (longest first,
-// snake order); barrier phases, the K/V ring and tensor memory carry over from
-// item to item.  Roles:
+// head.  A persistent grid of one CTA per SM walks the items in snake order,
+// which the planner fills so that every CTA gets about the same number of
+// key-tile steps; barrier phases, the K/V ring and tensor memory carry over
+// from item to item.  Roles:
 //  - warp 8 (TMA): loads each item's query tiles (A and B) into shared memory
 //    and streams 128-key K and V tiles of the paged cache, in the order
-//    K0 V0 K1 V1 ..., through a 4-stage ring of 32 KB stages (128-byte
+//    K0 V0 K1 V1 ..., through a 5-stage ring of 32 KB stages (128-byte
 //    swizzle), looking block ids up through the block table;
 //  - warp 9 (MMA): one thread issues, per query tile X, S_X = Q_X K^T
 //    (M=128, N=128 keys, K=128; Q from shared memory) into tensor memory and
@@ -32,7 +33,8 @@
 //    its log-sum-exp when the item covers one piece of a split key range).
 // Tensor memory (512 columns x 128 lanes): S/P of A [0,128), O of A
 // [128,256), S/P of B [256,384), O of B [384,512).  Shared memory: Q of A and
-// B (32 KB each) and the ring (128 KB), about 193 KB: one CTA per SM.
+// B (32 KB each) and the ring (160 KB), about 225 KB: one CTA per SM.  Each
+// group of eight MMAs (K = 128) is issued from one instruction block.
 // Every wait is bounded; on timeout the kernel records RBKV_ERR_TIMEOUT, lets
 // its copies and MMAs drain (bounded), frees its tensor memory and returns.
 #include <algorithm>
@@ -55,7 +57,7 @@ using namespace tc;
 
 constexpr int kRows = kChunkTileRows;       // 128 query rows (MMA M)
 constexpr int kKeys = kChunkTileKeys;       // 128 keys per KV tile (MMA N of QK^T)
-constexpr int kStages = 4;                  // ring stages, each one K or one V tile
+constexpr int kStages = 5;                  // ring stages, each one K or one V tile
 constexpr int kHalf = kKeys * 128;          // 16 KB: 128 rows x 64 head dims
 constexpr int kTileBytes = 2 * kHalf;       // 32 KB: 128 rows x 128 head dims
 constexpr int kProducerWarp = 8;
@@ -90,6 +92,7 @@ struct Bars {
   uint64_t s_full[2];    // QK^T of tile X done: S_X readable
   uint64_t p_full[2];    // softmax of tile X done: P_X written (and V tail rows zeroed)
   uint64_t o_done[2];    // PV of tile X done
+  uint64_t drain;        // every MMA the CTA issued done (before tensor memory is freed)
   uint64_t o_free[2];    // epilogue of tile X read O_X: the next item may overwrite it
   uint32_t tmem_base;
   int abort_flag;
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bars->s_full[x], 1);
       ptx::mbar_init(&bars->p_full[x], 4 * 32);
       ptx::mbar_init(&bars->o_done[x], 1);
+      if (x == 0) ptx::mbar_init(&bars->drain, 1);
       ptx::mbar_init(&bars->o_free[x], 4 * 32);
     }
     for (int s = 0; s < kStages; ++s) {
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w = item_of(k);
         if (w < 0) break;
         const Item it = load_item(dp, w);
+        #pragma unroll
         for (int x = 0; x < 2 && !stop; ++x) {
           if (it.n[x] == 0) continue;
           if (qi[x] > 0 &&
@@ -229,20 +234,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int32_t* table = dp.block_ids + dp.chunk_tiles[it.tile[0]].table_off;
         for (int j = 0; j < it.nmax && !stop; ++j) {
-          // cache rows of the boxes of key tile j (-1: out-of-range block, skipped)
-          int32_t rows[kKeys / 8];
-          int nsub = 0, loads = 0;
-          for (int r = 0; r < kKeys; r += box_rows) {
-            const int key = it.kb + j * kKeys + r;
-            if (key >= it.ke) break;
+          // the boxes of key tile j: box i holds keys key0 + i * box_rows ..; a
+          // box whose block id is out of range is skipped (and reported).  Rows
+          // are recomputed where needed rather than kept in an array (a
+          // runtime-indexed array would live in local memory)
+          const int key0 = it.kb + j * kKeys;
+          const int nsub = (min(it.ke - key0, kKeys) + box_rows - 1) / box_rows;
+          auto box_row = [&](int i) -> int {
+            const int key = key0 + i * box_rows;
             const int32_t blk = table[key / B];
-            if (blk < 0 || blk >= dp.num_blocks) {
+            if (blk < 0 || blk >= dp.num_blocks) return -1;
+            return (blk * shp.H_kv + it.kv_head) * B + (key % B);
+          };
+          int loads = 0;
+          for (int i = 0; i < nsub; ++i) {
+            if (box_row(i) >= 0)
+              ++loads;
+            else
               atomicCAS(dp.status, 0, kDevBounds);
-              rows[nsub++] = -1;
-              continue;
-            }
-            rows[nsub++] = (blk * shp.H_kv + it.kv_head) * B + (key % B);
-            ++loads;
           }
           for (int kv = 0; kv < 2; ++kv, ++gi) {
             const int s = gi % kStages;
@@ -261,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = kv_s + s * kTileBytes;
             ptx::mbar_arrive_expect_tx(&bars->kv_full[s], (uint32_t)(loads * box_rows * 128 * 2));
             for (int i = 0; i < nsub; ++i) {
-              if (rows[i] < 0) continue;
+              const int row = box_row(i);
+              if (row < 0) continue;
               const int off = i * box_rows * 128;
-              ptx::tma_load_2d(dst + off, map, 0, rows[i], &bars->kv_full[s]);
-              ptx::tma_load_2d(dst + kHalf + off, map, 64, rows[i], &bars->kv_full[s]);
+              ptx::tma_load_2d(dst + off, map, 0, row, &bars->kv_full[s]);
+              ptx::tma_load_2d(dst + kHalf + off, map, 64, row, &bars->kv_full[s]);
             }
           }
         }
@@ -272,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every copy must land before the CTA may exit
       for (uint32_t t = gi > (uint32_t)kStages ? gi - kStages : 0; t < gi; ++t)
         ptx::mbar_wait(&bars->kv_full[t % kStages], (t / kStages) & 1, kWaitLimit);
+      #pragma unroll
       for (int x = 0; x < 2; ++x)
         if (qi[x] > 0) ptx::mbar_wait(&bars->q_full[x], (qi[x] - 1) & 1, kWaitLimit);
     }
@@ -293,12 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qt = q_lo + ((x * kTileBytes) >> 4);
         const uint32_t kt = k_lo + (((gk % kStages) * kTileBytes) >> 4);
         const uint32_t d = tmem + x * kTileCols;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // head dims 16kk .. 16kk+15: the half kk/4 of Q and K, 32-byte step kk%4
-          const uint32_t ko = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          tc_mma_ss_w(d, qt + ko, kt + ko, hi, idesc_s, kk > 0);
-        }
+        // head dims 16kk .. 16kk+15 in step kk: the half kk/4 of Q and K, 32-byte step kk%4
+        tc_mma_ss_k128(d, qt, kt, hi, idesc_s, false);
         tc_commit(&bars->s_full[x]);
         if (last) tc_commit(&bars->q_empty[x]);
       };
@@ -306,25 +313,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int x, uint32_t gv, bool acc) {
         const uint32_t vt = v_lo + (((gv % kStages) * kTileBytes) >> 4);
         const uint32_t pt = tmem + x * kTileCols;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // keys 16kk .. 16kk+15: P columns 8kk.., V rows 16kk.. (MN-major)
-          tc_mma_ts_w(pt + kOCol, pt + kk * 8, vt + ((kk * 2048) >> 4), hi, idesc_o,
-                      acc || kk > 0);
-        }
+        // keys 16kk .. 16kk+15 in step kk: P columns 8kk.., V rows 16kk.. (MN-major)
+        static_assert(kKeys == 128 && kHalf == 16384, "the K = 128 issue blocks assume these");
+        tc_mma_ts_k128(pt + kOCol, pt, vt, hi, idesc_o, acc);
         tc_commit(&bars->o_done[x]);
       };
       bool ok = true;
       int site = 0, at = 0;
       uint32_t gi = 0, qi[2] = {0, 0}, c[2] = {0, 0}, oi[2] = {0, 0};
-      auto wait_bar = [&](uint64_t* bar, uint32_t parity, int where, int index) {
+      // After a wait on a barrier that other threads' tensor-memory accesses
+      // complete (P written, O read) the MMAs that follow are ordered after
+      // those accesses with a tcgen05 fence.  Tiles that the TMA loaded need
+      // none: the barrier's transaction count already covers the copy.
+      auto wait_bar = [&](uint64_t* bar, uint32_t parity, int where, int index,
+                          bool tmem_sync) {
         if (!ptx::mbar_wait(bar, parity, kWaitLimit) || *abort_flag) {
           ok = false;
           site = where;
           at = index;
           return false;
         }
-        tc_fence_after();
+        if (tmem_sync) tc_fence_after();
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -333,13 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = load_item(dp, w);
         const uint32_t base = gi;
         gi += 2 * it.nmax;
+        #pragma unroll
         for (int x = 0; x < 2 && ok; ++x) {
           if (it.n[x] == 0) continue;
-          if (wait_bar(&bars->q_full[x], qi[x] & 1, 43, k)) ++qi[x];
+          if (wait_bar(&bars->q_full[x], qi[x] & 1, 43, k, false)) ++qi[x];
         }
         // K_0: the first QK^T of both tiles
-        if (!ok || !wait_bar(&bars->kv_full[base % kStages], (base / kStages) & 1, 44, (int)base))
+        if (!ok || !wait_bar(&bars->kv_full[base % kStages], (base / kStages) & 1, 44, (int)base, false))
           break;
+        #pragma unroll
         for (int x = 0; x < 2; ++x)
           if (it.n[x] > 0) issue_qk(x, base, it.n[x] == 1);
         tc_commit(&bars->kv_empty[base % kStages]);
@@ -348,19 +359,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < it.nmax; ++j) {
           const uint32_t gv = base + 2 * j + 1, gk = gv + 1;
           bool v_in = false, k_in = false;
+          #pragma unroll
           for (int x = 0; ok && x < 2; ++x) {
             if (j >= it.n[x]) continue;
-            if (!wait_bar(&bars->p_full[x], c[x] & 1, 46, (int)c[x])) break;
+            if (!wait_bar(&bars->p_full[x], c[x] & 1, 46, (int)c[x], true)) break;
             if (j == 0 && oi[x] > 0 &&   // the previous item's epilogue must have read O_X
-                !wait_bar(&bars->o_free[x], (oi[x] - 1) & 1, 47, (int)oi[x]))
+                !wait_bar(&bars->o_free[x], (oi[x] - 1) & 1, 47, (int)oi[x], true))
               break;
-            if (!v_in && !wait_bar(&bars->kv_full[gv % kStages], (gv / kStages) & 1, 45, (int)gv))
+            if (!v_in && !wait_bar(&bars->kv_full[gv % kStages], (gv / kStages) & 1, 45, (int)gv, false))
               break;
             v_in = true;
             issue_pv(x, gv, j > 0);
             ++c[x];
             if (j + 1 < it.n[x]) {
-              if (!k_in && !wait_bar(&bars->kv_full[gk % kStages], (gk / kStages) & 1, 48, (int)gk))
+              if (!k_in && !wait_bar(&bars->kv_full[gk % kStages], (gk / kStages) & 1, 48, (int)gk, false))
                 break;
               k_in = true;
               issue_qk(x, gk, j + 2 == it.n[x]);
@@ -368,13 +380,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           // a stage is released once every product that reads it was issued
+          // (and its copy has landed)
           tc_commit(&bars->kv_empty[gv % kStages]);
           if (j + 1 < it.nmax) {
-            if (!k_in && !wait_bar(&bars->kv_full[gk % kStages], (gk / kStages) & 1, 49, (int)gk))
+            if (!k_in && !wait_bar(&bars->kv_full[gk % kStages], (gk / kStages) & 1, 49, (int)gk, false))
               break;
             tc_commit(&bars->kv_empty[gk % kStages]);
           }
         }
+        #pragma unroll
         for (int x = 0; x < 2; ++x)
           if (it.n[x] > 0) ++oi[x];
       }
@@ -382,10 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::report_wait(dp.status, kDevTimeout, site, at);
         *abort_flag = 1;
       }
-      // the last PV of each tile (and so every earlier MMA) must finish before
-      // tensor memory is released
-      for (int x = 0; x < 2; ++x)
-        if (c[x] > 0) ptx::mbar_wait(&bars->o_done[x], (c[x] - 1) & 1, kWaitLimit);
+      // every MMA issued must finish before tensor memory is released
+      tc_commit(&bars->drain);
+      ptx::mbar_wait(&bars->drain, 0, kWaitLimit);
     }
   }
   } else {
@@ -402,13 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = item_of(k);
       if (w < 0) break;
       const Item it = load_item(dp, w);
-      const int nx = it.n[x];
+      // this warpgroup's tile, selected without indexing by x (a runtime value)
+      const int nx = x ? it.n[1] : it.n[0];
       if (nx == 0) {
         gbase += 2 * it.nmax;
         continue;
       }
-      const ChunkTile tile = dp.chunk_tiles[it.tile[x]];
-      const int h = it.head[x];
+      const ChunkTile tile = dp.chunk_tiles[x ? it.tile[1] : it.tile[0]];
+      const int h = x ? it.head[1] : it.head[0];
       const int kb = it.kb;
       const int ke = tile.key_end;
       const int pos = tile.pos_begin + row;           // position of this query row

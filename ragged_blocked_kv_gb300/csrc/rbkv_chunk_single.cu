@@ -7,9 +7,10 @@
 // overlaps one tile's softmax with the other tile's products, which needs
 // enough items to give every SM pairs.
 //
-// Roles (one CTA per SM, persistent over the items, longest first in snake
-// order; barrier phases, the K/V ring and the score buffers carry over from
-// item to item, tensor memory is allocated once):
+// Roles (one CTA per SM, persistent over the items, which it walks in snake
+// order, the planner having balanced the key-tile steps per CTA; barrier
+// phases, the K/V ring and the score buffers carry over from item to item,
+// tensor memory is allocated once):
 //  - warp 4 (TMA): streams 128-key K and V tiles of the paged cache into a
 //    3-stage ring (128-byte swizzle), looking block ids up a tile ahead;
 //  - warp 5 (MMA): allocates 512 TMEM columns; one thread issues

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -172,6 +173,7 @@ struct Plan {
   std::vector<ChunkTile> chunk;
   std::vector<ChunkItem> chunk_items;
   std::vector<CombineRow> combine;
+  int64_t chunk_steps_total = 0, chunk_steps_max = 0;
   int32_t n_parts = 0;
   int32_t decode_grid = 0;
   int32_t decode_packed = 0;  // some decode units pack several prompt rows
@@ -253,6 +255,68 @@ void snake_order(std::vector<WorkItem>& items, int32_t G) {
     out[i] = items[src];
   }
   items.swap(out);
+}
+
+// Place chunk work items (sorted longest first) so that the persistent chunk
+// grid of G CTAs, which walks them in snake order (CTA b takes, in round k,
+// position k*G + b on even rounds and k*G + G-1-b on odd ones), ends with
+// nearly equal work per CTA.  Snake dealing alone leaves the CTAs of a last,
+// partial round one item above the rest; here the snake assignment is the
+// start, and items are swapped one for one (so every CTA keeps its number of
+// positions) between the most and the least loaded CTA while a swap narrows
+// their gap.  Each CTA then takes its items longest first.  `cost` is an
+// item's work in key-tile steps; returns the most work one CTA gets.
+int64_t balance_chunk_items(std::vector<ChunkItem>& items, int32_t G,
+                            const std::vector<int32_t>& cost) {
+  const size_t n = items.size();
+  if (G <= 0 || n <= (size_t)G)
+    return n ? (int64_t)*std::max_element(cost.begin(), cost.end()) : 0;
+  auto cta_of = [&](size_t pos) -> int32_t {
+    const size_t k = pos / G, i = pos % G;
+    return (int32_t)((k & 1) ? G - 1 - i : i);
+  };
+  std::vector<std::vector<int32_t>> bins(G);   // item indices of each CTA
+  std::vector<int64_t> load(G, 0);
+  for (size_t pos = 0; pos < n; ++pos) {
+    const int32_t b = cta_of(pos);
+    bins[b].push_back((int32_t)pos);
+    load[b] += cost[pos];
+  }
+  for (int iter = 0; iter < 8 * G; ++iter) {
+    int32_t hi = 0, lo = 0;
+    for (int32_t b = 1; b < G; ++b) {
+      if (load[b] > load[hi]) hi = b;
+      if (load[b] < load[lo]) lo = b;
+    }
+    const int64_t gap = load[hi] - load[lo];
+    int best_a = -1, best_b = -1;
+    int64_t best_d = 0;
+    for (size_t a = 0; a < bins[hi].size(); ++a)
+      for (size_t c = 0; c < bins[lo].size(); ++c) {
+        const int64_t d = (int64_t)cost[bins[hi][a]] - cost[bins[lo][c]];
+        if (d <= 0 || d >= gap) continue;
+        if (best_a < 0 || std::llabs(gap - 2 * d) < std::llabs(gap - 2 * best_d)) {
+          best_a = (int)a;
+          best_b = (int)c;
+          best_d = d;
+        }
+      }
+    if (best_a < 0) break;
+    std::swap(bins[hi][best_a], bins[lo][best_b]);
+    load[hi] -= best_d;
+    load[lo] += best_d;
+  }
+  std::vector<ChunkItem> out(n);
+  std::vector<size_t> next(G, 0);
+  for (int32_t b = 0; b < G; ++b)
+    std::stable_sort(bins[b].begin(), bins[b].end(),
+                     [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+  for (size_t pos = 0; pos < n; ++pos) {
+    const int32_t b = cta_of(pos);
+    out[pos] = items[bins[b][next[b]++]];
+  }
+  items.swap(out);
+  return *std::max_element(load.begin(), load.end());
 }
 
 Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
@@ -471,7 +535,24 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
                    [](const ChunkItem& a, const ChunkItem& b) {
                      return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
                    });
-  int32_t grid = (int32_t)std::min<int64_t>((int64_t)decode.size(),
+  if (!pl.chunk_items.empty()) {
+    // an item's work: the key-tile steps of its query tiles, plus one for its
+    // epilogue
+    std::vector<int32_t> cost(pl.chunk_items.size());
+    for (size_t i = 0; i < cost.size(); ++i) {
+      const ChunkItem& ci = pl.chunk_items[i];
+      int32_t c = 1;
+      for (int x = 0; x < 2; ++x)
+        if (ci.tile[x] >= 0)
+          c += ceil_div(pl.chunk[ci.tile[x]].key_end - ci.key_begin, kChunkTileKeys);
+      cost[i] = c;
+    }
+    for (int32_t c : cost) pl.chunk_steps_total += c;
+    pl.chunk_steps_max = balance_chunk_items(
+        pl.chunk_items, (int32_t)std::min<int64_t>((int64_t)cost.size(), std::max(1, num_sms)),
+        cost);
+  }
+  int32_t grid =(int32_t)std::min<int64_t>((int64_t)decode.size(),
                                             (int64_t)std::max(1, num_sms) * decode_ctas_per_sm(s));
   if (grid > 0) snake_order(decode, grid);
   pl.decode_grid = grid;
@@ -489,6 +570,8 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   in.chunk_tiles = (int32_t)pl.chunk.size();
   in.chunk_items = (int32_t)pl.chunk_items.size();
   in.chunk_single = pl.chunk_single;
+  in.chunk_steps_total = (int32_t)std::min<int64_t>(pl.chunk_steps_total, INT32_MAX);
+  in.chunk_steps_max = (int32_t)std::min<int64_t>(pl.chunk_steps_max, INT32_MAX);
   in.generic_items = (int32_t)pl.generic.size();
   in.fast_decode = fast_decode ? 1 : 0;
   in.fast_chunk = fast_chunk ? 1 : 0;

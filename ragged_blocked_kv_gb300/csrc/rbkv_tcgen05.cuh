@@ -138,6 +138,65 @@ __device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Eight MMAs over K = 128 (eight K = 16 steps) in one block, with the
+// per-step operand offsets as immediates, so that nothing the compiler
+// schedules sits between them.
+// SS, both operands K-major with 128-byte swizzle and two 64-column halves
+// 16 KB apart: step kk reads columns 16kk.. at byte offset (kk/4) * 16384 +
+// (kk%4) * 32, i.e. descriptor address units 0, 2, 4, 6, 1024, ..., 1030.
+__device__ __forceinline__ void tc_mma_ss_k128(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                               uint32_t hi, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 a, b;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.u32 p0, %5, 0;\n\tsetp.eq.u32 p1, %5, %5;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p0;\n\t"
+      "add.u32 a, %1, 2;\n\tadd.u32 b, %2, 2;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 a, %1, 4;\n\tadd.u32 b, %2, 4;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 a, %1, 6;\n\tadd.u32 b, %2, 6;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 a, %1, 1024;\n\tadd.u32 b, %2, 1024;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 a, %1, 1026;\n\tadd.u32 b, %2, 1026;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 a, %1, 1028;\n\tadd.u32 b, %2, 1028;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 a, %1, 1030;\n\tadd.u32 b, %2, 1030;\n\tmov.b64 da, {a, %3};\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// TS over K = 128: A (P, bf16 pairs) in tensor memory, step kk at column
+// a_tmem + 8kk; B (V) MN-major with 128-byte swizzle, step kk 16 rows on,
+// i.e. 2048 bytes = 128 descriptor address units.
+__device__ __forceinline__ void tc_mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t hi, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 a, b;\n\t.reg .b64 db;\n\t"
+      "setp.ne.u32 p0, %5, 0;\n\tsetp.eq.u32 p1, %5, %5;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+      "add.u32 a, %1, 8;\n\tadd.u32 b, %2, 128;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t"
+      "add.u32 a, %1, 16;\n\tadd.u32 b, %2, 256;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t"
+      "add.u32 a, %1, 24;\n\tadd.u32 b, %2, 384;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t"
+      "add.u32 a, %1, 32;\n\tadd.u32 b, %2, 512;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t"
+      "add.u32 a, %1, 40;\n\tadd.u32 b, %2, 640;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t"
+      "add.u32 a, %1, 48;\n\tadd.u32 b, %2, 768;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t"
+      "add.u32 a, %1, 56;\n\tadd.u32 b, %2, 896;\n\tmov.b64 db, {b, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 in, fp32 accumulate).
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, bool accumulate) {
