@@ -54,7 +54,9 @@ HBM_FALLBACK_GBS = 6800.0
 # the kernel source they were taken on (sha256 prefix of its .cu file)
 TRAFFIC_BYTES = {
     ("mistral_7b", "decode"): ("rbkv_decode.cu", "b394238259fb", 9_182_830_000),
-    ("prefill_mistral", "chunk"): ("rbkv_chunk.cu", "69ff5bb693b5", 909_876_736),
+    ("llama2_7b", "decode"): ("rbkv_decode.cu", "b394238259fb", 614_143_744),
+    ("decode_stress", "decode"): ("rbkv_decode.cu", "b394238259fb", 1_182_816_768),
+    ("prefill_mistral", "chunk"): ("rbkv_chunk.cu", "a1a66ed0886e", 770_232_832),
 }
 BF16_FALLBACK_TFLOPS = 1900.0
 BF16_SUSTAINED_FALLBACK_TFLOPS = 1700.0   # the same GEMM held for seconds under the power cap
