@@ -20,6 +20,13 @@
 // memory (2 x 256 columns) so that a tile's epilogue overlaps the next tile's
 // products.  Warp 0 loads, warp 1 issues the MMAs, warps 2-5 (one TMEM lane
 // quadrant each) run the epilogue.  Every wait is bounded.
+// Schedule: whole waves of tiles run as whole tiles; when the tiles that are
+// left would fill a last wave only in part, their K range is split into
+// pieces spread over all SMs (fp32 partials in a caller workspace, summed and
+// finished by a second kernel).  With fewer tiles than SMs, every tile is
+// split.  The tiles left over are the last column blocks (tiles are numbered
+// with the M tiles of one weight tile next to each other), so the partials
+// cover only those columns.
 #include <algorithm>
 #include <atomic>
 
@@ -68,10 +75,36 @@ struct GemmArgs {
   int32_t ldc;                // row stride of C (and R) in elements
   int32_t epilogue;           // 0 plain, 1 residual, 2 SwiGLU, 3 split into three outputs
   int32_t m_tiles, n_tiles;
-  int32_t splits;             // K split in this many pieces (1: no split)
+  int32_t full;               // tiles 0 .. full-1 run whole (a multiple of m_tiles)
+  int32_t splits;             // the other tiles' K in this many pieces (1: none left)
   int32_t kps;                // k steps per piece
-  float* ws;                  // splits > 1: fp32 partials [splits][M][N]
+  int32_t tail_col0;          // first column of the split tiles: (full / m_tiles) * kBN
+  float* ws;                  // fp32 partials [splits][M][N - tail_col0]
 };
+
+// Work unit u: a whole tile (u < full) or one K piece of a split tile.
+struct Unit {
+  int tile, piece, k_begin, k_end;
+  bool partial;
+};
+__device__ __forceinline__ Unit unit_of(const GemmArgs& g, int u, int k_steps) {
+  Unit x;
+  if (u < g.full) {
+    x.tile = u;
+    x.piece = 0;
+    x.k_begin = 0;
+    x.k_end = k_steps;
+    x.partial = false;
+  } else {
+    const int v = u - g.full;
+    x.tile = g.full + v / g.splits;
+    x.piece = v % g.splits;
+    x.k_begin = x.piece * g.kps;
+    x.k_end = min(k_steps, x.k_begin + g.kps);
+    x.partial = true;
+  }
+  return x;
+}
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
 
@@ -86,8 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   GemmBars* bars = reinterpret_cast<GemmBars*>(smem_raw + kStages * kStageBytes);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work unit u: tile u / splits, piece u % splits of K
-  const int units = g.m_tiles * g.n_tiles * g.splits;
+  const int units = g.full + (g.m_tiles * g.n_tiles - g.full) * g.splits;
   const int k_steps = (g.K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -121,10 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < units && !stop; u += gridDim.x) {
-        const int t = u / g.splits, piece = u % g.splits;
-        const int m0 = (t % g.m_tiles) * kBM, n0 = (t / g.m_tiles) * kBN;
-        const int k_end = min(k_steps, (piece + 1) * g.kps);
-        for (int ks = piece * g.kps; ks < k_end; ++ks, ++it) {
+        const Unit w = unit_of(g, u, k_steps);
+        const int m0 = (w.tile % g.m_tiles) * kBM, n0 = (w.tile / g.m_tiles) * kBN;
+        for (int ks = w.k_begin; ks < w.k_end; ++ks, ++it) {
           const int s = it % kStages;
           if (*abort_flag) {
             stop = true;
@@ -157,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int site = 0, at = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++n) {
-        const int piece = u % g.splits;
-        const int k_begin = piece * g.kps, k_end = min(k_steps, (piece + 1) * g.kps);
+        const Unit w = unit_of(g, u, k_steps);
+        const int k_begin = w.k_begin, k_end = w.k_end;
         const uint32_t buf = n & 1;
         // the epilogue must have read this accumulator's previous tile
         if (n >= 2 && (!ptx::mbar_wait(&bars->acc_empty[buf], ((n >> 1) - 1) & 1, kWaitLimit) ||
@@ -208,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++n) {
-      const int t = u / g.splits, piece = u % g.splits;
+      const Unit w = unit_of(g, u, k_steps);
+      const int t = w.tile, piece = w.piece;
       const uint32_t buf = n & 1;
       const bool got = ptx::mbar_wait(&bars->acc_full[buf], (n >> 1) & 1, kWaitLimit);
       if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -220,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = m0 + row_in_tile;
       const bool live = row < g.M;
       const uint32_t taddr = tmem + buf * kAccCols + ((uint32_t)(quad * 32) << 16);
-      if (g.splits > 1) {
+      if (w.partial) {
         // one piece of K: the fp32 partial sums go to the workspace; the
         // reduce kernel adds the pieces and applies the epilogue
 #pragma unroll 1
@@ -230,8 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           const int col = n0 + c * 32;
           if (live && col < g.N) {
+            const int tail_cols = g.N - g.tail_col0;
             float4* dst = reinterpret_cast<float4*>(
-                g.ws + ((int64_t)piece * g.M + row) * g.N + col);
+                g.ws + ((int64_t)piece * g.M + row) * tail_cols + (col - g.tail_col0));
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -322,19 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Split-K reduction: the pieces' fp32 partials summed, then the epilogue
 // ---------------------------------------------------------------------------
-// Thread i takes 8 consecutive outputs of C (of the SwiGLU output for
-// epilogue 2: the 8 gates and the 8 ups of those outputs).
+// Thread i takes 8 consecutive outputs of C in the split tiles' columns (of
+// the SwiGLU output for epilogue 2: the 8 gates and the 8 ups of those
+// outputs).
 __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(GemmArgs g) {
   const int out_n = g.epilogue == 2 ? g.N / 2 : g.N;
+  const int out_c0 = g.epilogue == 2 ? g.tail_col0 / 2 : g.tail_col0;
+  const int tail_cols = g.N - g.tail_col0;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t per_row = out_n / 8;
+  const int64_t per_row = (out_n - out_c0) / 8;
   if (i >= (int64_t)g.M * per_row) return;
-  const int row = (int)(i / per_row), j0 = (int)(i % per_row) * 8;
-  const int64_t piece_stride = (int64_t)g.M * g.N;
+  const int row = (int)(i / per_row), j0 = out_c0 + (int)(i % per_row) * 8;
+  const int64_t piece_stride = (int64_t)g.M * tail_cols;
   auto sum8 = [&](int col, float* v) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = 0.f;
-    const float* src = g.ws + (int64_t)row * g.N + col;
+    const float* src = g.ws + (int64_t)row * tail_cols + (col - g.tail_col0);
     for (int p = 0; p < g.splits; ++p) {
       const float4 a = *reinterpret_cast<const float4*>(src + p * piece_stride);
       const float4 b = *reinterpret_cast<const float4*>(src + p * piece_stride + 4);
@@ -437,21 +473,50 @@ int sms_of_current(cudaError_t* err) {
 
 }  // namespace
 
-int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-  const int64_t k_steps = (K + kBK - 1) / kBK;
-  if (tiles >= sms) return 1;
-  // enough pieces to give every SM a unit, each at least 8 k steps long
-  int64_t s = std::min<int64_t>(sms / tiles, k_steps / 8);
-  return (int)std::max<int64_t>(1, std::min<int64_t>(s, 16));
+// How a product is scheduled over `sms` SMs: the tiles that run whole, the
+// pieces each other tile's K is split into, and the k steps of a piece.
+struct GemmPlan {
+  int64_t full, splits, kps, tail_col0;
+};
+
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
+  const int64_t tiles = m_tiles * n_tiles, k_steps = (K + kBK - 1) / kBK;
+  const GemmPlan whole{tiles, 1, k_steps, N};
+  if (sms <= 0) return whole;
+  // the tiles of whole waves run whole (rounded down to whole column blocks);
+  // the rest are split into enough pieces to give every SM a unit, each at
+  // least 8 k steps long
+  const int64_t full = tiles < sms ? 0 : (tiles / sms) * sms / m_tiles * m_tiles;
+  const int64_t tail = tiles - full;
+  if (tail == 0) return whole;
+  int64_t s = std::min<int64_t>({(int64_t)sms / tail, k_steps / 8, 16});
+  if (s < 2) return whole;
+  const int64_t kps = (k_steps + s - 1) / s;
+  s = (k_steps + kps - 1) / kps;   // no empty piece
+  // k steps on the busiest SM, whole tiles against the split schedule (the
+  // grid walks units b, b + G, ...; the reduce kernel's pass comes on top)
+  auto busiest = [&](int64_t f, int64_t pieces, int64_t per_piece) {
+    const int64_t units = f + (tiles - f) * pieces;
+    const int64_t G = std::min<int64_t>(units, sms);
+    int64_t worst = 0;
+    for (int64_t b = 0; b < G; ++b) {
+      int64_t load = 0;
+      for (int64_t u = b; u < units; u += G) load += u < f ? k_steps : per_piece;
+      worst = std::max(worst, load);
+    }
+    return worst;
+  };
+  if (10 * busiest(full, s, kps) > 9 * busiest(tiles, 1, k_steps)) return whole;
+  return GemmPlan{full, s, kps, full / m_tiles * kBN};
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   cudaError_t e;
   const int sms = sms_of_current(&e);
   if (e != cudaSuccess || sms <= 0) return 0;
-  const int s = gemm_splits(M, N, K, sms);
-  return s > 1 ? (size_t)s * M * N * sizeof(float) : 0;
+  const GemmPlan p = gemm_plan(M, N, K, sms);
+  return p.splits > 1 ? (size_t)p.splits * M * (N - p.tail_col0) * sizeof(float) : 0;
 }
 
 cudaError_t launch_gemm_bf16(const void* a, const void* b, void* c, const void* r, int64_t M,
@@ -492,12 +557,18 @@ cudaError_t launch_gemm_bf16(const void* a, const void* b, void* c, const void* 
   g.m_tiles = (int32_t)((M + kBM - 1) / kBM);
   g.n_tiles = (int32_t)((N + kBN - 1) / kBN);
   const int64_t k_steps = (K + kBK - 1) / kBK;
-  g.splits = ws ? gemm_splits(M, N, K, sms) : 1;
-  if (g.splits > 1 && ws_bytes < (size_t)g.splits * M * N * sizeof(float)) g.splits = 1;
-  g.kps = (int32_t)((k_steps + g.splits - 1) / g.splits);
-  g.splits = (int32_t)((k_steps + g.kps - 1) / g.kps);   // no empty piece
+  // the split schedule needs the caller's workspace; without one (or with
+  // one too small) every tile runs whole
+  GemmPlan plan = gemm_plan(M, N, K, sms);
+  if (!ws || (plan.splits > 1 && ws_bytes < (size_t)plan.splits * M * (N - plan.tail_col0) *
+                                                sizeof(float)))
+    plan = GemmPlan{(int64_t)g.m_tiles * g.n_tiles, 1, k_steps, N};
+  g.full = (int32_t)plan.full;
+  g.splits = (int32_t)plan.splits;
+  g.kps = (int32_t)plan.kps;
+  g.tail_col0 = (int32_t)plan.tail_col0;
   g.ws = (float*)ws;
-  const int64_t units = (int64_t)g.m_tiles * g.n_tiles * g.splits;
+  const int64_t units = plan.full + ((int64_t)g.m_tiles * g.n_tiles - plan.full) * plan.splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::min<int64_t>(units, std::max(1, sms)));
   cfg.blockDim = dim3(kThreads);
@@ -505,7 +576,7 @@ cudaError_t launch_gemm_bf16(const void* a, const void* b, void* c, const void* 
   cfg.stream = st;
   e = cudaLaunchKernelEx(&cfg, gemm_bf16_tcgen05_kernel, ta, tb, g);
   if (e != cudaSuccess || g.splits == 1) return e;
-  const int64_t threads = M * ((epilogue == 2 ? N / 2 : N) / 8);
+  const int64_t threads = M * ((epilogue == 2 ? (N - plan.tail_col0) / 2 : N - plan.tail_col0) / 8);
   gemm_splitk_reduce_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(g);
   return cudaGetLastError();
 }

@@ -47,18 +47,25 @@ def _workspace(rbkv, m, n, k, split):
 
 @pytest.mark.parametrize("m,n,k", [(1, 32, 8), (100, 288, 200), (128, 256, 64), (257, 4096, 4096),
                                    (512, 12288, 4096), (300, 4096, 11008), (16, 4096, 11008),
-                                   (1, 12288, 4096)])
+                                   (1, 12288, 4096), (1280, 12288, 2048), (384, 26624, 1024)])
 @pytest.mark.parametrize("epilogue", ["plain", "residual"])
 @pytest.mark.parametrize("split", [False, True])
 def test_gemm_against_fp64(rbkv, m, n, k, epilogue, split):
     """With a workspace, products with fewer 128 x 256 tiles than SMs split K
-    over several SMs (the last two shapes: 16 and 48 tiles); same bar."""
+    over several SMs (16 and 48 tiles), and products whose tiles fill a last
+    wave only in part run whole waves whole and split the rest (512 x 12288:
+    152 whole tiles and 40 in 3 pieces; 1280 x 12288 x 2048: 450 whole, 30 in 4;
+    384 x 26624: 303 whole, 9 in 2); same bar."""
     gen = torch.Generator().manual_seed(m * 7 + n + k)
     a = _bf16((m, k), gen)
     b = _bf16((n, k), gen, 1.0 / math.sqrt(k))
     r = _bf16((m, n), gen) if epilogue == "residual" else None
-    if split and (m, n, k) in ((16, 4096, 11008), (1, 12288, 4096)):
+    if split and (m, n, k) in ((16, 4096, 11008), (1, 12288, 4096), (512, 12288, 4096),
+                               (1280, 12288, 2048), (384, 26624, 1024)):
         assert rbkv.gemm_workspace_bytes(m, n, k) > 0
+    if (m, n, k) == (512, 12288, 4096):
+        # the partials cover only the 40 split tiles' columns: 3 x 512 x 2560 fp32
+        assert rbkv.gemm_workspace_bytes(m, n, k) == 3 * 512 * 2560 * 4
     c = rbkv.gemm(a.cuda(), b.cuda(), residual=None if r is None else r.cuda(), epilogue=epilogue,
                   workspace=_workspace(rbkv, m, n, k, split))
     torch.cuda.synchronize()
@@ -87,7 +94,7 @@ def test_gemm_swiglu_against_fp64(rbkv, m, ffn, k, split):
     _check_gemm(c, ref, absdot)
 
 
-@pytest.mark.parametrize("hq,hkv,m", [(32, 32, 130), (32, 8, 130), (32, 8, 5)])
+@pytest.mark.parametrize("hq,hkv,m", [(32, 32, 130), (32, 8, 130), (32, 8, 5), (32, 32, 512)])
 def test_gemm_qkv_split_outputs(rbkv, hq, hkv, m):
     k, D = 4096, 128
     gen = torch.Generator().manual_seed(hq + hkv)
