@@ -1133,9 +1133,9 @@ class OracleRunner:
     the oracle composer after each cycle).
 
     A step is one pass: oracle composition and appending of the whole pass,
-    then oracle attention for ``pairs`` (row, query head) outputs of it, taken
-    in row-major order and continuing from step to step, so that every row and
-    head of the cycle is covered in turn.  A token counts as 1/H_q per output
+    then oracle attention for ``pairs`` (row, query head) outputs of it, the
+    rows taken in a stride permutation of the pass and continuing from step to
+    step, so that every row and head of the cycle is covered in turn.  A token counts as 1/H_q per output
     pair computed.  ``step`` returns the tokens credited, the seconds spent
     composing and appending, and the pass's tokens (for charging that per-pass
     cost in proportion to the tokens a sample credits)."""
@@ -1183,11 +1183,18 @@ class OracleRunner:
         self.oracle.kv_append(m, k, v, self.kc, self.vc)
         fixed = time.perf_counter() - t0
         H = self.shape.num_heads_q
-        total = m.num_tokens * H
+        T = m.num_tokens
+        total = T * H
+        # rows in a stride permutation of the pass (the stride is odd and
+        # prime to T), so that a short sample spreads over prompt rows and
+        # decode rows alike instead of taking the pass's first rows
+        stride = next(d for d in range(max(1, int(T * 0.618)) | 1, 2 * T + 2, 2)
+                      if math.gcd(d, T) == 1) if T else 1
         done = 0
         while done < pairs and total:
             c = self.cursor % total
-            t, h0 = divmod(c, H)
+            i, h0 = divmod(c, H)
+            t = (i * stride) % T
             n = min(pairs - done, H - h0)
             self.oracle.blocked_attention(m, q, self.kc, self.vc, H, tokens=[t],
                                           heads=range(h0, h0 + n))
