@@ -803,6 +803,7 @@ rbkv_status rbkv_compose_pass(rbkv_composer* c, int32_t token_budget, int32_t ma
 rbkv_status rbkv_compose_pass_policy(rbkv_composer* c, int32_t token_budget, int32_t max_chunk,
                                      int32_t chunk_policy, const rbkv_seq_state* states,
                                      int32_t n_states, rbkv_pass** out) {
+  rbkv::NvtxRange nvtx_range("rbkv_compose_pass");
   if (!c || !out) return fail(RBKV_ERR_INVALID, "composer or out is NULL");
   if (chunk_policy != RBKV_CHUNK_GREEDY && chunk_policy != RBKV_CHUNK_EQUAL)
     return fail(RBKV_ERR_INVALID, "unknown chunk policy");
@@ -1048,6 +1049,7 @@ void rbkv_pass_destroy(rbkv_pass* p) {
 
 rbkv_status rbkv_kv_append(rbkv_pass* p, const void* k_new, const void* v_new, void* k_cache,
                            void* v_cache, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_kv_append");
   if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
   if (p->slot.empty()) return RBKV_OK;
   if (!k_new || !v_new || !k_cache || !v_cache) return fail(RBKV_ERR_INVALID, "NULL tensor");
@@ -1070,6 +1072,7 @@ size_t rbkv_attention_workspace_bytes(rbkv_pass* p) {
 rbkv_status rbkv_ragged_attention(rbkv_pass* p, const void* q, const void* k_cache,
                                   const void* v_cache, void* o, void* workspace,
                                   size_t workspace_bytes, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_ragged_attention");
   if (!p) return fail(RBKV_ERR_INVALID, "pass is NULL");
   if (p->slot.empty()) return RBKV_OK;
   if (!q || !k_cache || !v_cache || !o) return fail(RBKV_ERR_INVALID, "NULL tensor");
@@ -1283,6 +1286,7 @@ rbkv_status rbkv_frame_create(const rbkv_config* cfg, const rbkv_frame_caps* cap
 void rbkv_frame_destroy(rbkv_frame* f) { delete f; }
 
 rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_frame_load");
   if (!f || !p) return fail(RBKV_ERR_INVALID, "frame or pass is NULL");
   if (!same_config(f->cfg, p->cfg)) return fail(RBKV_ERR_INVALID, "pass and frame configs differ");
   int dev = -1;
@@ -1363,6 +1367,7 @@ rbkv_status rbkv_frame_load(rbkv_frame* f, rbkv_pass* p, rbkv_stream stream) {
 
 rbkv_status rbkv_frame_kv_append(rbkv_frame* f, const void* k_new, const void* v_new,
                                  void* k_cache, void* v_cache, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_frame_kv_append");
   if (!f) return fail(RBKV_ERR_INVALID, "frame is NULL");
   if (!k_new || !v_new || !k_cache || !v_cache) return fail(RBKV_ERR_INVALID, "NULL tensor");
   cudaStream_t st = (cudaStream_t)stream;
@@ -1383,6 +1388,7 @@ size_t rbkv_frame_workspace_bytes(const rbkv_frame* f) {
 rbkv_status rbkv_frame_attention(rbkv_frame* f, const void* q, const void* k_cache,
                                  const void* v_cache, void* o, void* workspace,
                                  size_t workspace_bytes, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_frame_attention");
   if (!f) return fail(RBKV_ERR_INVALID, "frame is NULL");
   if (!q || !k_cache || !v_cache || !o) return fail(RBKV_ERR_INVALID, "NULL tensor");
   const size_t need = rbkv_frame_workspace_bytes(f);

@@ -6,10 +6,23 @@
 #include <stdint.h>
 
 #include "rbkv.h"
+#include <nvtx3/nvToolsExt.h>
 
 struct CUtensorMap_st;  // cuda.h's tensor-map type
 
 namespace rbkv {
+
+// A named NVTX range around a library call, so that a profiler that records
+// NVTX (`ncu --nvtx`, Nsight Systems) shows composition, appends, attention
+// and the layer's steps by name; without such a tool attached the push and
+// pop cost a test of a function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 
 // One unit of split attention work: the keys [key_begin, key_end) of one
 // sequence's KV head, for n_rows consecutive pass rows of that sequence (all

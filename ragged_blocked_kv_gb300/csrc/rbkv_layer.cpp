@@ -20,6 +20,7 @@ size_t rbkv_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
 rbkv_status rbkv_gemm_bf16(const void* a, const void* b, void* c, int64_t m, int64_t n, int64_t k,
                            const void* residual, int32_t epilogue, void* workspace,
                            size_t workspace_bytes, int32_t* status, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_gemm_bf16");
   if (m < 0 || n < 1 || k < 1) return invalid("m must be >= 0, n and k >= 1");
   if (m == 0) return RBKV_OK;
   if (!a || !b || !c) return invalid("NULL operand");
@@ -61,6 +62,7 @@ rbkv_status rbkv_gemm_bf16_qkv(const void* a, const void* w_qkv, void* q, void* 
                                void* v_out, int64_t m, int64_t n_q, int64_t n_kv, int64_t k,
                                void* workspace, size_t workspace_bytes, int32_t* status,
                                rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_gemm_bf16_qkv");
   if (m < 0 || n_q < 1 || n_kv < 1 || k < 1) return invalid("bad sizes");
   if (m == 0) return RBKV_OK;
   if (!a || !w_qkv || !q || !k_out || !v_out) return invalid("NULL operand");
@@ -86,6 +88,7 @@ rbkv_status rbkv_gemm_bf16_qkv(const void* a, const void* w_qkv, void* q, void* 
 
 rbkv_status rbkv_rmsnorm_bf16(const void* x, const void* weight, void* y, int64_t m,
                               int64_t hidden, float eps, rbkv_stream stream) {
+  rbkv::NvtxRange nvtx_range("rbkv_rmsnorm_bf16");
   if (m < 0 || hidden < 8 || hidden % 8) return invalid("hidden must be a positive multiple of 8");
   if (m == 0) return RBKV_OK;
   if (!x || !weight || !y) return invalid("NULL tensor");
