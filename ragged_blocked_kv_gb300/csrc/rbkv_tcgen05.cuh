@@ -35,17 +35,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                    ptx::smem_u32(bar))
                : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16 (bf16 in, fp32 accumulate).  A is
-// M rows = TMEM lanes, its K elements packed two per 32-bit column.
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
@@ -81,6 +70,8 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+// The kernels issue MMAs with its two 32-bit words (below); this 64-bit form
+// is the definition the words are checked against.
 __host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) |
@@ -114,7 +105,8 @@ static_assert((((uint64_t)desc_hi(1024) << 32) | desc_lo(0x2F3C0, 16)) ==
               desc_lo(0x08000, 16384) + (0x2000 >> 4) == desc_lo(0x0A000, 16384),
               "descriptor words must match the 64-bit descriptor");
 
-// D[tmem] (+)= A[smem] * B[smem] with the descriptors given as words.
+// D[tmem] (+)= A[smem] * B[smem] with the descriptors given as words,
+// kind::f16 (bf16 in, fp32 accumulate).
 __device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                             uint32_t hi, uint32_t idesc, bool accumulate) {
   asm volatile(
@@ -126,7 +118,8 @@ __device__ __forceinline__ void tc_mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem] with B's descriptor given as words.
+// D[tmem] (+)= A[tmem] * B[smem] with B's descriptor given as words.  A is M
+// rows = TMEM lanes, its K elements packed two per 32-bit column.
 __device__ __forceinline__ void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                             uint32_t hi, uint32_t idesc, bool accumulate) {
   asm volatile(
@@ -194,17 +187,6 @@ __device__ __forceinline__ void tc_mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem,
       "add.u32 a, %1, 56;\n\tadd.u32 b, %2, 896;\n\tmov.b64 db, {b, %3};\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %4, p1;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 
