@@ -438,9 +438,13 @@ class GpuRunner:
         the pass tokens."""
         torch, rbkv = self.torch, self.rbkv
         n = len(self.cycle)
+        # at least two buffer sets, so that one pass's copies overlap the
+        # next pass's compute also when the cycle has a single pass
+        nsets = max(2, n)
         if not hasattr(self, "e2e_sets"):
             self.e2e_sets = []
-            for (q, k, v, o) in self.inputs:
+            for j in range(nsets):
+                q, k, v, o = self.inputs[j % n]
                 parts = (q, k, v)
                 flat = torch.empty(sum(t.numel() for t in parts), dtype=q.dtype,
                                    device=q.device)
@@ -453,44 +457,44 @@ class GpuRunner:
                 o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
                 self.e2e_sets.append((flat, views, o_dev, host_flat, o_host))
             self.cs_in, self.cs_out = torch.cuda.Stream(), torch.cuda.Stream()
-            self.ev_in = [torch.cuda.Event() for _ in range(n)]
-            self.ev_done = [torch.cuda.Event() for _ in range(n)]
-            self.ev_out = [torch.cuda.Event() for _ in range(n)]
+            self.ev_in = [torch.cuda.Event() for _ in range(nsets)]
+            self.ev_done = [torch.cuda.Event() for _ in range(nsets)]
+            self.ev_out = [torch.cuda.Event() for _ in range(nsets)]
         comp = self.stream
 
         def copy_in(i):
-            kpos = i % n
-            flat, _, _, host_flat, _ = self.e2e_sets[kpos]
-            self.cs_in.wait_event(self.ev_done[kpos])     # the set's last pass is done
+            b = i % nsets
+            flat, _, _, host_flat, _ = self.e2e_sets[b]
+            self.cs_in.wait_event(self.ev_done[b])        # the set's last pass is done
             with torch.cuda.stream(self.cs_in):
                 flat.copy_(host_flat, non_blocking=True)
-            self.ev_in[kpos].record(self.cs_in)
+            self.ev_in[b].record(self.cs_in)
 
         tokens = 0
         copy_in(first)
         for i in range(first, first + count):
-            kpos = i % n
+            kpos, b = i % n, i % nsets
             if i + 1 < first + count:
                 copy_in(i + 1)
-            _, (q, k, v), o, _, o_host = self.e2e_sets[kpos]
+            _, (q, k, v), o, _, o_host = self.e2e_sets[b]
             p = self.comp.compose(self.scn.budget, self.scn.max_chunk, self.cycle[kpos])
-            comp.wait_event(self.ev_in[kpos])
-            comp.wait_event(self.ev_out[kpos])              # O of the set copied out
+            comp.wait_event(self.ev_in[b])
+            comp.wait_event(self.ev_out[b])                 # O of the set copied out
             rbkv.kv_append(p, k, v, self.kc, self.vc, stream=self.h_stream)
             rbkv.ragged_attention(p, q, self.kc, self.vc, o=o, workspace=self.ws,
                                   stream=self.h_stream)
-            self.ev_done[kpos].record(comp)
-            self.cs_out.wait_event(self.ev_done[kpos])
+            self.ev_done[b].record(comp)
+            self.cs_out.wait_event(self.ev_done[b])
             with torch.cuda.stream(self.cs_out):
                 o_host.copy_(o, non_blocking=True)
-            self.ev_out[kpos].record(self.cs_out)
+            self.ev_out[b].record(self.cs_out)
             self.pending.append(p)
             if kpos == n - 1:
                 for pp in reversed(self.pending):
                     self.comp.rollback(pp)
                 self.pending.clear()
             tokens += self.T[kpos]
-        comp.wait_event(self.ev_out[(first + count - 1) % n])
+        comp.wait_event(self.ev_out[(first + count - 1) % nsets])
         return tokens
 
     def work_of(self, first, count):
