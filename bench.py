@@ -1132,6 +1132,16 @@ def run_trace_bench(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
+def sample_row(i, T):
+    """The i-th row (0 <= i < T) a sampled oracle pass computes: rows in a
+    stride permutation of the pass (the stride is odd, near 0.618 T and prime
+    to T), so that a short sample spreads over prompt rows and decode rows
+    alike instead of taking the pass's first rows."""
+    stride = next(d for d in range(max(1, int(T * 0.618)) | 1, 2 * T + 2, 2)
+                  if math.gcd(d, T) == 1)
+    return (i * stride) % T
+
+
 class OracleRunner:
     """The fp64 oracle driven through the same cycle of passes (rolled back on
     the oracle composer after each cycle).
@@ -1189,16 +1199,11 @@ class OracleRunner:
         H = self.shape.num_heads_q
         T = m.num_tokens
         total = T * H
-        # rows in a stride permutation of the pass (the stride is odd and
-        # prime to T), so that a short sample spreads over prompt rows and
-        # decode rows alike instead of taking the pass's first rows
-        stride = next(d for d in range(max(1, int(T * 0.618)) | 1, 2 * T + 2, 2)
-                      if math.gcd(d, T) == 1) if T else 1
         done = 0
         while done < pairs and total:
             c = self.cursor % total
             i, h0 = divmod(c, H)
-            t = (i * stride) % T
+            t = sample_row(i, T)
             n = min(pairs - done, H - h0)
             self.oracle.blocked_attention(m, q, self.kc, self.vc, H, tokens=[t],
                                           heads=range(h0, h0 + n))

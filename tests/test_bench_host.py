@@ -1,6 +1,6 @@
 """Host-side helpers of the benchmark (CPU only): the oracle baseline's start
-barrier and all-cores aggregate, and the rule that recorded DRAM traffic is
-reported only for the kernel source it was captured on."""
+barrier, all-cores aggregate and row sampling, and the rule that recorded DRAM
+traffic is reported only for the kernel source it was captured on."""
 import os
 import types
 
@@ -55,3 +55,15 @@ def test_traffic_is_reported_only_for_the_captured_source(monkeypatch):
 
 def test_cpu_model_is_named():
     assert bench.cpu_model()
+
+
+def test_sampled_rows_are_a_permutation_spread_over_the_pass():
+    """The oracle sample walks a pass's rows in a stride permutation: every
+    row exactly once per T rows, and the first few rows already spread over
+    the pass (its first and last quarters both reached)."""
+    for T in (1, 2, 7, 64, 512, 2048, 2111, 12288):
+        rows = [bench.sample_row(i, T) for i in range(T)]
+        assert sorted(rows) == list(range(T)), T
+        if T >= 64:
+            head = rows[:8]
+            assert min(head) < T // 4 and max(head) >= 3 * T // 4, (T, head)
