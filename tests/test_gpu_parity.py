@@ -22,7 +22,9 @@ def _ok(r, tight=False):
     assert r["mean_abs"] <= tol[1], r["mean_abs"]
 
 
-@pytest.mark.parametrize("split", [None, 16, 32, 64])
+# forced split lengths: one key block (the most splits), two splits of the
+# longest context, and one split of every context (1 << 20 keys)
+@pytest.mark.parametrize("split", [None, 16, 32, 64, 1 << 20])
 def test_tiny_fp32_all_outputs(rbkv, split):
     (r,) = run_scenario(rbkv, workloads.tiny(), split_keys=split)
     assert r["tokens"] == 64
@@ -34,7 +36,7 @@ def test_tiny_fp32_all_outputs(rbkv, split):
 
 @pytest.mark.parametrize("name,factor", [("llama2_7b", 8), ("decode_stress", 16),
                                          ("mistral_7b", 8)])
-@pytest.mark.parametrize("split", [None, 64, 256])
+@pytest.mark.parametrize("split", [None, 64, 256, 1 << 20])
 def test_scaled_scenarios_all_outputs(rbkv, name, factor, split):
     scn = workloads.scaled(workloads.SCENARIOS[name](0), factor)
     (r,) = run_scenario(rbkv, scn, split_keys=split)
@@ -42,6 +44,8 @@ def test_scaled_scenarios_all_outputs(rbkv, name, factor, split):
     assert r["pair"].cache_equal()
     plan = r["plan"]
     assert plan["decode_items"] > 0
+    if split == 1 << 20:
+        assert plan["max_splits"] == 1, plan   # every decode row in one piece
     if name != "decode_stress":
         # the scaled pass keeps its prompt chunks, on the tensor-core kernel
         assert plan["chunk_rows"] > 0 and plan["chunk_tiles"] > 0, plan
