@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define RBKV_ABI_VERSION 2
+#define RBKV_ABI_VERSION 3
 
 typedef enum {
   RBKV_OK = 0,
@@ -130,6 +130,12 @@ typedef struct {
   int32_t chunk_steps_max;    /* the most of it that one CTA of the persistent
                                  chunk grid walks, after the items' placement
                                  was balanced over min(items, SMs) CTAs */
+  int32_t decode_grid;        /* CTAs of the persistent decode grid */
+  int32_t decode_keys_total;  /* keys the decode-kernel units cover (each unit:
+                                 its key range; a KV head's keys count once
+                                 per head) */
+  int32_t decode_keys_max;    /* the most of them one CTA of the decode grid
+                                 walks, after the units' placement */
 } rbkv_plan_info;
 
 /* Library ABI version (RBKV_ABI_VERSION). */

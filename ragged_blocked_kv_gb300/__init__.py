@@ -61,7 +61,8 @@ class _PlanInfo(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_sms", "decode_rows", "decode_items", "max_splits", "split_keys", "partials",
         "chunk_rows", "chunk_tiles", "generic_items", "fast_decode", "fast_chunk",
-        "chunk_items", "chunk_single", "chunk_steps_total", "chunk_steps_max")]
+        "chunk_items", "chunk_single", "chunk_steps_total", "chunk_steps_max",
+        "decode_grid", "decode_keys_total", "decode_keys_max")]
 
 
 class _FrameCaps(C.Structure):

@@ -174,6 +174,7 @@ struct Plan {
   std::vector<ChunkItem> chunk_items;
   std::vector<CombineRow> combine;
   int64_t chunk_steps_total = 0, chunk_steps_max = 0;
+  int64_t decode_keys_total = 0, decode_keys_max = 0;
   int32_t n_parts = 0;
   int32_t decode_grid = 0;
   int32_t decode_packed = 0;  // some decode units pack several prompt rows
@@ -241,6 +242,13 @@ void split_keys(int32_t n_keys, int32_t split, int32_t gran, std::vector<int32_t
   bounds.push_back(n_keys);
 }
 
+// The snake deal of decode units is refined when there are at most this many
+// per CTA (more of them even out under the snake deal alone), a unit costing
+// its keys plus this many for its start-up and merge (about 0.7 us of a CTA
+// streaming about 45 keys a microsecond).
+constexpr int32_t kDecodeBalanceUnits = 4;
+constexpr int32_t kDecodeUnitStartKeys = 32;
+
 // Reorder `items` (sorted longest first) so that a persistent grid of G CTAs,
 // CTA c taking items c, c+G, c+2G, ..., receives them in snake order: round r
 // hands sorted items r*G .. r*G+G-1 to CTAs 0..G-1 on even rounds and to
@@ -257,63 +265,100 @@ void snake_order(std::vector<WorkItem>& items, int32_t G) {
   items.swap(out);
 }
 
-// Place chunk work items (sorted longest first) so that the persistent chunk
-// grid of G CTAs, which walks them in snake order (CTA b takes, in round k,
-// position k*G + b on even rounds and k*G + G-1-b on odd ones), ends with
-// nearly equal work per CTA.  Snake dealing alone leaves the CTAs of a last,
-// partial round one item above the rest; here the snake assignment is the
-// start, and items are swapped one for one (so every CTA keeps its number of
-// positions) between the most and the least loaded CTA while a swap narrows
-// their gap.  Each CTA then takes its items longest first.  `cost` is an
-// item's work in key-tile steps; returns the most work one CTA gets.
-int64_t balance_chunk_items(std::vector<ChunkItem>& items, int32_t G,
-                            const std::vector<int32_t>& cost) {
+// Even out the work of a persistent grid of G CTAs in which CTA cta_of(pos)
+// walks position `pos` of `items`.  The given placement is the start (snake
+// dealing of items sorted longest first leaves the CTAs of a last, partial
+// round one item above the rest, and with few items per CTA the busiest about
+// a tenth above the mean); items are then swapped one for one (so every CTA
+// keeps its number of positions) between the most and the least loaded CTA
+// while a swap narrows their gap, and each CTA takes its items costliest
+// first.  `cost[pos]` is the work of the item at `pos`; returns the most work
+// one CTA gets.  A few flat arrays, no allocation per CTA: the planner runs
+// for every pass.
+template <class T, class CtaOf>
+int64_t balance_items(std::vector<T>& items, int32_t G, const std::vector<int32_t>& cost,
+                      CtaOf cta_of) {
   const size_t n = items.size();
   if (G <= 0 || n <= (size_t)G)
     return n ? (int64_t)*std::max_element(cost.begin(), cost.end()) : 0;
-  auto cta_of = [&](size_t pos) -> int32_t {
-    const size_t k = pos / G, i = pos % G;
-    return (int32_t)((k & 1) ? G - 1 - i : i);
-  };
-  std::vector<std::vector<int32_t>> bins(G);   // item indices of each CTA
+  // slot[start[b] ..] = the items of CTA b (indices into `items`)
+  std::vector<int32_t> start(G + 1, 0), fill(G, 0), slot(n);
   std::vector<int64_t> load(G, 0);
+  for (size_t pos = 0; pos < n; ++pos) ++start[cta_of(pos) + 1];
+  for (int32_t b = 0; b < G; ++b) start[b + 1] += start[b];
   for (size_t pos = 0; pos < n; ++pos) {
     const int32_t b = cta_of(pos);
-    bins[b].push_back((int32_t)pos);
+    slot[start[b] + fill[b]++] = (int32_t)pos;
     load[b] += cost[pos];
   }
-  for (int iter = 0; iter < 8 * G; ++iter) {
-    int32_t hi = 0, lo = 0;
-    for (int32_t b = 1; b < G; ++b) {
-      if (load[b] > load[hi]) hi = b;
-      if (load[b] < load[lo]) lo = b;
+  // the most and the least loaded CTA (ties: lowest index) from two heaps of
+  // (load, CTA) entries; an entry whose load is no longer the CTA's is stale
+  // and dropped when it comes to the top
+  using Entry = std::pair<int64_t, int32_t>;
+  std::vector<Entry> most, least;   // keys (load, -b) and (load, b)
+  most.reserve(G + 256);
+  least.reserve(G + 256);
+  const auto greater = [](const Entry& x, const Entry& y) { return x > y; };
+  for (int32_t b = 0; b < G; ++b) {
+    most.push_back({load[b], -b});
+    least.push_back({load[b], b});
+  }
+  std::make_heap(most.begin(), most.end());
+  std::make_heap(least.begin(), least.end(), greater);
+  auto top_most = [&]() {
+    while (load[-most.front().second] != most.front().first) {
+      std::pop_heap(most.begin(), most.end());
+      most.pop_back();
     }
+    return -most.front().second;
+  };
+  auto top_least = [&]() {
+    while (load[least.front().second] != least.front().first) {
+      std::pop_heap(least.begin(), least.end(), greater);
+      least.pop_back();
+    }
+    return least.front().second;
+  };
+  for (int iter = 0; iter < 8 * G; ++iter) {
+    const int32_t hi = top_most(), lo = top_least();
     const int64_t gap = load[hi] - load[lo];
-    int best_a = -1, best_b = -1;
+    int32_t best_a = -1, best_b = -1;
     int64_t best_d = 0;
-    for (size_t a = 0; a < bins[hi].size(); ++a)
-      for (size_t c = 0; c < bins[lo].size(); ++c) {
-        const int64_t d = (int64_t)cost[bins[hi][a]] - cost[bins[lo][c]];
+    for (int32_t a = start[hi]; a < start[hi + 1]; ++a)
+      for (int32_t c = start[lo]; c < start[lo + 1]; ++c) {
+        const int64_t d = (int64_t)cost[slot[a]] - cost[slot[c]];
         if (d <= 0 || d >= gap) continue;
         if (best_a < 0 || std::llabs(gap - 2 * d) < std::llabs(gap - 2 * best_d)) {
-          best_a = (int)a;
-          best_b = (int)c;
+          best_a = a;
+          best_b = c;
           best_d = d;
         }
       }
     if (best_a < 0) break;
-    std::swap(bins[hi][best_a], bins[lo][best_b]);
+    std::swap(slot[best_a], slot[best_b]);
     load[hi] -= best_d;
     load[lo] += best_d;
+    for (const int32_t b : {hi, lo}) {
+      most.push_back({load[b], -b});
+      std::push_heap(most.begin(), most.end());
+      least.push_back({load[b], b});
+      std::push_heap(least.begin(), least.end(), greater);
+    }
   }
-  std::vector<ChunkItem> out(n);
-  std::vector<size_t> next(G, 0);
+  // each CTA's items costliest first (insertion sort: a few items each;
+  // equal costs keep their order)
   for (int32_t b = 0; b < G; ++b)
-    std::stable_sort(bins[b].begin(), bins[b].end(),
-                     [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+    for (int32_t i = start[b] + 1; i < start[b + 1]; ++i) {
+      const int32_t v = slot[i];
+      int32_t j = i;
+      for (; j > start[b] && cost[slot[j - 1]] < cost[v]; --j) slot[j] = slot[j - 1];
+      slot[j] = v;
+    }
+  std::vector<T> out(n);
+  std::fill(fill.begin(), fill.end(), 0);
   for (size_t pos = 0; pos < n; ++pos) {
     const int32_t b = cta_of(pos);
-    out[pos] = items[bins[b][next[b]++]];
+    out[pos] = items[slot[start[b] + fill[b]++]];
   }
   items.swap(out);
   return *std::max_element(load.begin(), load.end());
@@ -548,13 +593,34 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
       cost[i] = c;
     }
     for (int32_t c : cost) pl.chunk_steps_total += c;
-    pl.chunk_steps_max = balance_chunk_items(
-        pl.chunk_items, (int32_t)std::min<int64_t>((int64_t)cost.size(), std::max(1, num_sms)),
-        cost);
+    // the chunk grid walks its positions in snake order: CTA b takes, in
+    // round k, position k*G + b on even rounds and k*G + G-1-b on odd ones
+    const int32_t G = (int32_t)std::min<int64_t>((int64_t)cost.size(), std::max(1, num_sms));
+    pl.chunk_steps_max = balance_items(pl.chunk_items, G, cost, [G](size_t pos) -> int32_t {
+      const size_t k = pos / G, i = pos % G;
+      return (int32_t)((k & 1) ? G - 1 - i : i);
+    });
   }
   int32_t grid =(int32_t)std::min<int64_t>((int64_t)decode.size(),
                                             (int64_t)std::max(1, num_sms) * decode_ctas_per_sm(s));
-  if (grid > 0) snake_order(decode, grid);
+  if (grid > 0) {
+    // the decode grid walks positions c, c + G, c + 2G, ... (CTA c); the
+    // snake deal is the placement, refined when there are few units per CTA
+    snake_order(decode, grid);
+    if (decode.size() <= (size_t)kDecodeBalanceUnits * grid) {
+      std::vector<int32_t> cost(decode.size());
+      for (size_t i = 0; i < decode.size(); ++i)
+        cost[i] = decode[i].key_end - decode[i].key_begin + kDecodeUnitStartKeys;
+      balance_items(decode, grid, cost, [grid](size_t pos) { return (int32_t)(pos % grid); });
+    }
+    std::vector<int64_t> keys(grid, 0);
+    for (size_t i = 0; i < decode.size(); ++i) {
+      const int64_t k = decode[i].key_end - decode[i].key_begin;
+      keys[i % grid] += k;
+      pl.decode_keys_total += k;
+    }
+    pl.decode_keys_max = *std::max_element(keys.begin(), keys.end());
+  }
   pl.decode_grid = grid;
   pl.decode.swap(decode);
   pl.generic.swap(generic);
@@ -572,6 +638,9 @@ Plan make_plan(const rbkv_pass& p, int32_t num_sms) {
   in.chunk_single = pl.chunk_single;
   in.chunk_steps_total = (int32_t)std::min<int64_t>(pl.chunk_steps_total, INT32_MAX);
   in.chunk_steps_max = (int32_t)std::min<int64_t>(pl.chunk_steps_max, INT32_MAX);
+  in.decode_grid = pl.decode_grid;
+  in.decode_keys_total = (int32_t)std::min<int64_t>(pl.decode_keys_total, INT32_MAX);
+  in.decode_keys_max = (int32_t)std::min<int64_t>(pl.decode_keys_max, INT32_MAX);
   in.generic_items = (int32_t)pl.generic.size();
   in.fast_decode = fast_decode ? 1 : 0;
   in.fast_chunk = fast_chunk ? 1 : 0;

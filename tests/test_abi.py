@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol(rbkv):
                          capture_output=True, text=True).stdout
     exported = set(re.findall(r"\b(rbkv_[a-z0-9_]+)\b", out))
     assert set(declared_symbols()) <= exported
-    assert L.rbkv_abi_version() == 2
+    assert L.rbkv_abi_version() == 3
 
 
 def test_bad_config_is_rejected_without_a_gpu(rbkv):
