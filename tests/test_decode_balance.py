@@ -61,7 +61,7 @@ def test_random_decode_contexts_within_one_unit(seed):
     comp.compose(sum(ctxs), 0, [(i, c, 0) for i, c in zip(ids, ctxs)])
     p = comp.compose(n, 0, [(i, c, c) for i, c in zip(ids, ctxs)])
     assert p.num_tokens == n
-    for sms in (152, 40):
+    for sms in (152, 40, 3, 1):
         info = p.plan_for_sms(sms)
         assert info["decode_keys_total"] == sum(c + 1 for c in ctxs) * 8
         grid = info["decode_grid"]
